@@ -1,0 +1,218 @@
+"""Pins for the oracle's decoders (CPU only).
+
+* banded == unbanded: the pages' invariant that the layer-wise banded decode
+  keeps whole-image semantics ("Static Layer-Wise VAE Decode", "Semantics and
+  Communication"; "VAEP：VAE 并行解码", 按高度分片，逐层解码).
+* the decoder composed from PyTorch CPU float64 library modules (conv2d,
+  conv3d, group_norm, silu, interpolate, scaled_dot_product_attention) equals
+  the oracle on tiny instances of both families.  This pins each layer's
+  arithmetic and the wiring against a second, independent composition; the
+  wiring's match with the Diffusers modules themselves is unpinned (neither
+  Diffusers nor pretrained weights are available).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import synth
+from oracle import decoder
+
+KL_SMALL = dataclasses.replace(
+    synth.KL_ZIMAGE, mid_channels=16, stage_channels=(16, 16, 8, 8), stage_resnets=(1, 2, 1, 2),
+    stage_up_channels=(16, 16, 8, 0), norm_groups=4)
+WAN_SMALL = dataclasses.replace(
+    synth.WAN, mid_channels=16, stage_channels=(16, 16, 8, 4), stage_resnets=(1, 1, 2, 1),
+    stage_up_channels=(8, 8, 4, 0))
+
+
+def _t(a):
+    return torch.from_numpy(np.asarray(a, dtype=np.float64))
+
+
+def torch_decode_kl(arch, W, z):
+    T = {k: _t(v) for k, v in W.items()}
+    G, eps = arch.norm_groups, arch.eps
+
+    def conv(x, p):
+        w = T[p + ".weight"]
+        return F.conv2d(x, w, T[p + ".bias"], padding=w.shape[-1] // 2)
+
+    def gn(x, p):
+        return F.group_norm(x, G, T[p + ".weight"], T[p + ".bias"], eps)
+
+    def resnet(x, p):
+        h = conv(F.silu(gn(x, p + ".norm1")), p + ".conv1")
+        h = conv(F.silu(gn(h, p + ".norm2")), p + ".conv2")
+        sc = conv(x, p + ".conv_shortcut") if p + ".conv_shortcut.weight" in T else x
+        return sc + h
+
+    def attn(x, p):
+        n, c, h, w = x.shape
+        t = gn(x, p + ".group_norm").reshape(n, c, h * w).transpose(1, 2)
+        q = F.linear(t, T[p + ".to_q.weight"], T[p + ".to_q.bias"])
+        k = F.linear(t, T[p + ".to_k.weight"], T[p + ".to_k.bias"])
+        v = F.linear(t, T[p + ".to_v.weight"], T[p + ".to_v.bias"])
+        o = F.scaled_dot_product_attention(q, k, v)
+        o = F.linear(o, T[p + ".to_out.0.weight"], T[p + ".to_out.0.bias"])
+        return x + o.transpose(1, 2).reshape(n, c, h, w)
+
+    x = conv(_t(z), "conv_in")
+    x = resnet(x, "mid_block.resnets.0")
+    x = attn(x, "mid_block.attentions.0")
+    x = resnet(x, "mid_block.resnets.1")
+    for s in range(len(arch.stage_channels)):
+        for r in range(arch.stage_resnets[s]):
+            x = resnet(x, f"up_blocks.{s}.resnets.{r}")
+        if arch.stage_upsample[s]:
+            x = conv(F.interpolate(x, scale_factor=2, mode="nearest"), f"up_blocks.{s}.upsamplers.0.conv")
+    x = F.silu(gn(x, "conv_norm_out"))
+    return conv(x, "conv_out").numpy()
+
+
+def torch_decode_wan(arch, W, z):
+    """Wan decoder run frame-chunk by frame-chunk with the causal feature cache.
+
+    This follows the original module's streaming protocol (first latent frame
+    alone, then one latent frame per call, a 2-frame cache per causal conv,
+    the time_conv skipped on the first chunk), so it also pins the oracle's
+    whole-sequence reading of that protocol.
+    """
+    T = {k: _t(v) for k, v in W.items()}
+
+    def rms(x, g):
+        return F.normalize(x, dim=1) * (x.shape[1] ** 0.5) * g.view(1, -1, *([1] * (x.ndim - 2)))
+
+    caches = {}
+
+    def cconv(x, p, key):
+        w = T[p + ".weight"]
+        kt, kh = w.shape[2], w.shape[3]
+        prev = caches.get(key)
+        need = kt - 1
+        if need:
+            if prev is None:
+                prev = torch.zeros(x.shape[0], x.shape[1], 0, x.shape[3], x.shape[4], dtype=x.dtype)
+            xin = torch.cat([prev, x], dim=2)
+            xin = F.pad(xin, (0, 0, 0, 0, need - prev.shape[2], 0))
+            caches[key] = xin[:, :, -need:]
+        else:
+            xin = x
+        return F.conv3d(F.pad(xin, (kh // 2,) * 4), w, T[p + ".bias"])
+
+    def resnet(x, p):
+        h = cconv(F.silu(rms(x, T[p + ".norm1.gamma"])), p + ".conv1", p + ".conv1")
+        h = cconv(F.silu(rms(h, T[p + ".norm2.gamma"])), p + ".conv2", p + ".conv2")
+        sc = cconv(x, p + ".conv_shortcut", p + ".sc") if p + ".conv_shortcut.weight" in T else x
+        return sc + h
+
+    def attn(x, p):
+        n, c, t, h, w = x.shape
+        f = x.permute(0, 2, 1, 3, 4).reshape(n * t, c, h, w)
+        f = rms(f, T[p + ".norm.gamma"])
+        qkv = F.conv2d(f, T[p + ".to_qkv.weight"], T[p + ".to_qkv.bias"])
+        qkv = qkv.reshape(n * t, 3 * c, h * w).transpose(1, 2)
+        q, k, v = qkv[..., :c], qkv[..., c:2 * c], qkv[..., 2 * c:]
+        o = F.scaled_dot_product_attention(q, k, v).transpose(1, 2).reshape(n * t, c, h, w)
+        o = F.conv2d(o, T[p + ".proj.weight"], T[p + ".proj.bias"])
+        return x + o.reshape(n, t, c, h, w).permute(0, 2, 1, 3, 4)
+
+    def upsample(x, s, first_chunk):
+        pre = f"up_blocks.{s}.upsamplers.0"
+        if arch.stage_upsample[s] == 2 and not first_chunk:
+            y = cconv(x, pre + ".time_conv", pre + ".time_conv")
+            n, c2, t, h, w = y.shape
+            c = c2 // 2
+            x = torch.stack((y[:, :c], y[:, c:]), dim=3).reshape(n, c, 2 * t, h, w)
+        n, c, t, h, w = x.shape
+        f = x.permute(0, 2, 1, 3, 4).reshape(n * t, c, h, w)
+        f = F.conv2d(F.interpolate(f, scale_factor=2, mode="nearest-exact"), T[pre + ".resample.1.weight"],
+                     T[pre + ".resample.1.bias"], padding=1)
+        return f.reshape(n, t, -1, 2 * h, 2 * w).permute(0, 2, 1, 3, 4)
+
+    def chunk(x, first):
+        x = cconv(x, "conv_in", "conv_in")
+        x = resnet(x, "mid_block.resnets.0")
+        x = attn(x, "mid_block.attentions.0")
+        x = resnet(x, "mid_block.resnets.1")
+        for s in range(len(arch.stage_channels)):
+            for r in range(arch.stage_resnets[s]):
+                x = resnet(x, f"up_blocks.{s}.resnets.{r}")
+            if arch.stage_upsample[s]:
+                x = upsample(x, s, first)
+        x = F.silu(rms(x, T["norm_out.gamma"]))
+        return cconv(x, "conv_out", "conv_out")
+
+    zt = _t(z)
+    outs = [chunk(zt[:, :, i:i + 1], i == 0) for i in range(zt.shape[2])]
+    return torch.cat(outs, dim=2).numpy()
+
+
+@pytest.fixture(scope="module")
+def kl_small():
+    W = synth.make_weights(KL_SMALL, "fp32", seed=5)
+    z = synth.make_latent((2, 16, 7, 5), "fp32", seed=6)
+    return W, z, decoder.decode(KL_SMALL, W, z)
+
+
+@pytest.fixture(scope="module")
+def wan_small():
+    W = synth.make_weights(WAN_SMALL, "fp32", seed=7)
+    z = synth.make_latent((1, 16, 3, 5, 4), "fp32", seed=8)
+    return W, z, decoder.decode(WAN_SMALL, W, z)
+
+
+def test_kl_decoder_matches_torch_composition(kl_small):
+    W, z, y = kl_small
+    assert y.shape == decoder.output_shape(KL_SMALL, z.shape)
+    np.testing.assert_allclose(y, torch_decode_kl(KL_SMALL, W, z), rtol=1e-10, atol=1e-10)
+
+
+def test_wan_decoder_matches_streaming_torch_composition(wan_small):
+    W, z, y = wan_small
+    assert y.shape == decoder.output_shape(WAN_SMALL, z.shape)
+    np.testing.assert_allclose(y, torch_decode_wan(WAN_SMALL, W, z), rtol=1e-10, atol=1e-10)
+
+
+def test_tiny_workload_matches_torch_composition():
+    w = synth.WORKLOADS["kl_tiny_fp32"]
+    W = synth.make_weights(w.arch, w.dtype)
+    z = synth.make_latent(w.latent_shape, w.dtype)
+    np.testing.assert_allclose(decoder.decode(w.arch, W, z), torch_decode_kl(w.arch, W, z),
+                               rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("n_bands", [2, 3, 7])
+def test_kl_banded_equals_unbanded(kl_small, n_bands):
+    W, z, y = kl_small
+    yb = decoder.decode(KL_SMALL, W, z, n_bands)
+    np.testing.assert_allclose(yb, y, rtol=0, atol=1e-12 * np.abs(y).max())
+
+
+@pytest.mark.parametrize("n_bands", [2, 5])
+def test_wan_banded_equals_unbanded(wan_small, n_bands):
+    W, z, y = wan_small
+    yb = decoder.decode(WAN_SMALL, W, z, n_bands)
+    np.testing.assert_allclose(yb, y, rtol=0, atol=1e-12 * np.abs(y).max())
+
+
+def test_banded_without_halo_differs():
+    """A banded conv that used zero padding at interior cuts (no halo) would
+    differ from the unbanded decode at the band boundaries: the halo matters."""
+    W, z = synth.make_weights(KL_SMALL, "fp32", seed=5), synth.make_latent((1, 16, 6, 5), "fp32", seed=9)
+    from oracle import ops
+    x = z.astype(np.float64)
+    w, b = W["conv_in.weight"], W["conv_in.bias"]
+    whole = ops.conv2d_same(x, w, b)
+    cut = np.concatenate([ops.conv2d_same(x[:, :, :3], w, b), ops.conv2d_same(x[:, :, 3:], w, b)], axis=2)
+    halo = decoder.Banded(2).join(decoder.Banded(2).conv(decoder.Banded(2).split(x), w, b))
+    assert np.abs(cut - whole)[:, :, 2:4].max() > 1e-3
+    np.testing.assert_allclose(halo, whole, rtol=0, atol=1e-13)
+
+
+def test_too_many_bands_rejected():
+    W, z, _ = None, synth.make_latent((1, 16, 3, 4), "fp32"), None
+    with pytest.raises(ValueError):
+        decoder.decode(KL_SMALL, synth.make_weights(KL_SMALL, "fp32"), z, 4)
