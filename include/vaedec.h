@@ -1,0 +1,176 @@
+/*
+ * vaedec -- layerwise height-row-band VAE decode on one GPU (sm_103a).
+ *
+ * What it computes.  A diffusion VAE decoder (an AutoencoderKL-style 2D CNN or a
+ * WanDecoder3d-style causal 3D CNN) run layer by layer over height row bands, as
+ * ChituDiffusion's pages "VAEP：VAE 并行解码" (section 按高度分片，逐层解码) and
+ * "Static Layer-Wise VAE Decode" (table "Semantics and Communication") define it:
+ *   - the latent height is cut into disjoint row bands; uneven bands keep their
+ *     lengths, and every 2x upsample doubles each band's rows;
+ *   - every conv reads kernel-radius halo rows of the neighbouring band, with zero
+ *     padding only at the global image edges (section 卷积：交换边界行);
+ *   - GroupNorm merges per-part central moments with the element-count-weighted
+ *     rule mean = sum w_i mean_i, var = sum w_i (var_i + (mean_i - mean)^2), in
+ *     fp32 (section GroupNorm：合并全局统计量);
+ *   - mid-block attention keeps Q band-local and attends over all K/V
+ *     (section Attention：本地 Q，全局 K/V);
+ *   - SiLU, channel RMSNorm and nearest-2x upsample are local.
+ * On one GPU every band lives in the same device memory: halo rows are read in
+ * place, statistics are merged by a kernel, K/V are already resident.  The result
+ * equals the unbanded decode, and on this library it is bit-identical for every
+ * band count.
+ *
+ * Threading and streams.  A handle may be used from one host thread at a time.
+ * Calls are stream-ordered and asynchronous unless stated otherwise.  Two decodes
+ * on one handle must be ordered on the same stream (they share the handle's
+ * workspace).
+ *
+ * Errors.  Every entry point returns a vaedec_status; the message of the calling
+ * thread's last failure is available from vaedec_last_error().  Kernel-side
+ * failures (a bounded wait that ran out) are recorded in a device status word and
+ * reported by vaedec_sync() or the next synchronous call.
+ */
+#ifndef VAEDEC_H_
+#define VAEDEC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VAEDEC_ABI_VERSION 1
+#define VAEDEC_MAX_STAGES 6
+
+typedef struct vaedec vaedec_t; /* opaque: device weights + workspace */
+
+typedef enum {
+  VAEDEC_OK = 0,
+  VAEDEC_ERR_INVALID_ARG = 1, /* bad shape, dtype, band count, pointer, size */
+  VAEDEC_ERR_UNSUPPORTED = 2, /* geometry outside the method's scope (see below) */
+  VAEDEC_ERR_OOM = 3,         /* device allocation failed */
+  VAEDEC_ERR_CUDA = 4,        /* a CUDA call failed (message holds the CUDA error) */
+  VAEDEC_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (device status word) */
+  VAEDEC_ERR_STOPPED = 6      /* debug run stopped at the requested op (not a failure) */
+} vaedec_status;
+
+enum { VAEDEC_FAMILY_KL2D = 1, VAEDEC_FAMILY_WAN3D = 2 };
+enum { VAEDEC_DTYPE_F32 = 1, VAEDEC_DTYPE_BF16 = 2 };
+enum { VAEDEC_UP_NONE = 0, VAEDEC_UP_SPATIAL = 1, VAEDEC_UP_SPATIOTEMPORAL = 2 };
+
+/* A named HOST tensor, contiguous row-major, read only during vaedec_create. */
+typedef struct {
+  const char* name;   /* Diffusers state-dict key, e.g. "mid_block.resnets.0.conv1.weight" */
+  const void* data;   /* host pointer */
+  int dtype;          /* VAEDEC_DTYPE_F32 or VAEDEC_DTYPE_BF16 */
+  int ndim;
+  int64_t shape[5];
+} vaedec_tensor;
+
+/*
+ * Decoder description.  conv_in maps latent_channels -> mid_channels; the mid block
+ * is [resnet, attention, resnet] at mid_channels; stage s runs stage_resnets[s]
+ * residual blocks to stage_channels[s] channels, then an optional upsample whose
+ * 3x3 conv maps to stage_up_channels[s]; a final norm, SiLU and 3x3 conv_out map to
+ * out_channels.  KL2D uses GroupNorm(norm_groups, eps); WAN3D uses channel RMSNorm
+ * and causal 3x3x3 convs.
+ * max_latent = {B, T, H, W} upper bounds (T = 1 for KL2D): the workspace is sized
+ * for them once at create time.
+ */
+typedef struct {
+  int family;
+  int dtype; /* bf16: tensor-core path; f32: CUDA-core fp32 path (checks only) */
+  int latent_channels, mid_channels, out_channels;
+  int n_stages;
+  int stage_channels[VAEDEC_MAX_STAGES];
+  int stage_resnets[VAEDEC_MAX_STAGES];
+  int stage_upsample[VAEDEC_MAX_STAGES]; /* VAEDEC_UP_* */
+  int stage_up_channels[VAEDEC_MAX_STAGES];
+  int norm_groups;
+  float eps;
+  int64_t max_latent[4];
+} vaedec_config;
+
+/*
+ * Create a decoder on the current CUDA device.  Copies and repacks every weight
+ * (host memory, any of the two dtypes) into device layouts owned by the handle and
+ * allocates the workspace for config->max_latent.  Synchronous.
+ * Errors: INVALID_ARG (missing/extra-shaped weight, bad config), UNSUPPORTED
+ * (channel counts the kernels cannot tile), OOM, CUDA.  On error *out is NULL and
+ * nothing is leaked.
+ */
+vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* weights, int n_weights,
+                            vaedec_t** out);
+
+/* Release every device allocation of the handle.  Synchronises the device first.  NULL is a no-op. */
+void vaedec_destroy(vaedec_t* h);
+
+/* Decoded output shape for a latent shape (ndim 4: B,C,H,W; ndim 5: B,C,T,H,W). */
+vaedec_status vaedec_output_shape(const vaedec_t* h, const int64_t* latent_shape, int ndim, int64_t* out_shape);
+
+/* Bytes of device workspace the handle owns (weights excluded). */
+vaedec_status vaedec_workspace_bytes(const vaedec_t* h, size_t* bytes);
+
+/*
+ * Decode on `stream` (a cudaStream_t; NULL = legacy default stream).
+ * latent: DEVICE pointer, channels-first (NCHW or NCTHW), contiguous, model dtype.
+ * out:    DEVICE pointer, caller-allocated, channels-first, model dtype, shape from
+ *         vaedec_output_shape.
+ * n_bands in [1, latent H]: band b holds floor(H/n) latent rows, the first H mod n
+ * bands one more.  The output does not depend on n_bands (bit-identical).
+ * Asynchronous: returns after enqueueing.  Errors: INVALID_ARG (shape above
+ * max_latent, wrong ndim, channel mismatch, n_bands out of range, NULL pointer),
+ * CUDA (launch failure).
+ */
+vaedec_status vaedec_decode(vaedec_t* h, const void* latent, const int64_t* latent_shape, int ndim, void* out,
+                            int n_bands, void* stream);
+
+/*
+ * Same as vaedec_decode with HOST buffers: copies the latent host->device, decodes,
+ * copies the output device->host, and synchronises `stream` before returning.
+ * Host buffers should be pinned for full copy bandwidth.  Also reports kernel-side
+ * failures (TIMEOUT).
+ */
+vaedec_status vaedec_decode_host(vaedec_t* h, const void* latent_host, const int64_t* latent_shape, int ndim,
+                                 void* out_host, int n_bands, void* stream);
+
+/* Synchronise `stream` and report the device status word (TIMEOUT if a kernel gave up waiting); clears it. */
+vaedec_status vaedec_sync(vaedec_t* h, void* stream);
+
+/* Message of the calling thread's last failure ("" if none). */
+const char* vaedec_last_error(void);
+
+/* Number of kernel launches this handle has enqueued since vaedec_create. */
+vaedec_status vaedec_launch_count(const vaedec_t* h, uint64_t* n);
+
+/* ---- Per-op timing (profiling) -------------------------------------------------------
+ * When enabled, each op of a decode (see the inspection calls below) is bracketed by
+ * CUDA events recorded on the decode stream; the events cost a few microseconds of
+ * host time per op and nothing on the device.  vaedec_profile_read waits for the last
+ * profiled decode's events and writes each op's device milliseconds, in op order.
+ */
+vaedec_status vaedec_profile_enable(vaedec_t* h, int enable);
+vaedec_status vaedec_profile_read(vaedec_t* h, float* ms, int max_ops, int* n_ops);
+
+/* ---- Inspection (tests and profiling) ------------------------------------------------
+ * The decode is a fixed list of ops (latent layout, conv, groupnorm, rmsnorm,
+ * attention block, temporal upsample).  These calls describe that list for a latent
+ * shape and band count, and run the decode up to one op, copying the op's input,
+ * auxiliary input (a conv's residual, else nothing) and output activations into
+ * caller DEVICE buffers (channels-last [B][T][H][W][C] in the model dtype, except
+ * the final conv's channels-first output).
+ */
+vaedec_status vaedec_debug_num_ops(vaedec_t* h, const int64_t* latent_shape, int ndim, int n_bands, int* n_ops);
+/* One line "key=value ..." describing op `op`; INVALID_ARG if buf is too small. */
+vaedec_status vaedec_debug_op_desc(vaedec_t* h, const int64_t* latent_shape, int ndim, int n_bands, int op,
+                                   char* buf, int buf_len);
+/* Runs ops [0, op], copies, synchronises `stream`, returns OK (or the first error). */
+vaedec_status vaedec_debug_run_until(vaedec_t* h, const void* latent, const int64_t* latent_shape, int ndim,
+                                     int n_bands, int op, void* dst_in, size_t in_bytes, void* dst_aux,
+                                     size_t aux_bytes, void* dst_out, size_t out_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VAEDEC_H_ */

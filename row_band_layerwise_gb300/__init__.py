@@ -1,0 +1,273 @@
+"""Python binding of the ``vaedec`` C ABI (``include/vaedec.h``).
+
+Argument marshalling only: every step of the decode runs in the library's CUDA
+kernels.  PyTorch is used by callers for device memory and streams; this module
+accepts ``torch`` tensors for device buffers and numpy arrays for host weights.
+If the shared library has not been built, :func:`load_library` raises -- there
+is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Iterable, Optional, Sequence, Tuple
+
+import numpy as np
+
+from .build import lib_path
+
+__all__ = ["Decoder", "VaedecError", "load_library", "EXPORTED_SYMBOLS", "STATUS_NAMES"]
+
+FAMILY = {"kl2d": 1, "wan3d": 2}
+DTYPE = {"fp32": 1, "bf16": 2}
+MAX_STAGES = 6
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OOM", 4: "CUDA", 5: "TIMEOUT", 6: "STOPPED"}
+
+EXPORTED_SYMBOLS = (
+    "vaedec_create", "vaedec_destroy", "vaedec_output_shape", "vaedec_workspace_bytes",
+    "vaedec_decode", "vaedec_decode_host", "vaedec_sync", "vaedec_last_error",
+    "vaedec_launch_count", "vaedec_profile_enable", "vaedec_profile_read",
+    "vaedec_debug_num_ops", "vaedec_debug_op_desc", "vaedec_debug_run_until",
+)
+
+
+class VaedecError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class _Tensor(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("data", ctypes.c_void_p), ("dtype", ctypes.c_int),
+                ("ndim", ctypes.c_int), ("shape", ctypes.c_int64 * 5)]
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [("family", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("latent_channels", ctypes.c_int), ("mid_channels", ctypes.c_int),
+                ("out_channels", ctypes.c_int), ("n_stages", ctypes.c_int),
+                ("stage_channels", ctypes.c_int * MAX_STAGES),
+                ("stage_resnets", ctypes.c_int * MAX_STAGES),
+                ("stage_upsample", ctypes.c_int * MAX_STAGES),
+                ("stage_up_channels", ctypes.c_int * MAX_STAGES),
+                ("norm_groups", ctypes.c_int), ("eps", ctypes.c_float),
+                ("max_latent", ctypes.c_int64 * 4)]
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the built library (raises if it is missing)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or lib_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"vaedec library not built ({p} missing): run "
+                           "`python -m row_band_layerwise_gb300.build`")
+    lib = ctypes.CDLL(p)
+    vp, i64p, i = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_int
+    lib.vaedec_create.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Tensor), i, ctypes.POINTER(vp)]
+    lib.vaedec_destroy.argtypes = [vp]
+    lib.vaedec_destroy.restype = None
+    lib.vaedec_output_shape.argtypes = [vp, i64p, i, i64p]
+    lib.vaedec_workspace_bytes.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
+    lib.vaedec_decode.argtypes = [vp, vp, i64p, i, vp, i, vp]
+    lib.vaedec_decode_host.argtypes = [vp, vp, i64p, i, vp, i, vp]
+    lib.vaedec_sync.argtypes = [vp, vp]
+    lib.vaedec_last_error.restype = ctypes.c_char_p
+    lib.vaedec_last_error.argtypes = []
+    lib.vaedec_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
+    lib.vaedec_profile_enable.argtypes = [vp, i]
+    lib.vaedec_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i, ctypes.POINTER(i)]
+    lib.vaedec_debug_num_ops.argtypes = [vp, i64p, i, i, ctypes.POINTER(i)]
+    lib.vaedec_debug_op_desc.argtypes = [vp, i64p, i, i, i, ctypes.c_char_p, i]
+    lib.vaedec_debug_run_until.argtypes = [vp, vp, i64p, i, i, i, vp, ctypes.c_size_t, vp, ctypes.c_size_t,
+                                           vp, ctypes.c_size_t, vp]
+    for name in EXPORTED_SYMBOLS:
+        if name not in ("vaedec_destroy", "vaedec_last_error"):
+            getattr(lib, name).restype = ctypes.c_int
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _check(lib, status: int) -> None:
+    if status != 0:
+        raise VaedecError(status, lib.vaedec_last_error().decode(errors="replace"))
+
+
+def _shape_arg(shape: Sequence[int]):
+    return (ctypes.c_int64 * len(shape))(*[int(s) for s in shape])
+
+
+def make_config(arch, dtype: str, max_latent: Sequence[int]) -> _Config:
+    """Fill a ``vaedec_config`` from an architecture description.
+
+    ``arch`` needs the attributes family, latent_channels, mid_channels,
+    out_channels, stage_channels, stage_resnets, stage_upsample,
+    stage_up_channels, norm_groups and eps; ``max_latent`` is (B, T, H, W).
+    """
+    c = _Config()
+    c.family = FAMILY[arch.family]
+    c.dtype = DTYPE[dtype]
+    c.latent_channels = arch.latent_channels
+    c.mid_channels = arch.mid_channels
+    c.out_channels = arch.out_channels
+    n = len(arch.stage_channels)
+    if n > MAX_STAGES:
+        raise ValueError("too many stages")
+    c.n_stages = n
+    for s in range(n):
+        c.stage_channels[s] = arch.stage_channels[s]
+        c.stage_resnets[s] = arch.stage_resnets[s]
+        c.stage_upsample[s] = arch.stage_upsample[s]
+        c.stage_up_channels[s] = arch.stage_up_channels[s]
+    c.norm_groups = arch.norm_groups
+    c.eps = arch.eps
+    for k in range(4):
+        c.max_latent[k] = int(max_latent[k])
+    return c
+
+
+def _torch():
+    import torch
+    return torch
+
+
+class Decoder:
+    """One decoder handle: device weights plus workspace sized for ``max_latent``."""
+
+    def __init__(self, arch, weights: Dict[str, np.ndarray], dtype: str,
+                 max_latent: Sequence[int], lib_file: Optional[str] = None):
+        self.lib = load_library(lib_file)
+        self.arch = arch
+        self.dtype = dtype
+        self.family = arch.family
+        cfg = make_config(arch, dtype, max_latent)
+        keep = []
+        arr = (_Tensor * len(weights))()
+        for i, (name, w) in enumerate(weights.items()):
+            a = np.ascontiguousarray(w, dtype=np.float32)
+            keep.append(a)
+            arr[i].name = name.encode()
+            arr[i].data = a.ctypes.data
+            arr[i].dtype = DTYPE["fp32"]
+            arr[i].ndim = a.ndim
+            for k in range(a.ndim):
+                arr[i].shape[k] = a.shape[k]
+        handle = ctypes.c_void_p()
+        _check(self.lib, self.lib.vaedec_create(ctypes.byref(cfg), arr, len(weights), ctypes.byref(handle)))
+        self._h = handle
+        del keep
+
+    # ------------------------------------------------------------------ basics
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            self.lib.vaedec_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @property
+    def torch_dtype(self):
+        torch = _torch()
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def output_shape(self, latent_shape: Sequence[int]) -> Tuple[int, ...]:
+        n = len(latent_shape)
+        out = (ctypes.c_int64 * n)()
+        _check(self.lib, self.lib.vaedec_output_shape(self._h, _shape_arg(latent_shape), n, out))
+        return tuple(int(v) for v in out)
+
+    def workspace_bytes(self) -> int:
+        v = ctypes.c_size_t()
+        _check(self.lib, self.lib.vaedec_workspace_bytes(self._h, ctypes.byref(v)))
+        return int(v.value)
+
+    @staticmethod
+    def _stream_ptr(stream) -> int:
+        torch = _torch()
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        return int(stream.cuda_stream)
+
+    # ------------------------------------------------------------------ decode
+    def decode(self, latent, n_bands: int, out=None, stream=None):
+        """Decode a device latent (torch tensor, channels-first, model dtype) on ``stream``."""
+        torch = _torch()
+        if not latent.is_cuda or latent.dtype != self.torch_dtype or not latent.is_contiguous():
+            raise ValueError("latent must be a contiguous CUDA tensor in the model dtype")
+        oshape = self.output_shape(latent.shape)
+        if out is None:
+            out = torch.empty(oshape, dtype=self.torch_dtype, device=latent.device)
+        elif tuple(out.shape) != oshape or out.dtype != self.torch_dtype or not out.is_contiguous():
+            raise ValueError("out has the wrong shape, dtype or layout")
+        _check(self.lib, self.lib.vaedec_decode(self._h, latent.data_ptr(), _shape_arg(latent.shape),
+                                                latent.dim(), out.data_ptr(), int(n_bands),
+                                                self._stream_ptr(stream)))
+        return out
+
+    def decode_host(self, latent_host, out_host, n_bands: int, stream=None):
+        """Host buffers in, host buffers out (copies inside the call; synchronous)."""
+        _check(self.lib, self.lib.vaedec_decode_host(self._h, latent_host.data_ptr(),
+                                                     _shape_arg(latent_host.shape), latent_host.dim(),
+                                                     out_host.data_ptr(), int(n_bands),
+                                                     self._stream_ptr(stream)))
+        return out_host
+
+    def sync(self, stream=None) -> None:
+        _check(self.lib, self.lib.vaedec_sync(self._h, self._stream_ptr(stream)))
+
+    def launch_count(self) -> int:
+        n = ctypes.c_uint64()
+        _check(self.lib, self.lib.vaedec_launch_count(self._h, ctypes.byref(n)))
+        return int(n.value)
+
+    def profile(self, enable: bool) -> None:
+        _check(self.lib, self.lib.vaedec_profile_enable(self._h, 1 if enable else 0))
+
+    def profile_read(self, max_ops: int = 4096):
+        """Per-op device milliseconds of the last profiled decode."""
+        buf = (ctypes.c_float * max_ops)()
+        n = ctypes.c_int()
+        _check(self.lib, self.lib.vaedec_profile_read(self._h, buf, max_ops, ctypes.byref(n)))
+        return [float(buf[i]) for i in range(min(n.value, max_ops))]
+
+    # ------------------------------------------------------------------ inspection
+    def num_ops(self, latent_shape: Sequence[int], n_bands: int) -> int:
+        n = ctypes.c_int()
+        _check(self.lib, self.lib.vaedec_debug_num_ops(self._h, _shape_arg(latent_shape), len(latent_shape),
+                                                       int(n_bands), ctypes.byref(n)))
+        return n.value
+
+    def op_desc(self, latent_shape: Sequence[int], n_bands: int, op: int) -> Dict[str, str]:
+        buf = ctypes.create_string_buffer(1024)
+        _check(self.lib, self.lib.vaedec_debug_op_desc(self._h, _shape_arg(latent_shape), len(latent_shape),
+                                                       int(n_bands), int(op), buf, 1024))
+        return dict(kv.split("=", 1) for kv in buf.value.decode().split())
+
+    def ops(self, latent_shape: Sequence[int], n_bands: int) -> Iterable[Dict[str, str]]:
+        return [self.op_desc(latent_shape, n_bands, i) for i in range(self.num_ops(latent_shape, n_bands))]
+
+    def run_until(self, latent, n_bands: int, op: int, dst_in=None, dst_aux=None, dst_out=None, stream=None):
+        """Run ops [0, op] and copy that op's input / aux / output activations into the given device tensors."""
+        def ptr_size(t):
+            return (0, 0) if t is None else (t.data_ptr(), t.numel() * t.element_size())
+        pi, si = ptr_size(dst_in)
+        pa, sa = ptr_size(dst_aux)
+        po, so = ptr_size(dst_out)
+        _check(self.lib, self.lib.vaedec_debug_run_until(
+            self._h, latent.data_ptr(), _shape_arg(latent.shape), latent.dim(), int(n_bands), int(op),
+            pi or None, si, pa or None, sa, po or None, so, self._stream_ptr(stream)))

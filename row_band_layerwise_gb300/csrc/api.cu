@@ -1,0 +1,1229 @@
+// C ABI of the decoder: weight repacking, workspace planning, and the layer walk
+// that enqueues the kernels of one decode.
+//
+// The walk follows the decoder module order.  One GPU holds every band, so:
+//  * convs run as one launch over all rows: a band's halo rows are its
+//    neighbour's rows in the same tensor, read in place, and zero padding
+//    appears only outside the image ("VAEP：VAE 并行解码", 卷积：交换边界行);
+//  * GroupNorm statistics come from fixed one-row chunks merged with the
+//    weighted rule (GroupNorm：合并全局统计量), independent of the band split;
+//  * attention runs band by band: the band's query rows against every key and
+//    value of the frame (Attention：本地 Q，全局 K/V), so the score buffer is
+//    bounded by the largest band;
+//  * SiLU, RMSNorm and upsampling are local (the upsample is folded into the
+//    next conv's addressing).
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <sstream>
+#include <string>
+#include <vector>
+
+#include "../../include/vaedec.h"
+#include "kernels.h"
+
+using namespace vd;
+
+namespace {
+
+thread_local std::string g_err;
+
+vaedec_status fail(vaedec_status s, const std::string& m) {
+  g_err = m;
+  return s;
+}
+
+vaedec_status cuda_fail(cudaError_t e, const std::string& where) {
+  return fail(VAEDEC_ERR_CUDA, where + ": " + cudaGetErrorString(e));
+}
+
+constexpr int kNumAct = 5;
+
+struct DevConv {
+  void* w = nullptr;     // [rows][ntaps][cin] model dtype
+  float* b = nullptr;    // [cout]
+  int rows = 0, ntaps = 0, cin = 0, cout = 0;
+  int kt = 1, kh = 1, kw = 1;
+};
+
+struct DevNorm {
+  float* g = nullptr;
+  float* b = nullptr;
+  int c = 0;
+};
+
+struct Act {
+  int buf = -1;          // activation buffer index, or -1 for an external pointer
+  void* ext = nullptr;
+  int dt = kBF16;        // element type (kF32 / kBF16)
+  int B = 0, T = 1, H = 0, W = 0, C = 0;
+  long long pixels() const { return (long long)B * T * H * W; }
+};
+
+enum ConvKind { K3, K1, C3, UP, TIME };
+
+std::vector<int> band_rows(int h, int n) {
+  std::vector<int> r(n, h / n);
+  for (int i = 0; i < h % n; ++i) r[i] += 1;
+  return r;
+}
+
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+// Placeholder output of dry walks (planning, op descriptions): never dereferenced,
+// it only marks the last conv as writing the caller's channels-first output.
+char kDryOutTag;
+void* const kDryOut = &kDryOutTag;
+
+}  // namespace
+
+struct vaedec {
+  vaedec_config cfg{};
+  int dtype = kBF16;
+  size_t es = 2;
+  std::map<std::string, DevConv> conv;
+  std::map<std::string, DevNorm> norm;
+  std::vector<void*> allocs;
+  // workspace
+  void* act[kNumAct] = {};
+  size_t act_bytes = 0;
+  void* attn_q = nullptr;
+  void* attn_k = nullptr;
+  void* attn_vt = nullptr;
+  size_t qkv_bytes = 0;
+  float* attn_s = nullptr;
+  void* attn_p = nullptr;
+  float* attn_l = nullptr;
+  size_t s_elems = 0, l_elems = 0;
+  GnPartial* gn_part = nullptr;
+  size_t part_elems = 0;
+  float* gn_scale = nullptr;
+  float* gn_shift = nullptr;
+  size_t sc_elems = 0;
+  void* io_latent = nullptr;
+  void* io_out = nullptr;
+  size_t io_latent_bytes = 0, io_out_bytes = 0;
+  int* status = nullptr;
+  size_t ws_bytes = 0;
+  // instrumentation
+  unsigned long long launches = 0;
+  bool profile = false;
+  std::vector<cudaEvent_t> prof_ev;   // 2 per op
+  int prof_ops = 0;
+
+  vaedec_status dalloc(void** p, size_t bytes, const char* what) {
+    *p = nullptr;
+    if (bytes == 0) return VAEDEC_OK;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      *p = nullptr;
+      return fail(VAEDEC_ERR_OOM, std::string("cudaMalloc failed for ") + what + " (" + std::to_string(bytes) +
+                                      " bytes): " + cudaGetErrorString(e));
+    }
+    allocs.push_back(*p);
+    return VAEDEC_OK;
+  }
+  ~vaedec() {
+    for (cudaEvent_t e : prof_ev) cudaEventDestroy(e);
+    for (void* p : allocs) cudaFree(p);
+  }
+};
+
+namespace {
+
+// Sizes a dry walk records for workspace planning.
+struct Plan {
+  size_t act = 0, qkv = 0, s = 0, l = 0, part = 0, sc = 0;
+};
+
+class Walker {
+ public:
+  Walker(vaedec* h, cudaStream_t st, bool dry, int n_bands)
+      : h_(h), st_(st), dry_(dry), n_bands_(n_bands), odt_(h->dtype), sdt_(kF32) {}
+
+  // configuration of a debug stop
+  int stop_at = -1;
+  std::string* desc_out = nullptr;
+  void* d_in = nullptr;
+  void* d_aux = nullptr;
+  void* d_out = nullptr;
+  size_t in_b = 0, aux_b = 0, out_b = 0;
+  Plan* plan = nullptr;
+
+  vaedec_status status = VAEDEC_OK;
+  bool stopped = false;
+  int n_ops = 0;
+
+  bool live() const { return status == VAEDEC_OK && !stopped; }
+
+  vaedec_status run(const void* latent, const int64_t* shape, int ndim, void* out) {
+    Act z;
+    z.B = (int)shape[0];
+    z.C = (int)shape[1];
+    if (ndim == 5) {
+      z.T = (int)shape[2];
+      z.H = (int)shape[3];
+      z.W = (int)shape[4];
+    } else {
+      z.T = 1;
+      z.H = (int)shape[2];
+      z.W = (int)shape[3];
+    }
+    z.dt = odt_;
+    Act x = latent_in(latent, z);
+    if (h_->cfg.family == VAEDEC_FAMILY_KL2D)
+      walk_kl(x, out);
+    else
+      walk_wan(x, out);
+    return status;
+  }
+
+ private:
+  vaedec* h_;
+  cudaStream_t st_;
+  bool dry_;
+  int n_bands_;
+  int odt_;   // operand dtype: what the MMAs read (the model dtype)
+  int sdt_;   // storage dtype of the residual stream and every pre-norm tensor (fp32)
+  int nest_ = 0;
+
+  bool mixed() const { return odt_ != sdt_; }
+
+  // ---------------------------------------------------------------- helpers
+  void* ptr(const Act& a) const { return a.buf >= 0 ? h_->act[a.buf] : a.ext; }
+  static size_t esz(int dt) { return dt == kBF16 ? 2 : 4; }
+  size_t bytes(const Act& a) const { return (size_t)a.pixels() * a.C * esz(a.dt); }
+  static const char* dts(int dt) { return dt == kBF16 ? "bf16" : "f32"; }
+
+  static int pick(std::initializer_list<int> busy) {
+    for (int i = 0; i < kNumAct; ++i)
+      if (std::find(busy.begin(), busy.end(), i) == busy.end()) return i;
+    return -1;
+  }
+
+  void note_act(const Act& a) {
+    if (plan && a.buf >= 0) plan->act = std::max(plan->act, bytes(a));
+  }
+
+  void set_err(vaedec_status s, const std::string& m) {
+    if (status == VAEDEC_OK) {
+      status = s;
+      g_err = m;
+    }
+  }
+
+  void check(cudaError_t e, const std::string& where) {
+    if (e != cudaSuccess && status == VAEDEC_OK) {
+      status = VAEDEC_ERR_CUDA;
+      g_err = where + ": " + cudaGetErrorString(e);
+    }
+  }
+
+  static std::string shp(const Act& a) {
+    std::ostringstream o;
+    o << a.B << "," << a.T << "," << a.H << "," << a.W << "," << a.C;
+    return o.str();
+  }
+
+  static std::string io(const Act& x, const Act* aux, const Act& y) {
+    std::string s = " in=" + shp(x) + " in_dt=" + dts(x.dt) + " out=" + shp(y) + " out_dt=" + dts(y.dt);
+    if (aux) s += std::string(" aux_dt=") + dts(aux->dt);
+    return s;
+  }
+
+  // Begin a traced op.  Returns true if its kernels should be enqueued.
+  bool begin(const std::string& desc) {
+    if (!live()) return false;
+    if (nest_ > 0) return !dry_;
+    const int idx = n_ops++;
+    if (idx == stop_at && desc_out) *desc_out = desc;
+    if (!dry_ && h_->profile) {
+      while ((int)h_->prof_ev.size() < 2 * (idx + 1)) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) {
+          set_err(VAEDEC_ERR_CUDA, "cudaEventCreate failed");
+          return false;
+        }
+        h_->prof_ev.push_back(e);
+      }
+      check(cudaEventRecord(h_->prof_ev[2 * idx], st_), "profile event");
+      h_->prof_ops = idx + 1;
+    }
+    return !dry_;
+  }
+
+  void count(int n = 1) {
+    if (!dry_) h_->launches += (unsigned long long)n;
+  }
+
+  // End a traced op: at the stop op, copy its activations out and stop.
+  void end(const Act* in, const Act* aux, const Act& out_act) {
+    if (nest_ > 0 || !live()) return;
+    const int idx = n_ops - 1;
+    if (!dry_ && h_->profile && 2 * idx + 1 < (int)h_->prof_ev.size())
+      check(cudaEventRecord(h_->prof_ev[2 * idx + 1], st_), "profile event");
+    if (idx != stop_at) return;
+    if (!dry_) {
+      auto cp = [&](void* dst, size_t cap, const Act* a, const char* what) {
+        if (dst == nullptr || a == nullptr) return;
+        const size_t n = bytes(*a);
+        if (cap < n) {
+          set_err(VAEDEC_ERR_INVALID_ARG, std::string("debug buffer too small for ") + what);
+          return;
+        }
+        check(cudaMemcpyAsync(dst, ptr(*a), n, cudaMemcpyDeviceToDevice, st_), "debug copy");
+      };
+      cp(d_in, in_b, in, "input");
+      cp(d_aux, aux_b, aux, "aux");
+      cp(d_out, out_b, &out_act, "output");
+    }
+    stopped = true;
+  }
+
+  const DevConv* W(const std::string& name) {
+    auto it = h_->conv.find(name);
+    if (it == h_->conv.end()) {
+      set_err(VAEDEC_ERR_INVALID_ARG, "missing weights for " + name);
+      return nullptr;
+    }
+    return &it->second;
+  }
+  const DevNorm* N(const std::string& name) {
+    auto it = h_->norm.find(name);
+    if (it == h_->norm.end()) {
+      set_err(VAEDEC_ERR_INVALID_ARG, "missing norm parameters for " + name);
+      return nullptr;
+    }
+    return &it->second;
+  }
+
+  // ---------------------------------------------------------------- ops
+  Act latent_in(const void* latent, const Act& z) {
+    Act y = z;
+    y.buf = 0;
+    y.dt = odt_;
+    note_act(y);
+    Act zin = z;
+    zin.buf = -1;
+    zin.ext = const_cast<void*>(latent);
+    if (begin("kind=latent name=latent" + io(zin, nullptr, y))) {
+      count();
+      check(launch_to_channels_last(odt_, latent, ptr(y), z.B, z.C, (long long)z.T * z.H * z.W, st_),
+            "latent layout");
+    }
+    end(&zin, nullptr, y);
+    return y;
+  }
+
+  // Launch one GEMM/conv described by `g`.
+  void launch(const ConvGeom& g, const void* in, const DevConv& w, const void* wptr, const float* bias,
+              const void* residual, const float* rowscale, void* out, void* out2, const char* what) {
+    count();
+    if (h_->dtype == kBF16) {
+      const char* why = nullptr;
+      cudaError_t e = launch_conv_tc(g, in, wptr, w.ntaps, w.rows, bias, residual, rowscale, out, out2, h_->status,
+                                     st_, &why);
+      if (e != cudaSuccess) set_err(VAEDEC_ERR_CUDA, std::string(what) + ": " + (why ? why : cudaGetErrorString(e)));
+    } else {
+      check(launch_conv_simple_f32(g, static_cast<const float*>(in), static_cast<const float*>(wptr), w.ntaps, bias,
+                                   static_cast<const float*>(residual), rowscale, static_cast<float*>(out), st_),
+            what);
+    }
+  }
+
+  static void fill_taps(ConvGeom& g, ConvKind kind, const DevConv& w) {
+    std::memset(g.taps, 0, sizeof(g.taps));
+    g.nphase = 1;
+    if (kind == K1) {
+      g.ntaps = 1;
+      g.taps[0][0] = ConvTap{0, 0, 0, 0};
+    } else if (kind == K3) {
+      g.ntaps = 9;
+      for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 3; ++j)
+          g.taps[0][i * 3 + j] = ConvTap{0, (int8_t)(i - 1), (int8_t)(j - 1), (int8_t)(i * 3 + j)};
+    } else if (kind == C3) {
+      g.ntaps = w.kt * w.kh * w.kw;
+      for (int s = 0; s < w.kt; ++s)
+        for (int i = 0; i < w.kh; ++i)
+          for (int j = 0; j < w.kw; ++j) {
+            const int k = (s * w.kh + i) * w.kw + j;
+            g.taps[0][k] = ConvTap{(int8_t)(s - (w.kt - 1)), (int8_t)(i - w.kh / 2), (int8_t)(j - w.kw / 2), (int8_t)k};
+          }
+    } else if (kind == TIME) {
+      g.ntaps = w.kt;
+      for (int s = 0; s < w.kt; ++s) g.taps[0][s] = ConvTap{(int8_t)(s - (w.kt - 1)), 0, 0, (int8_t)s};
+    } else {  // UP: nearest-2x then 3x3, as four phases on the low-resolution grid
+      g.nphase = 4;
+      g.ntaps = 9;
+      for (int ph = 0; ph < 4; ++ph) {
+        const int py = ph >> 1, px = ph & 1;
+        for (int i = 0; i < 3; ++i)
+          for (int j = 0; j < 3; ++j) {
+            const int oy = (py + i - 1) >= 0 ? (py + i - 1) / 2 : -1;   // floor((py + i - 1) / 2)
+            const int ox = (px + j - 1) >= 0 ? (px + j - 1) / 2 : -1;
+            g.taps[ph][i * 3 + j] = ConvTap{0, (int8_t)oy, (int8_t)ox, (int8_t)(i * 3 + j)};
+          }
+      }
+    }
+  }
+
+  // conv op: x (operand dtype) -> y (`out_dt`, channels-last buffer `out_buf`, or the
+  // final channels-first output).  `copy` (optional) receives a bf16 copy of y.
+  Act conv(const Act& x, const std::string& name, ConvKind kind, const Act* res, int out_buf, int out_dt,
+           void* final_out = nullptr, Act* copy = nullptr, int copy_buf = -1) {
+    Act y = x;
+    const DevConv* w = W(name);
+    if (!w || !live()) return y;
+    if (w->cin != x.C) {
+      set_err(VAEDEC_ERR_INVALID_ARG, "channel mismatch at " + name);
+      return y;
+    }
+    if (x.dt != odt_) {
+      set_err(VAEDEC_ERR_INVALID_ARG, "internal: conv operand in the wrong dtype at " + name);
+      return y;
+    }
+    y.buf = final_out ? -1 : out_buf;
+    y.ext = final_out;
+    y.dt = final_out ? odt_ : out_dt;
+    y.C = (kind == TIME) ? w->cout / 2 : w->cout;
+    if (kind == UP) {
+      y.H *= 2;
+      y.W *= 2;
+    }
+    if (kind == TIME) y.T = 2 * x.T - 1;
+    note_act(y);
+    Act yc;
+    if (copy) {
+      yc = y;
+      yc.buf = copy_buf;
+      yc.dt = kBF16;
+      note_act(yc);
+      *copy = yc;
+    }
+    std::ostringstream d;
+    d << "kind=conv name=" << name << " conv="
+      << (kind == K3 ? "k3" : kind == K1 ? "k1" : kind == C3 ? "causal3" : kind == UP ? "up2x_k3" : "time")
+      << io(x, res, y) << " res=" << (res ? 1 : 0) << " final=" << (final_out ? 1 : 0);
+    if (begin(d.str())) {
+      ConvGeom g;
+      std::memset(&g, 0, sizeof(g));
+      g.B = x.B;
+      g.T = x.T;
+      g.H = x.H;
+      g.W = x.W;
+      g.Cin = x.C;
+      g.Cout = w->cout;
+      fill_taps(g, kind, *w);
+      g.oT = y.T;
+      g.oH = y.H;
+      g.oW = y.W;
+      g.oC = y.C;
+      g.osy = g.osx = (kind == UP) ? 2 : 1;
+      g.time_up_c = (kind == TIME) ? y.C : 0;
+      g.out_chfirst = final_out ? 1 : 0;
+      g.out_f32 = y.dt == kF32 ? 1 : 0;
+      g.res_f32 = (res && res->dt == kF32) ? 1 : 0;
+      g.scale = 1.f;
+      const char* in = static_cast<const char*>(ptr(x));
+      void* out2 = copy ? ptr(yc) : nullptr;
+      if (kind == TIME) {
+        // frame 0 passes through; frames 1..T-1 feed the causal time conv
+        if (y.dt != x.dt) set_err(VAEDEC_ERR_INVALID_ARG, "internal: time upsample dtype");
+        const size_t frame = (size_t)x.H * x.W * x.C * esz(x.dt);
+        check(cudaMemcpy2DAsync(ptr(y), frame * y.T, in, frame * x.T, frame, x.B, cudaMemcpyDeviceToDevice, st_),
+              "frame 0 copy");
+        // the time-conv view starts at frame 1 with T-1 frames while the sample
+        // stride stays T frames: one launch per sample
+        for (int b = 0; b < x.B && x.T > 1 && live(); ++b) {
+          ConvGeom gb = g;
+          gb.B = 1;
+          gb.T = x.T - 1;
+          const size_t in_off = (size_t)b * x.T * frame + frame;
+          const size_t out_off = (size_t)b * y.T * y.H * y.W * y.C * esz(y.dt);
+          launch(gb, in + in_off, *w, w->w, w->b, nullptr, nullptr, static_cast<char*>(ptr(y)) + out_off, nullptr,
+                 name.c_str());
+        }
+      } else {
+        launch(g, in, *w, w->w, w->b, res ? ptr(*res) : nullptr, nullptr, ptr(y), out2, name.c_str());
+      }
+    }
+    end(&x, res, y);
+    return y;
+  }
+
+  // GroupNorm: x (any dtype) -> operand dtype; `raw` (optional) receives x cast.
+  Act group_norm(const Act& x, const std::string& prefix, bool silu, int out_buf, Act* raw = nullptr,
+                 int raw_buf = -1) {
+    Act y = x;
+    y.buf = out_buf;
+    y.dt = odt_;
+    const DevNorm* n = N(prefix);
+    if (!n || !live()) return y;
+    const int G = h_->cfg.norm_groups;
+    const int rows = x.T * x.H;
+    if (plan) {
+      plan->part = std::max(plan->part, (size_t)x.B * rows * G);
+      plan->sc = std::max(plan->sc, (size_t)x.B * x.C);
+    }
+    note_act(y);
+    Act yr;
+    if (raw) {
+      yr = x;
+      yr.buf = raw_buf;
+      yr.dt = odt_;
+      note_act(yr);
+      *raw = yr;
+    }
+    if (begin("kind=groupnorm name=" + prefix + io(x, nullptr, y) + " silu=" + (silu ? "1" : "0") +
+              " groups=" + std::to_string(G))) {
+      count(3);
+      check(launch_gn_partials(x.dt, ptr(x), x.B, rows, x.W, x.C, G, 1, h_->gn_part, st_), "gn partials");
+      check(launch_gn_finalize(h_->gn_part, x.B, rows, x.C, G, n->g, n->b, h_->cfg.eps, h_->gn_scale, h_->gn_shift,
+                               st_),
+            "gn finalize");
+      check(launch_gn_apply(x.dt, y.dt, ptr(x), ptr(y), raw ? ptr(yr) : nullptr, (long long)x.T * x.H * x.W, x.B,
+                            x.C, h_->gn_scale, h_->gn_shift, silu ? 1 : 0, st_),
+            "gn apply");
+    }
+    end(&x, nullptr, y);
+    return y;
+  }
+
+  Act rms_norm(const Act& x, const std::string& prefix, bool silu, int out_buf, Act* raw = nullptr,
+               int raw_buf = -1) {
+    Act y = x;
+    y.buf = out_buf;
+    y.dt = odt_;
+    const DevNorm* n = N(prefix);
+    if (!n || !live()) return y;
+    note_act(y);
+    Act yr;
+    if (raw) {
+      yr = x;
+      yr.buf = raw_buf;
+      yr.dt = odt_;
+      note_act(yr);
+      *raw = yr;
+    }
+    if (begin("kind=rmsnorm name=" + prefix + io(x, nullptr, y) + " silu=" + (silu ? "1" : "0"))) {
+      count();
+      check(launch_rms_norm(x.dt, y.dt, ptr(x), ptr(y), raw ? ptr(yr) : nullptr, x.pixels(), x.C, n->g,
+                            silu ? 1 : 0, st_),
+            "rms norm");
+    }
+    end(&x, nullptr, y);
+    return y;
+  }
+
+  // Attention block over frames (B*T sequences of H*W tokens) with band-local queries.
+  Act attention(const Act& x, const std::string& prefix, bool wan) {
+    const int a_buf = pick({x.buf});
+    const int o_buf = pick({x.buf, a_buf});
+    Act y = x;
+    y.buf = o_buf;
+    y.dt = sdt_;
+    const int C = x.C;
+    const long long Ntok = (long long)x.H * x.W;
+    const int F = x.B * x.T;   // sequences
+    const size_t oes = esz(odt_);
+    if (plan) {
+      plan->qkv = std::max(plan->qkv, (size_t)F * (size_t)Ntok * (size_t)C * oes);
+      int maxrows = 0;
+      for (int r : band_rows(x.H, n_bands_)) maxrows = std::max(maxrows, r);
+      plan->s = std::max(plan->s, (size_t)maxrows * (size_t)x.W * (size_t)Ntok);
+      plan->l = std::max(plan->l, (size_t)maxrows * x.W);
+    }
+    note_act(y);
+    const bool run = begin("kind=attention name=" + prefix + io(x, nullptr, y) + " wan=" + (wan ? "1" : "0") +
+                           " bands=" + std::to_string(n_bands_));
+    ++nest_;
+    if (live()) {
+      // normalisation (GroupNorm for KL, channel RMSNorm for Wan), no SiLU
+      Act hn = wan ? rms_norm(x, prefix + ".norm", false, a_buf) : group_norm(x, prefix + ".group_norm", false, a_buf);
+      DevConv wq, wk, wv, wo;
+      bool ok = true;
+      if (wan) {
+        const DevConv* qkv = W(prefix + ".to_qkv");
+        const DevConv* pr = W(prefix + ".proj");
+        ok = qkv && pr;
+        if (ok) {
+          const size_t blk = (size_t)C * qkv->ntaps * qkv->cin * oes;
+          wq = wk = wv = *qkv;
+          wq.cout = wk.cout = wv.cout = C;
+          wq.rows = wk.rows = wv.rows = C;
+          wk.w = static_cast<char*>(qkv->w) + blk;
+          wv.w = static_cast<char*>(qkv->w) + 2 * blk;
+          wk.b = qkv->b + C;
+          wv.b = qkv->b + 2 * C;
+          wo = *pr;
+        }
+      } else {
+        const DevConv *a = W(prefix + ".to_q"), *b = W(prefix + ".to_k"), *c = W(prefix + ".to_v"),
+                      *d = W(prefix + ".to_out.0");
+        ok = a && b && c && d;
+        if (ok) {
+          wq = *a;
+          wk = *b;
+          wv = *c;
+          wo = *d;
+        }
+      }
+      if (ok && run) {
+        // projections on a (F, 1, H, W) grid: Q, K channels-last, V channels-first (V^T per frame)
+        ConvGeom g;
+        std::memset(&g, 0, sizeof(g));
+        g.B = F;
+        g.T = 1;
+        g.H = x.H;
+        g.W = x.W;
+        g.Cin = C;
+        g.Cout = C;
+        g.nphase = 1;
+        g.ntaps = 1;
+        g.oT = 1;
+        g.oH = x.H;
+        g.oW = x.W;
+        g.oC = C;
+        g.osy = g.osx = 1;
+        g.out_f32 = odt_ == kF32;
+        g.scale = 1.f;
+        launch(g, ptr(hn), wq, wq.w, wq.b, nullptr, nullptr, h_->attn_q, nullptr, "attention q");
+        launch(g, ptr(hn), wk, wk.w, wk.b, nullptr, nullptr, h_->attn_k, nullptr, "attention k");
+        ConvGeom gv = g;
+        gv.out_chfirst = 1;
+        launch(gv, ptr(hn), wv, wv.w, wv.b, nullptr, nullptr, h_->attn_vt, nullptr, "attention v");
+        // band-local queries against every key/value of the frame
+        const std::vector<int> rows = band_rows(x.H, n_bands_);
+        DevConv kview;
+        kview.ntaps = 1;
+        kview.cin = C;
+        kview.rows = (int)Ntok;
+        kview.cout = (int)Ntok;
+        DevConv vview;
+        vview.ntaps = 1;
+        vview.cin = (int)Ntok;
+        vview.rows = C;
+        vview.cout = C;
+        const float scale = 1.f / std::sqrt((float)C);
+        for (int f = 0; f < F && live(); ++f) {
+          int r0 = 0;
+          for (int band = 0; band < n_bands_ && live(); ++band) {
+            const int nr = rows[band] * x.W;
+            const size_t qoff = ((size_t)f * Ntok + (size_t)r0 * x.W) * C;
+            ConvGeom gs;
+            std::memset(&gs, 0, sizeof(gs));
+            gs.B = 1;
+            gs.T = 1;
+            gs.H = 1;
+            gs.W = nr;
+            gs.Cin = C;
+            gs.Cout = (int)Ntok;
+            gs.nphase = 1;
+            gs.ntaps = 1;
+            gs.oT = 1;
+            gs.oH = 1;
+            gs.oW = nr;
+            gs.oC = (int)Ntok;
+            gs.osy = gs.osx = 1;
+            gs.out_f32 = 1;
+            gs.scale = scale;
+            launch(gs, static_cast<char*>(h_->attn_q) + qoff * oes, kview,
+                   static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes, nullptr, nullptr, nullptr,
+                   h_->attn_s, nullptr, "attention scores");
+            count();
+            check(launch_softmax_rows(odt_, h_->attn_s, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
+            ConvGeom go = gs;
+            go.Cin = (int)Ntok;
+            go.Cout = C;
+            go.oC = C;
+            go.out_f32 = odt_ == kF32;
+            go.scale = 1.f;
+            // O overwrites the band's rows of the normalised tensor (no longer needed)
+            launch(go, h_->attn_p, vview, static_cast<char*>(h_->attn_vt) + (size_t)f * C * Ntok * oes, nullptr,
+                   nullptr, h_->attn_l, static_cast<char*>(ptr(hn)) + qoff * oes, nullptr, "attention pv");
+            r0 += rows[band];
+          }
+        }
+        // output projection + residual in fp32
+        ConvGeom gp = g;
+        gp.out_f32 = y.dt == kF32;
+        gp.res_f32 = x.dt == kF32;
+        launch(gp, ptr(hn), wo, wo.w, wo.b, ptr(x), nullptr, ptr(y), nullptr, "attention out");
+      }
+    }
+    --nest_;
+    end(&x, nullptr, y);
+    return y;
+  }
+
+  // ---------------------------------------------------------------- blocks
+  // Residual block on the fp32 stream x.  When `copy` is given, the block output
+  // is also stored as a bf16 operand copy (for a following upsample conv).
+  Act resnet(const Act& x, const std::string& p, bool wan, Act* copy) {
+    const bool sc = h_->conv.count(p + ".conv_shortcut") > 0;
+    const int tb = pick({x.buf});
+    Act xb = x;   // operand copy of x for the shortcut conv
+    const bool need_raw = sc && mixed();
+    const int rb = need_raw ? pick({x.buf, tb}) : -1;
+    Act t = wan ? rms_norm(x, p + ".norm1", true, tb, need_raw ? &xb : nullptr, rb)
+                : group_norm(x, p + ".norm1", true, tb, need_raw ? &xb : nullptr, rb);
+    const int hb = pick({x.buf, tb, rb});
+    Act hh = conv(t, p + ".conv1", wan ? C3 : K3, nullptr, hb, sdt_);
+    Act t2 = wan ? rms_norm(hh, p + ".norm2", true, tb) : group_norm(hh, p + ".norm2", true, tb);
+    Act res = x;
+    int scb = -1;
+    if (sc) {
+      scb = pick({x.buf, tb, hb, rb});
+      res = conv(xb, p + ".conv_shortcut", wan ? C3 : K1, nullptr, scb, sdt_);
+    }
+    const int out_buf = hb;
+    if (copy && mixed()) {
+      const int cb = sc ? pick({tb, hb, scb}) : pick({x.buf, tb, hb});
+      return conv(t2, p + ".conv2", wan ? C3 : K3, &res, out_buf, sdt_, nullptr, copy, cb);
+    }
+    Act y = conv(t2, p + ".conv2", wan ? C3 : K3, &res, out_buf, sdt_);
+    if (copy) *copy = y;
+    return y;
+  }
+
+  void walk_kl(Act x, void* out) {
+    const vaedec_config& c = h_->cfg;
+    x = conv(x, "conv_in", K3, nullptr, pick({x.buf}), sdt_);
+    x = resnet(x, "mid_block.resnets.0", false, nullptr);
+    x = attention(x, "mid_block.attentions.0", false);
+    x = resnet(x, "mid_block.resnets.1", false, nullptr);
+    for (int s = 0; s < c.n_stages && live(); ++s) {
+      const std::string pre = "up_blocks." + std::to_string(s);
+      Act xc;
+      for (int r = 0; r < c.stage_resnets[s]; ++r) {
+        const bool last = (r + 1 == c.stage_resnets[s]) && c.stage_upsample[s];
+        x = resnet(x, pre + ".resnets." + std::to_string(r), false, last ? &xc : nullptr);
+      }
+      if (c.stage_upsample[s]) x = conv(xc, pre + ".upsamplers.0.conv", UP, nullptr, pick({x.buf, xc.buf}), sdt_);
+    }
+    Act t = group_norm(x, "conv_norm_out", true, pick({x.buf}));
+    conv(t, "conv_out", K3, nullptr, -1, odt_, out);
+  }
+
+  void walk_wan(Act x, void* out) {
+    const vaedec_config& c = h_->cfg;
+    x = conv(x, "conv_in", C3, nullptr, pick({x.buf}), sdt_);
+    x = resnet(x, "mid_block.resnets.0", true, nullptr);
+    x = attention(x, "mid_block.attentions.0", true);
+    x = resnet(x, "mid_block.resnets.1", true, nullptr);
+    for (int s = 0; s < c.n_stages && live(); ++s) {
+      const std::string pre = "up_blocks." + std::to_string(s);
+      Act xc;
+      for (int r = 0; r < c.stage_resnets[s]; ++r) {
+        const bool last = (r + 1 == c.stage_resnets[s]) && c.stage_upsample[s];
+        x = resnet(x, pre + ".resnets." + std::to_string(r), true, last ? &xc : nullptr);
+      }
+      if (c.stage_upsample[s] == VAEDEC_UP_SPATIOTEMPORAL)
+        xc = conv(xc, pre + ".upsamplers.0.time_conv", TIME, nullptr, pick({x.buf, xc.buf}), odt_);
+      if (c.stage_upsample[s])
+        x = conv(xc, pre + ".upsamplers.0.resample.1", UP, nullptr, pick({x.buf, xc.buf}), sdt_);
+    }
+    Act t = rms_norm(x, "norm_out", true, pick({x.buf}));
+    conv(t, "conv_out", C3, nullptr, -1, odt_, out);
+  }
+};
+
+// ---------------------------------------------------------------- create helpers
+float to_f32(const vaedec_tensor& t, size_t i) {
+  if (t.dtype == VAEDEC_DTYPE_F32) return static_cast<const float*>(t.data)[i];
+  uint16_t u = static_cast<const uint16_t*>(t.data)[i];
+  uint32_t v = static_cast<uint32_t>(u) << 16;
+  float f;
+  std::memcpy(&f, &v, 4);
+  return f;
+}
+
+uint16_t f32_to_bf16(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;  // NaN
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+size_t numel(const vaedec_tensor& t) {
+  size_t n = 1;
+  for (int i = 0; i < t.ndim; ++i) n *= (size_t)t.shape[i];
+  return n;
+}
+
+// Every conv / linear / norm the architecture uses, with expected shapes.
+struct Need {
+  std::string name;
+  int kind;                // 0 conv (weight+bias), 1 groupnorm (weight+bias), 2 rms (gamma)
+  int cout, cin, kt, kh, kw;
+  bool linear;             // 2D weight [cout, cin]
+};
+
+void needs_kl(const vaedec_config& c, std::vector<Need>& v) {
+  auto conv = [&](const std::string& n, int ci, int co, int k) { v.push_back({n, 0, co, ci, 1, k, k, false}); };
+  auto gn = [&](const std::string& n, int ch) { v.push_back({n, 1, ch, ch, 1, 1, 1, false}); };
+  auto resnet = [&](const std::string& p, int ci, int co) {
+    gn(p + ".norm1", ci);
+    conv(p + ".conv1", ci, co, 3);
+    gn(p + ".norm2", co);
+    conv(p + ".conv2", co, co, 3);
+    if (ci != co) conv(p + ".conv_shortcut", ci, co, 1);
+  };
+  const int C = c.mid_channels;
+  conv("conv_in", c.latent_channels, C, 3);
+  resnet("mid_block.resnets.0", C, C);
+  const std::string a = "mid_block.attentions.0";
+  gn(a + ".group_norm", C);
+  for (const char* p : {".to_q", ".to_k", ".to_v", ".to_out.0"}) v.push_back({a + p, 0, C, C, 1, 1, 1, true});
+  resnet("mid_block.resnets.1", C, C);
+  int cin = C;
+  for (int s = 0; s < c.n_stages; ++s) {
+    const int co = c.stage_channels[s];
+    for (int r = 0; r < c.stage_resnets[s]; ++r)
+      resnet("up_blocks." + std::to_string(s) + ".resnets." + std::to_string(r), r == 0 ? cin : co, co);
+    cin = co;
+    if (c.stage_upsample[s]) {
+      conv("up_blocks." + std::to_string(s) + ".upsamplers.0.conv", co, c.stage_up_channels[s], 3);
+      cin = c.stage_up_channels[s];
+    }
+  }
+  gn("conv_norm_out", cin);
+  conv("conv_out", cin, c.out_channels, 3);
+}
+
+void needs_wan(const vaedec_config& c, std::vector<Need>& v) {
+  auto conv3 = [&](const std::string& n, int ci, int co, int kt, int k) { v.push_back({n, 0, co, ci, kt, k, k, false}); };
+  auto conv2 = [&](const std::string& n, int ci, int co, int k) { v.push_back({n, 0, co, ci, 0, k, k, false}); };
+  auto rms = [&](const std::string& n, int ch) { v.push_back({n, 2, ch, ch, 1, 1, 1, false}); };
+  auto resnet = [&](const std::string& p, int ci, int co) {
+    rms(p + ".norm1", ci);
+    conv3(p + ".conv1", ci, co, 3, 3);
+    rms(p + ".norm2", co);
+    conv3(p + ".conv2", co, co, 3, 3);
+    if (ci != co) conv3(p + ".conv_shortcut", ci, co, 1, 1);
+  };
+  const int C = c.mid_channels;
+  conv3("conv_in", c.latent_channels, C, 3, 3);
+  resnet("mid_block.resnets.0", C, C);
+  const std::string a = "mid_block.attentions.0";
+  rms(a + ".norm", C);
+  conv2(a + ".to_qkv", C, 3 * C, 1);
+  conv2(a + ".proj", C, C, 1);
+  resnet("mid_block.resnets.1", C, C);
+  int cin = C;
+  for (int s = 0; s < c.n_stages; ++s) {
+    const int co = c.stage_channels[s];
+    const std::string pre = "up_blocks." + std::to_string(s);
+    for (int r = 0; r < c.stage_resnets[s]; ++r) resnet(pre + ".resnets." + std::to_string(r), r == 0 ? cin : co, co);
+    cin = co;
+    if (c.stage_upsample[s] == VAEDEC_UP_SPATIOTEMPORAL) v.push_back({pre + ".upsamplers.0.time_conv", 0, 2 * co, co, 3, 1, 1, false});
+    if (c.stage_upsample[s]) {
+      conv2(pre + ".upsamplers.0.resample.1", co, c.stage_up_channels[s], 3);
+      cin = c.stage_up_channels[s];
+    }
+  }
+  rms("norm_out", cin);
+  conv3("conv_out", cin, c.out_channels, 3, 3);
+}
+
+const vaedec_tensor* find_tensor(const vaedec_tensor* ws, int n, const std::string& name) {
+  for (int i = 0; i < n; ++i)
+    if (ws[i].name && name == ws[i].name) return &ws[i];
+  return nullptr;
+}
+
+vaedec_status upload_f32(vaedec* h, const std::vector<float>& v, float** dst, const char* what) {
+  void* p = nullptr;
+  vaedec_status s = h->dalloc(&p, v.size() * sizeof(float), what);
+  if (s != VAEDEC_OK) return s;
+  cudaError_t e = cudaMemcpy(p, v.data(), v.size() * sizeof(float), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  *dst = static_cast<float*>(p);
+  return VAEDEC_OK;
+}
+
+vaedec_status validate_config(const vaedec_config* c) {
+  if (c->family != VAEDEC_FAMILY_KL2D && c->family != VAEDEC_FAMILY_WAN3D) return fail(VAEDEC_ERR_INVALID_ARG, "unknown family");
+  if (c->dtype != VAEDEC_DTYPE_F32 && c->dtype != VAEDEC_DTYPE_BF16) return fail(VAEDEC_ERR_INVALID_ARG, "unknown dtype");
+  if (c->n_stages < 1 || c->n_stages > VAEDEC_MAX_STAGES) return fail(VAEDEC_ERR_INVALID_ARG, "n_stages out of range");
+  if (c->latent_channels < 1 || c->mid_channels < 1 || c->out_channels < 1)
+    return fail(VAEDEC_ERR_INVALID_ARG, "channel counts must be positive");
+  for (int i = 0; i < 4; ++i)
+    if (c->max_latent[i] < 1) return fail(VAEDEC_ERR_INVALID_ARG, "max_latent entries must be positive");
+  if (c->family == VAEDEC_FAMILY_KL2D && c->max_latent[1] != 1) return fail(VAEDEC_ERR_INVALID_ARG, "max_latent T must be 1 for KL2D");
+  std::vector<int> chans = {c->mid_channels};
+  for (int s = 0; s < c->n_stages; ++s) {
+    if (c->stage_channels[s] < 1 || c->stage_resnets[s] < 1 || c->stage_upsample[s] < 0 || c->stage_upsample[s] > 2)
+      return fail(VAEDEC_ERR_INVALID_ARG, "bad stage description");
+    if (c->stage_upsample[s] && c->stage_up_channels[s] < 1) return fail(VAEDEC_ERR_INVALID_ARG, "bad upsample channels");
+    if (c->family == VAEDEC_FAMILY_KL2D && c->stage_upsample[s] == 2)
+      return fail(VAEDEC_ERR_INVALID_ARG, "KL2D has no temporal upsample");
+    chans.push_back(c->stage_channels[s]);
+    if (c->stage_upsample[s]) chans.push_back(c->stage_up_channels[s]);
+  }
+  for (int ch : chans) {
+    if (ch % 8 != 0) return fail(VAEDEC_ERR_UNSUPPORTED, "activation channel counts must be multiples of 8");
+    if (c->dtype == VAEDEC_DTYPE_BF16 && ch % 16 != 0)
+      return fail(VAEDEC_ERR_UNSUPPORTED, "bf16 path needs channel counts that are multiples of 16");
+    if (ch > 2048) return fail(VAEDEC_ERR_UNSUPPORTED, "channel count too large");
+    if (c->family == VAEDEC_FAMILY_KL2D && (c->norm_groups < 1 || ch % c->norm_groups != 0))
+      return fail(VAEDEC_ERR_INVALID_ARG, "GroupNorm groups must divide every channel count");
+    if (c->family == VAEDEC_FAMILY_WAN3D && ch > 512) return fail(VAEDEC_ERR_UNSUPPORTED, "RMSNorm supports up to 512 channels");
+  }
+  if (c->dtype == VAEDEC_DTYPE_BF16 && c->latent_channels % 16 != 0)
+    return fail(VAEDEC_ERR_UNSUPPORTED, "bf16 path needs latent channels that are a multiple of 16");
+  if (c->family == VAEDEC_FAMILY_KL2D && !(c->eps > 0.f)) return fail(VAEDEC_ERR_INVALID_ARG, "eps must be positive");
+  return VAEDEC_OK;
+}
+
+vaedec_status check_latent(const vaedec* h, const int64_t* shape, int ndim, int n_bands) {
+  if (shape == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "latent shape is NULL");
+  const int want = h->cfg.family == VAEDEC_FAMILY_KL2D ? 4 : 5;
+  if (ndim != want) return fail(VAEDEC_ERR_INVALID_ARG, "latent ndim must be " + std::to_string(want));
+  for (int i = 0; i < ndim; ++i)
+    if (shape[i] < 1) return fail(VAEDEC_ERR_INVALID_ARG, "latent dims must be positive");
+  if (shape[1] != h->cfg.latent_channels) return fail(VAEDEC_ERR_INVALID_ARG, "latent channel count mismatch");
+  const int64_t B = shape[0], T = ndim == 5 ? shape[2] : 1, H = shape[ndim - 2], W = shape[ndim - 1];
+  const int64_t* m = h->cfg.max_latent;
+  if (B > m[0] || T > m[1] || H > m[2] || W > m[3]) return fail(VAEDEC_ERR_INVALID_ARG, "latent shape exceeds max_latent");
+  // the workspace was planned for max_latent: B*T*H*W and H*W must also fit
+  if (B * T * H * W > m[0] * m[1] * m[2] * m[3]) return fail(VAEDEC_ERR_INVALID_ARG, "latent shape exceeds max_latent");
+  if (n_bands < 1 || n_bands > H) return fail(VAEDEC_ERR_INVALID_ARG, "n_bands must be in [1, latent H]");
+  // the tensor-core attention streams keys as 16-byte-aligned rows
+  if (h->dtype == kBF16 && (H * W) % 8 != 0)
+    return fail(VAEDEC_ERR_UNSUPPORTED, "bf16 path needs latent H*W to be a multiple of 8");
+  return VAEDEC_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* vaedec_last_error(void) { return g_err.c_str(); }
+
+vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* weights, int n_weights,
+                            vaedec_t** out) {
+  g_err.clear();
+  if (out == nullptr || config == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  *out = nullptr;
+  if (n_weights < 0 || (n_weights > 0 && weights == nullptr)) return fail(VAEDEC_ERR_INVALID_ARG, "bad weight list");
+  vaedec_status s = validate_config(config);
+  if (s != VAEDEC_OK) return s;
+  vaedec* h = new vaedec();
+  h->cfg = *config;
+  h->dtype = config->dtype == VAEDEC_DTYPE_BF16 ? kBF16 : kF32;
+  h->es = h->dtype == kBF16 ? 2 : 4;
+  auto bail = [&](vaedec_status st) {
+    delete h;
+    return st;
+  };
+
+  std::vector<Need> needs;
+  if (config->family == VAEDEC_FAMILY_KL2D)
+    needs_kl(*config, needs);
+  else
+    needs_wan(*config, needs);
+
+  for (const Need& nd : needs) {
+    if (nd.kind == 0) {
+      const vaedec_tensor* w = find_tensor(weights, n_weights, nd.name + ".weight");
+      const vaedec_tensor* b = find_tensor(weights, n_weights, nd.name + ".bias");
+      if (!w || !b) return bail(fail(VAEDEC_ERR_INVALID_ARG, "missing tensor " + nd.name + ".weight/.bias"));
+      // expected weight shape
+      std::vector<int64_t> exp;
+      if (nd.linear)
+        exp = {nd.cout, nd.cin};
+      else if (config->family == VAEDEC_FAMILY_WAN3D && nd.kt > 0)
+        exp = {nd.cout, nd.cin, nd.kt, nd.kh, nd.kw};
+      else
+        exp = {nd.cout, nd.cin, nd.kh, nd.kw};
+      bool okshape = w->ndim == (int)exp.size();
+      for (size_t i = 0; okshape && i < exp.size(); ++i) okshape = w->shape[i] == exp[i];
+      if (!okshape) return bail(fail(VAEDEC_ERR_INVALID_ARG, "unexpected shape for " + nd.name + ".weight"));
+      if (b->ndim != 1 || b->shape[0] != nd.cout) return bail(fail(VAEDEC_ERR_INVALID_ARG, "unexpected shape for " + nd.name + ".bias"));
+      if (w->data == nullptr || b->data == nullptr) return bail(fail(VAEDEC_ERR_INVALID_ARG, "NULL data for " + nd.name));
+      const int kt = (nd.kt > 0) ? nd.kt : 1;
+      const int ntaps = kt * nd.kh * nd.kw;
+      DevConv dc;
+      dc.cin = nd.cin;
+      dc.cout = nd.cout;
+      dc.ntaps = ntaps;
+      dc.kt = kt;
+      dc.kh = nd.kh;
+      dc.kw = nd.kw;
+      dc.rows = h->dtype == kBF16 ? round_up(nd.cout, 16) : nd.cout;
+      // repack [cout][cin][taps] -> [rows][taps][cin]
+      const size_t n = (size_t)dc.rows * ntaps * nd.cin;
+      if (h->dtype == kBF16) {
+        std::vector<uint16_t> buf(n, 0);
+        for (int co = 0; co < nd.cout; ++co)
+          for (int ci = 0; ci < nd.cin; ++ci)
+            for (int t = 0; t < ntaps; ++t)
+              buf[((size_t)co * ntaps + t) * nd.cin + ci] = f32_to_bf16(to_f32(*w, ((size_t)co * nd.cin + ci) * ntaps + t));
+        s = h->dalloc(&dc.w, n * 2, nd.name.c_str());
+        if (s != VAEDEC_OK) return bail(s);
+        cudaError_t e = cudaMemcpy(dc.w, buf.data(), n * 2, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return bail(cuda_fail(e, "weight upload"));
+      } else {
+        std::vector<float> buf(n, 0.f);
+        for (int co = 0; co < nd.cout; ++co)
+          for (int ci = 0; ci < nd.cin; ++ci)
+            for (int t = 0; t < ntaps; ++t)
+              buf[((size_t)co * ntaps + t) * nd.cin + ci] = to_f32(*w, ((size_t)co * nd.cin + ci) * ntaps + t);
+        s = h->dalloc(&dc.w, n * 4, nd.name.c_str());
+        if (s != VAEDEC_OK) return bail(s);
+        cudaError_t e = cudaMemcpy(dc.w, buf.data(), n * 4, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return bail(cuda_fail(e, "weight upload"));
+      }
+      std::vector<float> bias(nd.cout);
+      for (int i = 0; i < nd.cout; ++i) bias[i] = to_f32(*b, i);
+      s = upload_f32(h, bias, &dc.b, nd.name.c_str());
+      if (s != VAEDEC_OK) return bail(s);
+      h->conv[nd.name] = dc;
+    } else {
+      DevNorm dn;
+      dn.c = nd.cout;
+      const std::string gname = nd.kind == 1 ? nd.name + ".weight" : nd.name + ".gamma";
+      const vaedec_tensor* g = find_tensor(weights, n_weights, gname);
+      if (!g || numel(*g) != (size_t)nd.cout || !g->data)
+        return bail(fail(VAEDEC_ERR_INVALID_ARG, "missing or mis-shaped " + gname));
+      std::vector<float> gv(nd.cout), bv(nd.cout, 0.f);
+      for (int i = 0; i < nd.cout; ++i) gv[i] = to_f32(*g, i);
+      if (nd.kind == 1) {
+        const vaedec_tensor* b = find_tensor(weights, n_weights, nd.name + ".bias");
+        if (!b || numel(*b) != (size_t)nd.cout || !b->data)
+          return bail(fail(VAEDEC_ERR_INVALID_ARG, "missing or mis-shaped " + nd.name + ".bias"));
+        for (int i = 0; i < nd.cout; ++i) bv[i] = to_f32(*b, i);
+      }
+      s = upload_f32(h, gv, &dn.g, gname.c_str());
+      if (s != VAEDEC_OK) return bail(s);
+      s = upload_f32(h, bv, &dn.b, gname.c_str());
+      if (s != VAEDEC_OK) return bail(s);
+      h->norm[nd.name] = dn;
+    }
+  }
+
+  // workspace plan: a dry walk at max_latent with one band (the largest score buffer)
+  Plan plan;
+  {
+    int64_t shape[5];
+    int ndim;
+    const int64_t* m = config->max_latent;
+    if (config->family == VAEDEC_FAMILY_KL2D) {
+      ndim = 4;
+      shape[0] = m[0]; shape[1] = config->latent_channels; shape[2] = m[2]; shape[3] = m[3];
+    } else {
+      ndim = 5;
+      shape[0] = m[0]; shape[1] = config->latent_channels; shape[2] = m[1]; shape[3] = m[2]; shape[4] = m[3];
+    }
+    Walker w(h, nullptr, true, 1);
+    w.plan = &plan;
+    s = w.run(nullptr, shape, ndim, kDryOut);
+    if (s != VAEDEC_OK) return bail(s);
+    int64_t oshape[5];
+    if (vaedec_output_shape(h, shape, ndim, oshape) != VAEDEC_OK) return bail(VAEDEC_ERR_INVALID_ARG);
+    h->io_latent_bytes = 1;
+    for (int i = 0; i < ndim; ++i) h->io_latent_bytes *= (size_t)shape[i];
+    h->io_out_bytes = 1;
+    for (int i = 0; i < ndim; ++i) h->io_out_bytes *= (size_t)oshape[i];
+    h->io_latent_bytes *= h->es;
+    h->io_out_bytes *= h->es;
+  }
+  h->act_bytes = plan.act;
+  for (int i = 0; i < kNumAct && s == VAEDEC_OK; ++i) s = h->dalloc(&h->act[i], plan.act, "activations");
+  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_q, plan.qkv, "attention q");
+  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_k, plan.qkv, "attention k");
+  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_vt, plan.qkv, "attention v");
+  h->qkv_bytes = plan.qkv;
+  void* tmp = nullptr;
+  if (s == VAEDEC_OK) s = h->dalloc(&tmp, plan.s * sizeof(float), "attention scores");
+  h->attn_s = static_cast<float*>(tmp);
+  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_p, plan.s * h->es, "attention probabilities");
+  if (s == VAEDEC_OK) s = h->dalloc(&tmp, plan.l * sizeof(float), "attention row sums");
+  h->attn_l = static_cast<float*>(tmp);
+  h->s_elems = plan.s;
+  h->l_elems = plan.l;
+  if (s == VAEDEC_OK) s = h->dalloc(&tmp, std::max<size_t>(plan.part, 1) * sizeof(GnPartial), "groupnorm partials");
+  h->gn_part = static_cast<GnPartial*>(tmp);
+  if (s == VAEDEC_OK) s = h->dalloc(&tmp, std::max<size_t>(plan.sc, 1) * sizeof(float), "groupnorm scale");
+  h->gn_scale = static_cast<float*>(tmp);
+  if (s == VAEDEC_OK) s = h->dalloc(&tmp, std::max<size_t>(plan.sc, 1) * sizeof(float), "groupnorm shift");
+  h->gn_shift = static_cast<float*>(tmp);
+  if (s == VAEDEC_OK) s = h->dalloc(&h->io_latent, h->io_latent_bytes, "host-path latent");
+  if (s == VAEDEC_OK) s = h->dalloc(&h->io_out, h->io_out_bytes, "host-path output");
+  if (s == VAEDEC_OK) s = h->dalloc(&tmp, sizeof(int), "status word");
+  h->status = static_cast<int*>(tmp);
+  if (s != VAEDEC_OK) return bail(s);
+  cudaError_t e = cudaMemset(h->status, 0, sizeof(int));
+  if (e != cudaSuccess) return bail(cuda_fail(e, "status init"));
+  h->ws_bytes = kNumAct * plan.act + 3 * plan.qkv + plan.s * (4 + h->es) + plan.l * 4 + plan.part * sizeof(GnPartial) +
+                2 * plan.sc * 4 + h->io_latent_bytes + h->io_out_bytes;
+  *out = h;
+  return VAEDEC_OK;
+}
+
+void vaedec_destroy(vaedec_t* h) {
+  if (h == nullptr) return;
+  cudaDeviceSynchronize();
+  delete h;
+}
+
+vaedec_status vaedec_output_shape(const vaedec_t* h, const int64_t* shape, int ndim, int64_t* out_shape) {
+  if (h == nullptr || shape == nullptr || out_shape == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  const int want = h->cfg.family == VAEDEC_FAMILY_KL2D ? 4 : 5;
+  if (ndim != want) return fail(VAEDEC_ERR_INVALID_ARG, "latent ndim must be " + std::to_string(want));
+  int64_t f = 1, T = ndim == 5 ? shape[2] : 1;
+  for (int s = 0; s < h->cfg.n_stages; ++s) {
+    if (h->cfg.stage_upsample[s]) f *= 2;
+    if (h->cfg.stage_upsample[s] == VAEDEC_UP_SPATIOTEMPORAL) T = 2 * T - 1;
+  }
+  out_shape[0] = shape[0];
+  out_shape[1] = h->cfg.out_channels;
+  if (ndim == 5) {
+    out_shape[2] = T;
+    out_shape[3] = shape[3] * f;
+    out_shape[4] = shape[4] * f;
+  } else {
+    out_shape[2] = shape[2] * f;
+    out_shape[3] = shape[3] * f;
+  }
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_workspace_bytes(const vaedec_t* h, size_t* bytes) {
+  if (h == nullptr || bytes == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  *bytes = h->ws_bytes;
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_decode(vaedec_t* h, const void* latent, const int64_t* shape, int ndim, void* out, int n_bands,
+                            void* stream) {
+  if (h == nullptr || latent == nullptr || out == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  vaedec_status s = check_latent(h, shape, ndim, n_bands);
+  if (s != VAEDEC_OK) return s;
+  Walker w(h, static_cast<cudaStream_t>(stream), false, n_bands);
+  return w.run(latent, shape, ndim, out);
+}
+
+vaedec_status vaedec_sync(vaedec_t* h, void* stream) {
+  if (h == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL handle");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (word != 0) {
+    cudaMemset(h->status, 0, sizeof(int));
+    return fail(VAEDEC_ERR_TIMEOUT, "a kernel's bounded wait ran out (status word " + std::to_string(word) + ")");
+  }
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_decode_host(vaedec_t* h, const void* latent_host, const int64_t* shape, int ndim, void* out_host,
+                                 int n_bands, void* stream) {
+  if (h == nullptr || latent_host == nullptr || out_host == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  vaedec_status s = check_latent(h, shape, ndim, n_bands);
+  if (s != VAEDEC_OK) return s;
+  int64_t oshape[5];
+  s = vaedec_output_shape(h, shape, ndim, oshape);
+  if (s != VAEDEC_OK) return s;
+  size_t in_b = h->es, out_b = h->es;
+  for (int i = 0; i < ndim; ++i) {
+    in_b *= (size_t)shape[i];
+    out_b *= (size_t)oshape[i];
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h->io_latent, latent_host, in_b, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "latent upload");
+  s = vaedec_decode(h, h->io_latent, shape, ndim, h->io_out, n_bands, stream);
+  if (s != VAEDEC_OK) return s;
+  e = cudaMemcpyAsync(out_host, h->io_out, out_b, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "output download");
+  return vaedec_sync(h, stream);
+}
+
+vaedec_status vaedec_launch_count(const vaedec_t* h, uint64_t* n) {
+  if (h == nullptr || n == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  *n = h->launches;
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_profile_enable(vaedec_t* h, int enable) {
+  if (h == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL handle");
+  h->profile = enable != 0;
+  h->prof_ops = 0;
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_profile_read(vaedec_t* h, float* ms, int max_ops, int* n_ops) {
+  if (h == nullptr || n_ops == nullptr || (ms == nullptr && max_ops > 0)) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  *n_ops = h->prof_ops;
+  for (int i = 0; i < h->prof_ops && i < max_ops; ++i) {
+    cudaError_t e = cudaEventSynchronize(h->prof_ev[2 * i + 1]);
+    if (e != cudaSuccess) return cuda_fail(e, "profile event synchronize");
+    e = cudaEventElapsedTime(&ms[i], h->prof_ev[2 * i], h->prof_ev[2 * i + 1]);
+    if (e != cudaSuccess) return cuda_fail(e, "profile event elapsed");
+  }
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_debug_num_ops(vaedec_t* h, const int64_t* shape, int ndim, int n_bands, int* n_ops) {
+  if (h == nullptr || n_ops == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  vaedec_status s = check_latent(h, shape, ndim, n_bands);
+  if (s != VAEDEC_OK) return s;
+  Walker w(h, nullptr, true, n_bands);
+  s = w.run(nullptr, shape, ndim, kDryOut);
+  *n_ops = w.n_ops;
+  return s;
+}
+
+vaedec_status vaedec_debug_op_desc(vaedec_t* h, const int64_t* shape, int ndim, int n_bands, int op, char* buf,
+                                   int buf_len) {
+  if (h == nullptr || buf == nullptr || buf_len < 1) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  vaedec_status s = check_latent(h, shape, ndim, n_bands);
+  if (s != VAEDEC_OK) return s;
+  std::string d;
+  Walker w(h, nullptr, true, n_bands);
+  w.stop_at = op;
+  w.desc_out = &d;
+  s = w.run(nullptr, shape, ndim, kDryOut);
+  if (s != VAEDEC_OK) return s;
+  if (d.empty()) return fail(VAEDEC_ERR_INVALID_ARG, "op index out of range");
+  if ((int)d.size() + 1 > buf_len) return fail(VAEDEC_ERR_INVALID_ARG, "description buffer too small");
+  std::memcpy(buf, d.c_str(), d.size() + 1);
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_debug_run_until(vaedec_t* h, const void* latent, const int64_t* shape, int ndim, int n_bands,
+                                     int op, void* dst_in, size_t in_bytes, void* dst_aux, size_t aux_bytes,
+                                     void* dst_out, size_t out_bytes, void* stream) {
+  if (h == nullptr || latent == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  vaedec_status s = check_latent(h, shape, ndim, n_bands);
+  if (s != VAEDEC_OK) return s;
+  if (op < 0) return fail(VAEDEC_ERR_INVALID_ARG, "op index out of range");
+  // the final op writes the caller's output: route it to a scratch output buffer
+  Walker w(h, static_cast<cudaStream_t>(stream), false, n_bands);
+  w.stop_at = op;
+  w.d_in = dst_in;
+  w.in_b = in_bytes;
+  w.d_aux = dst_aux;
+  w.aux_b = aux_bytes;
+  w.d_out = dst_out;
+  w.out_b = out_bytes;
+  s = w.run(latent, shape, ndim, h->io_out);
+  if (s != VAEDEC_OK) return s;
+  if (!w.stopped) return fail(VAEDEC_ERR_INVALID_ARG, "op index out of range");
+  return vaedec_sync(h, stream);
+}
+
+}  // extern "C"

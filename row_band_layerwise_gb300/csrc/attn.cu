@@ -1,0 +1,112 @@
+// Attention softmax for band-local queries against global keys
+// ("VAEP：VAE 并行解码", section Attention：本地 Q，全局 K/V): the scores of one
+// band's query rows against every key are normalised row by row.
+// Also the small layout kernel that turns the caller's channels-first latent
+// into the channels-last activation layout.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace vd {
+
+namespace {
+
+constexpr int kSmThreads = 256;
+
+__device__ __forceinline__ float block_reduce_max(float v, float* sh) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) sh[w] = v;
+  __syncthreads();
+  float r = sh[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = fmaxf(r, sh[i]);
+  return r;
+}
+
+__device__ __forceinline__ float block_reduce_sum(float v, float* sh) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) sh[w] = v;
+  __syncthreads();
+  float r = sh[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r += sh[i];
+  return r;
+}
+
+template <typename P>
+__device__ __forceinline__ float store_p(P* p, float v);
+template <>
+__device__ __forceinline__ float store_p<float>(float* p, float v) {
+  *p = v;
+  return v;
+}
+template <>
+__device__ __forceinline__ float store_p<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  *p = h;
+  return __bfloat162float(h);
+}
+
+template <typename P>
+__global__ void __launch_bounds__(kSmThreads) softmax_rows_kernel(const float* __restrict__ S, P* __restrict__ Pm,
+                                                                  float* __restrict__ inv_l, int nk) {
+  __shared__ float red[32];
+  const long long row = blockIdx.x;
+  const float* s = S + row * nk;
+  P* p = Pm + row * nk;
+  float m = -INFINITY;
+  for (int k = threadIdx.x; k < nk; k += blockDim.x) m = fmaxf(m, s[k]);
+  m = block_reduce_max(m, red);
+  float l = 0.f;
+  for (int k = threadIdx.x; k < nk; k += blockDim.x) l += store_p<P>(p + k, __expf(s[k] - m));
+  l = block_reduce_sum(l, red);
+  if (threadIdx.x == 0) inv_l[row] = 1.f / l;
+}
+
+template <typename T>
+__global__ void to_channels_last_kernel(const T* __restrict__ x, T* __restrict__ y, int C, long long spatial,
+                                        long long total) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = static_cast<int>(i % C);
+    const long long r = i / C;
+    const long long sp = r % spatial;
+    const long long b = r / spatial;
+    y[i] = x[(b * C + c) * spatial + sp];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv_l, int rows, int nk,
+                                cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  if (p_dtype == kBF16)
+    softmax_rows_kernel<__nv_bfloat16><<<rows, kSmThreads, 0, stream>>>(S, static_cast<__nv_bfloat16*>(P), inv_l, nk);
+  else
+    softmax_rows_kernel<float><<<rows, kSmThreads, 0, stream>>>(S, static_cast<float*>(P), inv_l, nk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_channels_last(int dtype, const void* x, void* y, int B, int C, long long spatial,
+                                    cudaStream_t stream) {
+  const long long total = (long long)B * C * spatial;
+  if (total <= 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 152LL * 32) blocks = 152LL * 32;
+  if (dtype == kBF16)
+    to_channels_last_kernel<__nv_bfloat16><<<(int)blocks, threads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), C, spatial, total);
+  else
+    to_channels_last_kernel<float><<<(int)blocks, threads, 0, stream>>>(static_cast<const float*>(x),
+                                                                       static_cast<float*>(y), C, spatial, total);
+  return cudaGetLastError();
+}
+
+}  // namespace vd

@@ -1,0 +1,472 @@
+// Implicit-GEMM convolution on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// One CTA computes a 128-pixel x BN-channel output tile:
+//   warp 0      TMA producer: per K step (tap, 64/32/16-channel chunk) loads the
+//               shifted 128-pixel activation box and the weight box into a
+//               swizzled shared-memory stage.  Out-of-range boxes read zeros,
+//               which is the conv's zero padding at the global image edges (and
+//               the causal zero frames in time); rows of a neighbouring band are
+//               in range and read their real values (the conv halo of
+//               "VAEP：VAE 并行解码", section 卷积：交换边界行).
+//   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16) from
+//               one thread, accumulating fp32 in TMEM; commits free each stage.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane per pixel),
+//               scale, add bias and residual in fp32, round once, store.
+// Every wait is bounded (see ptx.cuh); on timeout the CTA records an error,
+// drains its own copies, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+
+#include "conv.h"
+#include "ptx.cuh"
+#include "kernels.h"
+
+namespace vd {
+
+struct ConvTcParams {
+  CUtensorMap tmA;       // activations [B][T][H][W][Cin] as 5D (Cin, W, H, T, B)
+  CUtensorMap tmB;       // weights [rows][ntaps_w][Cin] as 3D (Cin, ntaps_w, rows)
+  ConvGeom g;
+  int BX, BY;            // pixel tile: BY rows x BX columns, BX * BY = 128
+  int tiles_x, tiles_y;
+  int BN, n_ntiles;
+  int n_kchunks, stages;
+  uint32_t stage_a_bytes, stage_b_bytes, tmem_cols;
+  const float* bias;     // [Cout] or null
+  const void* residual;  // channels-last (fp32 or bf16, see g.res_f32), same index as out, or null
+  const float* rowscale; // per output pixel (flat grid index), or null
+  void* out;
+  __nv_bfloat16* out2;   // optional bf16 copy of a channels-last output
+  int* status;
+};
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+
+template <int BK>
+struct SwizzleOf {
+  // row pitch BK*2 bytes; 8-row swizzle atom
+  static constexpr uint32_t kSbo = BK * 2 * 8;
+  static constexpr uint32_t kMode = BK == 64 ? 2u : (BK == 32 ? 4u : 6u);
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 16 consecutive channels of one pixel: 64-byte (fp32) or 32-byte (bf16) vector
+// accesses when all 16 are valid, scalar otherwise.
+__device__ __forceinline__ void add_f32x16(float (&v)[16], const float* r, int n) {
+  if (n == 16) {
+    const float4* r4 = reinterpret_cast<const float4*>(r);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 a = r4[j];
+      v[4 * j] += a.x;
+      v[4 * j + 1] += a.y;
+      v[4 * j + 2] += a.z;
+      v[4 * j + 3] += a.w;
+    }
+  } else {
+    for (int j = 0; j < n; ++j) v[j] += r[j];
+  }
+}
+
+__device__ __forceinline__ void add_bf16x16(float (&v)[16], const __nv_bfloat16* r, int n) {
+  if (n == 16) {
+    const uint4* rp = reinterpret_cast<const uint4*>(r);
+    uint4 r0 = rp[0], r1 = rp[1];
+    const __nv_bfloat16* h0 = reinterpret_cast<const __nv_bfloat16*>(&r0);
+    const __nv_bfloat16* h1 = reinterpret_cast<const __nv_bfloat16*>(&r1);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] += __bfloat162float(h0[j]);
+      v[8 + j] += __bfloat162float(h1[j]);
+    }
+  } else {
+    for (int j = 0; j < n; ++j) v[j] += __bfloat162float(r[j]);
+  }
+}
+
+__device__ __forceinline__ void store_f32x16(float* o, const float (&v)[16], int n) {
+  if (n == 16) {
+    float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  } else {
+    for (int j = 0; j < n; ++j) o[j] = v[j];
+  }
+}
+
+__device__ __forceinline__ void store_bf16x16(__nv_bfloat16* o, const float (&v)[16], int n) {
+  if (n == 16) {
+    uint4 w0, w1;
+    w0.x = pack_bf16x2(v[0], v[1]);
+    w0.y = pack_bf16x2(v[2], v[3]);
+    w0.z = pack_bf16x2(v[4], v[5]);
+    w0.w = pack_bf16x2(v[6], v[7]);
+    w1.x = pack_bf16x2(v[8], v[9]);
+    w1.y = pack_bf16x2(v[10], v[11]);
+    w1.z = pack_bf16x2(v[12], v[13]);
+    w1.w = pack_bf16x2(v[14], v[15]);
+    reinterpret_cast<uint4*>(o)[0] = w0;
+    reinterpret_cast<uint4*>(o)[1] = w1;
+  } else {
+    for (int j = 0; j < n; ++j) o[j] = __float2bfloat16_rn(v[j]);
+  }
+}
+
+template <int BK>
+__global__ void __launch_bounds__(kThreads, 1) conv_tc_kernel(const __grid_constant__ ConvTcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[8];
+  __shared__ __align__(8) uint64_t empty_bar[8];
+  __shared__ __align__(8) uint64_t accum_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+  __shared__ float bias_sh[256];
+
+  const ConvGeom& g = p.g;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + p.stages * p.stage_a_bytes;
+
+  // ---- tile coordinates
+  int bid = blockIdx.x;
+  const int ntile = bid % p.n_ntiles;
+  bid /= p.n_ntiles;
+  const int phase = bid % g.nphase;
+  bid /= g.nphase;
+  const int tx = bid % p.tiles_x;
+  bid /= p.tiles_x;
+  const int ty = bid % p.tiles_y;
+  bid /= p.tiles_y;
+  const int tt = bid % g.T;
+  const int bb = bid / g.T;
+  const int x0 = tx * p.BX, y0 = ty * p.BY, n0 = ntile * p.BN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&accum_bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, p.tmem_cols);
+    tmem_relinquish();
+  }
+  if (warp >= 2) {
+    for (int i = threadIdx.x - 64; i < p.BN; i += 128) {
+      const int co = n0 + i;
+      bias_sh[i] = (p.bias != nullptr && co < g.Cout) ? p.bias[co] : 0.f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  const int ksteps = g.ntaps * p.n_kchunks;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint32_t tx_bytes = static_cast<uint32_t>(kBM * BK * 2 + p.BN * BK * 2);
+      int issued = 0;
+      for (int ks = 0; ks < ksteps; ++ks) {
+        const int s = ks % p.stages;
+        const uint32_t ph = static_cast<uint32_t>(ks / p.stages) & 1u;
+        if (ks >= p.stages && !mbar_wait(&empty_bar[s], ph ^ 1u, p.status, kErrTimeoutEmpty, &abort_flag)) break;
+        const int tap = ks / p.n_kchunks;
+        const int kc = ks - tap * p.n_kchunks;
+        const ConvTap tp = g.taps[phase][tap];
+        mbar_arrive_expect_tx(&full_bar[s], tx_bytes);
+        tma_load_5d(smA + s * p.stage_a_bytes, &p.tmA, &full_bar[s], kc * BK, x0 + tp.dx, y0 + tp.dy, tt + tp.dt, bb);
+        tma_load_3d(smB + s * p.stage_b_bytes, &p.tmB, &full_bar[s], kc * BK, tp.wtap, n0);
+        issued = ks + 1;
+      }
+      if (abort_flag) {
+        // Drain: wait (bounded) until every stage this thread filled has landed.
+        int dummy = 0;
+        volatile int no_abort = 0;
+        for (int ks = max(0, issued - p.stages); ks < issued; ++ks) {
+          const int s = ks % p.stages;
+          mbar_wait(&full_bar[s], static_cast<uint32_t>(ks / p.stages) & 1u, &dummy, 0, &no_abort);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, p.BN);
+      const uint32_t a_base = smem_u32(smA), b_base = smem_u32(smB);
+      for (int ks = 0; ks < ksteps; ++ks) {
+        const int s = ks % p.stages;
+        const uint32_t ph = static_cast<uint32_t>(ks / p.stages) & 1u;
+        if (!mbar_wait(&full_bar[s], ph, p.status, kErrTimeoutFull, &abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a0 = a_base + s * p.stage_a_bytes;
+        const uint32_t b0 = b_base + s * p.stage_b_bytes;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t da = smem_desc_kmajor(a0 + k * 32, SwizzleOf<BK>::kSbo, SwizzleOf<BK>::kMode);
+          const uint64_t db = smem_desc_kmajor(b0 + k * 32, SwizzleOf<BK>::kSbo, SwizzleOf<BK>::kMode);
+          tc_mma_bf16(tmem, da, db, idesc, (ks | k) != 0 ? 1u : 0u);
+        }
+        tc_commit(&empty_bar[s]);
+      }
+      tc_commit(&accum_bar);
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: warps 2..5 cover TMEM lane quarters (warp % 4)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int ly = row / p.BX, lx = row - ly * p.BX;
+    const int y = y0 + ly, x = x0 + lx;
+    const bool valid = (y < g.H) && (x < g.W);
+    const bool ok = mbar_wait(&accum_bar, 0, p.status, kErrTimeoutAccum, &abort_flag);
+    tc_fence_after();
+    // warp-uniform decision: tcgen05.ld is a warp-collective instruction
+    const bool go = __all_sync(0xffffffffu, ok && !abort_flag);
+    if (go) {
+      const int py = phase >> 1, px = phase & 1;
+      const int grid_pix = ((bb * g.T + tt) * g.H + y) * g.W + x;
+      const float rs = (p.rowscale != nullptr && valid) ? p.rowscale[grid_pix] : 1.f;
+      const int yo = y * g.osy + (g.nphase > 1 ? py : 0);
+      const int xo = x * g.osx + (g.nphase > 1 ? px : 0);
+      for (int c0 = 0; c0 < p.BN; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld_16x_32x32b(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, r);
+        tmem_ld_wait();
+        const int co0 = n0 + c0;
+        if (!valid || co0 >= g.Cout) continue;
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) * g.scale * rs + bias_sh[c0 + j];
+        int to = tt, ch0 = co0, oc = g.oC;
+        if (g.time_up_c > 0) {
+          const int half = co0 >= g.time_up_c ? 1 : 0;
+          to = 1 + 2 * tt + half;
+          ch0 = co0 - half * g.time_up_c;
+        }
+        const long long opix = ((static_cast<long long>(bb) * g.oT + to) * g.oH + yo) * g.oW + xo;
+        const int nvalid = min(16, g.Cout - co0);
+        if (!g.out_chfirst) {
+          const long long base = opix * oc + ch0;
+          if (p.residual != nullptr) {
+            if (g.res_f32)
+              add_f32x16(v, reinterpret_cast<const float*>(p.residual) + base, nvalid);
+            else
+              add_bf16x16(v, reinterpret_cast<const __nv_bfloat16*>(p.residual) + base, nvalid);
+          }
+          if (g.out_f32)
+            store_f32x16(reinterpret_cast<float*>(p.out) + base, v, nvalid);
+          else
+            store_bf16x16(reinterpret_cast<__nv_bfloat16*>(p.out) + base, v, nvalid);
+          if (p.out2 != nullptr) store_bf16x16(p.out2 + base, v, nvalid);
+        } else {
+          // channels-first [B][oC][oT][oH][oW]
+          const long long plane = static_cast<long long>(g.oT) * g.oH * g.oW;
+          const long long sp = ((static_cast<long long>(to)) * g.oH + yo) * g.oW + xo;
+          for (int j = 0; j < nvalid; ++j) {
+            const long long a = (static_cast<long long>(bb) * oc + ch0 + j) * plane + sp;
+            if (g.out_f32)
+              reinterpret_cast<float*>(p.out)[a] = v[j];
+            else
+              reinterpret_cast<__nv_bfloat16*>(p.out)[a] = __float2bfloat16_rn(v[j]);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+CUtensorMapSwizzle swizzle_for(int bk) {
+  return bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+}  // namespace
+
+const char* conv_tc_plan(const ConvGeom& g, int* bk_out) {
+  if (g.Cin % 8 != 0) return "tensor-core conv needs C_in a multiple of 8";
+  if (g.Cout < 1) return "C_out must be positive";
+  if (g.ntaps < 1 || g.ntaps > kMaxTaps || g.nphase < 1 || g.nphase > kMaxPhases) return "bad tap table";
+  // BK: the largest chunk whose padded K is within 5% of the tightest one.
+  int best = 1 << 30;
+  for (int bk : {64, 32, 16}) best = std::min(best, round_up(g.Cin, bk));
+  int bk = 16;
+  for (int cand : {64, 32, 16}) {
+    if (round_up(g.Cin, cand) * 100 <= best * 105) {
+      bk = cand;
+      break;
+    }
+  }
+  *bk_out = bk;
+  return nullptr;
+}
+
+cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
+                           const float* bias, const void* residual, const float* rowscale, void* out, void* out2,
+                           int* status, cudaStream_t stream, const char** why) {
+  *why = nullptr;
+  int bk = 64;
+  if (const char* e = conv_tc_plan(g, &bk)) {
+    *why = e;
+    return cudaErrorInvalidValue;
+  }
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) {
+    *why = "cuTensorMapEncodeTiled unavailable";
+    return cudaErrorNotSupported;
+  }
+  if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(wts) & 15)) {
+    *why = "conv operands must be 16-byte aligned";
+    return cudaErrorInvalidValue;
+  }
+  ConvTcParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.g = g;
+
+  // Pixel tile: BY x BX = 128, BX a power of two chosen to waste the fewest pixels.
+  long long best_cost = -1;
+  for (int bx = 128; bx >= 8; bx >>= 1) {
+    const int by = 128 / bx;
+    const long long cost = static_cast<long long>((g.W + bx - 1) / bx) * bx * ((g.H + by - 1) / by) * by;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      p.BX = bx;
+      p.BY = by;
+    }
+  }
+  p.tiles_x = (g.W + p.BX - 1) / p.BX;
+  p.tiles_y = (g.H + p.BY - 1) / p.BY;
+  p.n_ntiles = (g.Cout + 255) / 256;
+  p.BN = round_up((g.Cout + p.n_ntiles - 1) / p.n_ntiles, 16);
+  p.n_kchunks = (g.Cin + bk - 1) / bk;
+  p.stage_a_bytes = kBM * bk * 2;
+  p.stage_b_bytes = static_cast<uint32_t>(round_up(p.BN * bk * 2, 1024));
+  const int stage_bytes = static_cast<int>(p.stage_a_bytes + p.stage_b_bytes);
+  p.stages = std::min(8, (200 * 1024) / stage_bytes);
+  if (p.stages < 2) {
+    *why = "tile does not fit shared memory";
+    return cudaErrorInvalidValue;
+  }
+  p.tmem_cols = 32;
+  while (p.tmem_cols < static_cast<uint32_t>(p.BN)) p.tmem_cols <<= 1;
+  p.bias = bias;
+  p.residual = residual;
+  p.out2 = static_cast<__nv_bfloat16*>(out2);
+  if (out2 != nullptr && g.out_chfirst) {
+    *why = "a second output needs a channels-last store";
+    return cudaErrorInvalidValue;
+  }
+  p.rowscale = rowscale;
+  p.out = out;
+  p.status = status;
+
+  const cuuint32_t ones[5] = {1, 1, 1, 1, 1};
+  {
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(g.Cin), static_cast<cuuint64_t>(g.W),
+                                static_cast<cuuint64_t>(g.H), static_cast<cuuint64_t>(g.T),
+                                static_cast<cuuint64_t>(g.B)};
+    const cuuint64_t es = 2;
+    const cuuint64_t strides[4] = {dims[0] * es, dims[0] * dims[1] * es, dims[0] * dims[1] * dims[2] * es,
+                                   dims[0] * dims[1] * dims[2] * dims[3] * es};
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(bk), static_cast<cuuint32_t>(p.BX),
+                               static_cast<cuuint32_t>(p.BY), 1, 1};
+    CUresult r = enc(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(in), dims, strides, box, ones,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      *why = "activation tensor map rejected";
+      return cudaErrorInvalidValue;
+    }
+  }
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.Cin), static_cast<cuuint64_t>(ntaps_w),
+                                static_cast<cuuint64_t>(w_rows)};
+    const cuuint64_t strides[2] = {dims[0] * 2, dims[0] * dims[1] * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(bk), 1, static_cast<cuuint32_t>(p.BN)};
+    CUresult r = enc(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(wts), dims, strides, box, ones,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      *why = "weight tensor map rejected";
+      return cudaErrorInvalidValue;
+    }
+  }
+  const long long nblocks =
+      static_cast<long long>(g.B) * g.T * p.tiles_y * p.tiles_x * g.nphase * p.n_ntiles;
+  if (nblocks <= 0) return cudaSuccess;
+  if (nblocks > 0x7fffffffLL) {
+    *why = "grid too large";
+    return cudaErrorInvalidValue;
+  }
+  const size_t smem = static_cast<size_t>(p.stages) * stage_bytes + 1024;
+  cudaError_t e = cudaSuccess;
+  switch (bk) {
+    case 64:
+      e = cudaFuncSetAttribute(conv_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) conv_tc_kernel<64><<<(unsigned)nblocks, kThreads, smem, stream>>>(p);
+      break;
+    case 32:
+      e = cudaFuncSetAttribute(conv_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) conv_tc_kernel<32><<<(unsigned)nblocks, kThreads, smem, stream>>>(p);
+      break;
+    default:
+      e = cudaFuncSetAttribute(conv_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) conv_tc_kernel<16><<<(unsigned)nblocks, kThreads, smem, stream>>>(p);
+      break;
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace vd

@@ -1,0 +1,64 @@
+// Host-side launchers of every kernel in the library (internal interface).
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "conv.h"
+
+namespace vd {
+
+enum DType : int { kF32 = 1, kBF16 = 2 };
+
+// ---------------------------------------------------------------- convolution
+// Tensor-core implicit GEMM (bf16 in, fp32 accumulate, bf16/fp32 out).
+// `wts` is [w_rows][ntaps_w][Cin] bf16 (K-major per output channel).  `out2`
+// (optional) receives a bf16 copy of a channels-last output.
+const char* conv_tc_plan(const ConvGeom& g, int* bk_out);
+cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
+                           const float* bias, const void* residual, const float* rowscale, void* out, void* out2,
+                           int* status, cudaStream_t stream, const char** why);
+
+// CUDA-core fp32 direct convolution over the same ConvGeom (the fp32 path).
+// `wts` is [w_rows][ntaps_w][Cin] fp32.
+cudaError_t launch_conv_simple_f32(const ConvGeom& g, const float* in, const float* wts, int ntaps_w,
+                                   const float* bias, const float* residual, const float* rowscale, float* out,
+                                   cudaStream_t stream);
+
+// ---------------------------------------------------------------- GroupNorm
+// Central moments of one fixed row chunk and one group: count, mean, sum of
+// squared deviations.
+struct GnPartial {
+  float n, mean, m2, pad;
+};
+
+// Phase 1: per (sample, row chunk, group) central moments of a channels-last
+// [B][rows][W][C] tensor (rows = T*H for video; chunk = `chunk_rows` rows).
+cudaError_t launch_gn_partials(int dtype, const void* x, int B, int rows, int W, int C, int G, int chunk_rows,
+                               GnPartial* part, cudaStream_t stream);
+// Phase 2: merge the chunks of each (sample, group) with the weighted rule and
+// fold mean, variance, gamma and beta into a per-(sample, channel) scale/shift.
+cudaError_t launch_gn_finalize(const GnPartial* part, int B, int n_chunks, int C, int G, const float* gamma,
+                               const float* beta, float eps, float* scale, float* shift, cudaStream_t stream);
+// y = x * scale[b, c] + shift[b, c], then SiLU when `silu`; x in `in_dtype`,
+// y in `out_dtype`; `y_raw` (optional, `out_dtype`) receives x itself, cast.
+cudaError_t launch_gn_apply(int in_dtype, int out_dtype, const void* x, void* y, void* y_raw,
+                            long long pixels_per_sample, int B, int C, const float* scale, const float* shift,
+                            int silu, cudaStream_t stream);
+
+// Channel RMSNorm (Wan): y = x / max(||x||_2, 1e-12) * sqrt(C) * gamma, then SiLU
+// when `silu`; dtypes and `y_raw` as for launch_gn_apply.
+cudaError_t launch_rms_norm(int in_dtype, int out_dtype, const void* x, void* y, void* y_raw, long long pixels,
+                            int C, const float* gamma, int silu, cudaStream_t stream);
+
+// ---------------------------------------------------------------- attention
+// Row softmax numerators: P[r, k] = exp(S[r, k] - max_k S[r, :]) stored as
+// `p_dtype`, inv_l[r] = 1 / sum_k P[r, k] (sum of the stored values).
+cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv_l, int rows, int nk,
+                                cudaStream_t stream);
+
+// ---------------------------------------------------------------- layout
+// [B][C][S] -> [B][S][C] (same dtype).
+cudaError_t launch_to_channels_last(int dtype, const void* x, void* y, int B, int C, long long spatial,
+                                    cudaStream_t stream);
+
+}  // namespace vd

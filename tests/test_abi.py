@@ -1,0 +1,64 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import synth
+import row_band_layerwise_gb300 as rbl
+from row_band_layerwise_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vaedec.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(build.lib_path()):
+        build.build()
+    return rbl.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vaedec_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(rbl.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_create_rejects_bad_config_without_cuda(lib):
+    cfg = rbl.make_config(synth.KL_TINY, "fp32", (1, 1, 16, 16))
+    h = ctypes.c_void_p()
+    cfg.family = 7
+    assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 1
+    assert b"family" in lib.vaedec_last_error()
+    cfg = rbl.make_config(synth.KL_TINY, "fp32", (1, 1, 16, 16))
+    cfg.norm_groups = 5   # does not divide 64
+    assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 1
+    cfg = rbl.make_config(synth.KL_TINY, "bf16", (1, 1, 16, 16))   # latent channels 4: not a bf16 tile
+    assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 2
+    cfg = rbl.make_config(synth.KL_TINY, "fp32", (1, 2, 16, 16))   # T must be 1 for the 2D decoder
+    assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 1
+    assert not h.value
+
+
+def test_null_arguments_rejected(lib):
+    assert lib.vaedec_create(None, None, 0, None) == 1
+    assert lib.vaedec_decode(None, None, None, 0, None, 1, None) == 1
+    assert lib.vaedec_sync(None, None) == 1
+    lib.vaedec_destroy(None)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        rbl.load_library(str(tmp_path / "nope.so"))

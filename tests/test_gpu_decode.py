@@ -1,0 +1,156 @@
+"""GPU parity: the CUDA decode (through the C ABI) against the float64 oracle.
+
+Per-op checks trace every op of the decode (its captured input, residual and
+output) and compare the output with the oracle's op applied to the same input.
+End-to-end checks compare whole decodes with the oracle's decode within the
+stated tolerances: bf16 tensor-core path max-abs <= 3e-2 and rel-L2 <= 1e-2,
+fp32 path rel-L2 <= 1e-4.  Band-count invariance is checked bit for bit.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_helpers import Case, max_abs, oracle_op, parse_shape, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX_ABS = 3e-2
+BF16_REL_L2 = 1e-2
+F32_REL_L2 = 1e-4
+
+# Per-op tolerances: one bf16 rounding of the output dominates (2^-9 relative).
+OP_TOL = {"bf16": dict(rel=6e-3, attn_rel=1.2e-2), "fp32": dict(rel=1e-5, attn_rel=1e-5)}
+
+
+def check_all_ops(case: Case, n_bands: int, stride: int = 1):
+    n_ops = case.dec.num_ops(case.shape, n_bands)
+    assert n_ops > 5
+    tol = OP_TOL[case.dtype]
+    seen = set()
+    for op in range(0, n_ops, stride):
+        d, x, aux, y = case.capture(n_bands, op)
+        seen.add(d["kind"] + ":" + d.get("conv", ""))
+        in_shape = parse_shape(d["in"])
+        if d["kind"] == "latent":
+            xin = x.reshape(case.shape)
+            exp = np.moveaxis(xin, 1, -1) if xin.ndim == 4 else np.moveaxis(xin, 1, -1)
+            np.testing.assert_array_equal(y.reshape(exp.shape), exp)
+            continue
+        ref = oracle_op(d, case.W, case.arch, x.reshape(in_shape), aux)
+        got = y.reshape(ref.shape)
+        lim = tol["attn_rel"] if d["kind"] == "attention" else tol["rel"]
+        err = rel_l2(got, ref)
+        assert err <= lim, f"op {op} {d}: rel-L2 {err:.3e} > {lim}"
+    return seen
+
+
+# ---------------------------------------------------------------- fp32 path
+@pytest.fixture(scope="module")
+def tiny():
+    w = synth.WORKLOADS["kl_tiny_fp32"]
+    return Case(w.arch, w.dtype, w.latent_shape)
+
+
+def test_tiny_fp32_every_op(tiny):
+    kinds = check_all_ops(tiny, 2)
+    assert {"conv:k3", "conv:up2x_k3", "groupnorm:", "attention:"} <= kinds
+
+
+def test_tiny_fp32_decode_matches_oracle(tiny):
+    out = tiny.decode(2)
+    ref = tiny.oracle()
+    got = out.float().cpu().numpy()
+    assert got.shape == ref.shape
+    assert rel_l2(got, ref) <= F32_REL_L2
+
+
+def test_tiny_fp32_band_count_bitwise(tiny):
+    base = tiny.decode(1).cpu()
+    for nb in (2, 3, 16):
+        assert bool((tiny.decode(nb).cpu() == base).all()), nb
+
+
+# ---------------------------------------------------------------- bf16 KL path
+@pytest.fixture(scope="module")
+def kl_ops():
+    # full Z-Image channel widths on a small, ragged latent (6 x 12)
+    return Case(synth.KL_ZIMAGE, "bf16", (1, 16, 6, 12))
+
+
+def test_kl_bf16_every_op(kl_ops):
+    kinds = check_all_ops(kl_ops, 3)
+    assert {"conv:k3", "conv:k1", "conv:up2x_k3", "groupnorm:", "attention:"} <= kinds
+
+
+@pytest.fixture(scope="module")
+def kl_small():
+    return Case(synth.KL_ZIMAGE, "bf16", (1, 16, 12, 20))
+
+
+def test_kl_bf16_decode_matches_oracle(kl_small):
+    out = kl_small.decode(3).float().cpu().numpy()
+    ref = kl_small.oracle()
+    assert out.shape == ref.shape == (1, 3, 96, 160)
+    e_abs, e_rel = max_abs(out, ref), rel_l2(out, ref)
+    assert e_abs <= BF16_MAX_ABS and e_rel <= BF16_REL_L2, (e_abs, e_rel)
+
+
+def test_kl_bf16_band_count_bitwise(kl_small):
+    base = kl_small.decode(1).cpu()
+    for nb in (2, 3, 5, 12):
+        assert bool((kl_small.decode(nb).cpu() == base).all()), nb
+
+
+def test_kl_bf16_batch2_uneven_bands():
+    # batch 2, 10 latent rows in 3 bands (4/3/3): element-count-weighted merge, unequal halos
+    case = Case(synth.KL_ZIMAGE, "bf16", (2, 16, 10, 8), zseed=3)
+    out = case.decode(3).float().cpu().numpy()
+    ref = case.oracle(3)
+    e_abs, e_rel = max_abs(out, ref), rel_l2(out, ref)
+    assert e_abs <= BF16_MAX_ABS and e_rel <= BF16_REL_L2, (e_abs, e_rel)
+    assert bool((case.decode(1).cpu() == case.decode(3).cpu()).all())
+
+
+# ---------------------------------------------------------------- bf16 Wan path
+@pytest.fixture(scope="module")
+def wan_small():
+    return Case(synth.WAN, "bf16", (1, 16, 2, 6, 8))
+
+
+def test_wan_bf16_every_op(wan_small):
+    kinds = check_all_ops(wan_small, 2)
+    assert {"conv:causal3", "conv:time", "conv:up2x_k3", "rmsnorm:", "attention:"} <= kinds
+
+
+def test_wan_bf16_decode_matches_oracle(wan_small):
+    out = wan_small.decode(2).float().cpu().numpy()
+    ref = wan_small.oracle()
+    assert out.shape == ref.shape == (1, 3, 5, 48, 64)
+    e_abs, e_rel = max_abs(out, ref), rel_l2(out, ref)
+    assert e_abs <= BF16_MAX_ABS and e_rel <= BF16_REL_L2, (e_abs, e_rel)
+
+
+def test_wan_bf16_band_count_bitwise(wan_small):
+    base = wan_small.decode(1).cpu()
+    for nb in (2, 3, 6):
+        assert bool((wan_small.decode(nb).cpu() == base).all()), nb
+
+
+# ---------------------------------------------------------------- host-side errors with a live handle
+def test_bad_band_counts_rejected(kl_small):
+    import row_band_layerwise_gb300 as rbl
+    for nb in (0, 13, -1):
+        with pytest.raises(rbl.VaedecError):
+            kl_small.dec.decode(kl_small.z_dev, nb)
+    # the handle stays usable
+    assert kl_small.decode(2).shape == (1, 3, 96, 160)
+
+
+def test_shape_above_max_rejected(kl_small):
+    import torch
+    import row_band_layerwise_gb300 as rbl
+    z = torch.zeros((1, 16, 13, 20), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rbl.VaedecError):
+        kl_small.dec.decode(z, 1)
