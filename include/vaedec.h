@@ -153,6 +153,33 @@ vaedec_status vaedec_launch_count(const vaedec_t* h, uint64_t* n);
 vaedec_status vaedec_profile_enable(vaedec_t* h, int enable);
 vaedec_status vaedec_profile_read(vaedec_t* h, float* ms, int max_ops, int* n_ops);
 
+/* ---- GroupNorm without device allocation --------------------------------------------
+ * The pages have no counterpart for this entry point; it serves callers that cannot
+ * allocate device memory while they run: plugin hosts and inference servers that give
+ * a plugin only its input/output buffers and forbid cudaMalloc inside their enqueue
+ * callback, real-time pipelines whose memory is fixed at start-up, and code living
+ * under another allocator.  It runs the same GroupNorm kernels as the decoder
+ * (fixed one-row chunks of central moments, the weighted merge, scale/shift + optional
+ * SiLU) on one channels-last tensor, with all scratch in one fixed 2.25 MiB array
+ * compiled into this library.  It calls no cudaMalloc, cudaFree or allocating routine.
+ *
+ *   x      DEVICE [B][rows][W][C], in_dtype (VAEDEC_DTYPE_F32 or VAEDEC_DTYPE_BF16), 16-byte aligned
+ *   y      DEVICE [B][rows][W][C], out_dtype (f32->bf16, f32->f32 or bf16->bf16), 16-byte aligned
+ *   gamma, beta  DEVICE fp32 [C];  groups G divide C;  C a multiple of 8, at most 2048
+ *   stream a cudaStream_t (NULL = legacy default stream); asynchronous
+ * Limits of the fixed scratch: B * rows * G <= 131072 and B * C <= 32768; larger sizes
+ * return VAEDEC_ERR_INVALID_ARG with a message naming the limit, before any launch.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * once per device, with that device current); make that first call before any stream
+ * capture.  Every call shares the array and leaves its last contents there; nothing in
+ * it has to start at zero (each call writes every word it reads), but calls whose
+ * kernels overlap on the GPU (e.g. on two streams) race on it and must be ordered by
+ * the caller.  Every GPU that loads this library holds the array until process exit.
+ */
+vaedec_status vaedec_groupnorm_noalloc(int in_dtype, int out_dtype, const void* x, void* y, int B, int rows, int W,
+                                       int C, int G, const float* gamma, const float* beta, float eps, int silu,
+                                       void* stream);
+
 /* ---- Inspection (tests and profiling) ------------------------------------------------
  * The decode is a fixed list of ops (latent layout, conv, groupnorm, rmsnorm,
  * attention block, temporal upsample).  These calls describe that list for a latent

@@ -28,6 +28,7 @@ EXPORTED_SYMBOLS = (
     "vaedec_decode", "vaedec_decode_host", "vaedec_sync", "vaedec_last_error",
     "vaedec_launch_count", "vaedec_profile_enable", "vaedec_profile_read",
     "vaedec_debug_num_ops", "vaedec_debug_op_desc", "vaedec_debug_run_until",
+    "vaedec_groupnorm_noalloc",
 )
 
 
@@ -85,6 +86,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.vaedec_debug_op_desc.argtypes = [vp, i64p, i, i, i, ctypes.c_char_p, i]
     lib.vaedec_debug_run_until.argtypes = [vp, vp, i64p, i, i, i, vp, ctypes.c_size_t, vp, ctypes.c_size_t,
                                            vp, ctypes.c_size_t, vp]
+    lib.vaedec_groupnorm_noalloc.argtypes = [i, i, vp, vp, i, i, i, i, i, vp, vp, ctypes.c_float, i, vp]
     for name in EXPORTED_SYMBOLS:
         if name not in ("vaedec_destroy", "vaedec_last_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -129,6 +131,22 @@ def make_config(arch, dtype: str, max_latent: Sequence[int]) -> _Config:
     for k in range(4):
         c.max_latent[k] = int(max_latent[k])
     return c
+
+
+def groupnorm_noalloc(x, y, groups: int, gamma, beta, eps: float, silu: bool, stream=None) -> None:
+    """GroupNorm (+SiLU) of a channels-last [B, rows, W, C] device tensor into ``y`` without
+    any device allocation (scratch lives in a fixed array inside the library).
+
+    ``gamma``/``beta`` are fp32 device tensors of C values.  Asynchronous on ``stream``.
+    """
+    lib = load_library()
+    torch = _torch()
+    dt = {torch.float32: DTYPE["fp32"], torch.bfloat16: DTYPE["bf16"]}
+    B, rows, W, C = (int(v) for v in x.shape)
+    st = torch.cuda.current_stream() if stream is None else stream
+    _check(lib, lib.vaedec_groupnorm_noalloc(dt[x.dtype], dt[y.dtype], x.data_ptr(), y.data_ptr(), B, rows, W, C,
+                                             int(groups), gamma.data_ptr(), beta.data_ptr(), float(eps),
+                                             1 if silu else 0, int(st.cuda_stream)))
 
 
 def _torch():

@@ -410,7 +410,8 @@ class Walker {
     std::ostringstream d;
     d << "kind=conv name=" << name << " conv="
       << (kind == K3 ? "k3" : kind == K1 ? "k1" : kind == C3 ? "causal3" : kind == UP ? "up2x_k3" : "time")
-      << io(x, res, y) << " res=" << (res ? 1 : 0) << " final=" << (final_out ? 1 : 0);
+      << io(x, res, y) << " res=" << (res ? 1 : 0) << " final=" << (final_out ? 1 : 0) << " taps=" << w->ntaps
+      << " flops=" << conv_flops(x, y, *w, kind);
     if (begin(d.str())) {
       ConvGeom g;
       std::memset(&g, 0, sizeof(g));
@@ -456,6 +457,18 @@ class Walker {
     }
     end(&x, res, y);
     return y;
+  }
+
+  // Algorithmic multiply-add work of a conv op (2 flops per MAC): every output
+  // element is a dot product over taps x C_in (the upsampled conv counts its
+  // 3x3 taps on the high-resolution output, the time conv its frames 1..T-1).
+  static double conv_flops(const Act& x, const Act& y, const DevConv& w, ConvKind kind) {
+    double out_pix = (double)y.pixels();
+    double n = (double)w.cout;
+    if (kind == TIME) {
+      out_pix = (double)x.B * (x.T - 1) * x.H * x.W;   // time-conv outputs (2C channels each)
+    }
+    return 2.0 * out_pix * n * (double)w.ntaps * (double)x.C;
   }
 
   // GroupNorm: x (any dtype) -> operand dtype; `raw` (optional) receives x cast.
@@ -541,8 +554,12 @@ class Walker {
       plan->l = std::max(plan->l, (size_t)maxrows * x.W);
     }
     note_act(y);
+    // projections 4 x (2 N C^2) plus scores and probabilities x values 2 x (2 N^2 C), per sequence
+    const double attn_flops = (double)F * (8.0 * (double)Ntok * C * C + 4.0 * (double)Ntok * (double)Ntok * C);
+    std::ostringstream fl;
+    fl << attn_flops;
     const bool run = begin("kind=attention name=" + prefix + io(x, nullptr, y) + " wan=" + (wan ? "1" : "0") +
-                           " bands=" + std::to_string(n_bands_));
+                           " bands=" + std::to_string(n_bands_) + " flops=" + fl.str());
     ++nest_;
     if (live()) {
       // normalisation (GroupNorm for KL, channel RMSNorm for Wan), no SiLU
@@ -904,6 +921,8 @@ vaedec_status check_latent(const vaedec* h, const int64_t* shape, int ndim, int 
 }
 
 }  // namespace
+
+void vd::record_last_error(const std::string& message) { g_err = message; }
 
 // ====================================================================== C ABI
 extern "C" {

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <string>
 
 #include "conv.h"
 
@@ -60,5 +61,8 @@ cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv
 // [B][C][S] -> [B][S][C] (same dtype).
 cudaError_t launch_to_channels_last(int dtype, const void* x, void* y, int B, int C, long long spatial,
                                     cudaStream_t stream);
+
+// Message returned by vaedec_last_error() on the calling thread.
+void record_last_error(const std::string& message);
 
 }  // namespace vd
