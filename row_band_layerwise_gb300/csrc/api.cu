@@ -24,7 +24,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/vaedec.h"
+#include "vaedec.h"
 #include "kernels.h"
 
 using namespace vd;

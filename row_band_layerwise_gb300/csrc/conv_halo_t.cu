@@ -1,0 +1,412 @@
+// Channel-major halo-tile convolution on tcgen05 tensor cores.
+//
+// The GEMM is laid out with output channels on M (128 per CTA) and pixels on N
+// (one image row segment of up to 256 pixels): D[co, x] += W[co, tap, ci] *
+// in[x + offset(tap), ci].  As in the pixel-major halo kernel, every input
+// channel chunk stages the R + 2 input rows a tile needs once (zero-filled
+// outside the image: the global-edge padding; real rows across band boundaries:
+// the halo of "VAEP：VAE 并行解码", 卷积：交换边界行), and each 3x3 tap reads those
+// rows through a shared-memory descriptor shifted by whole pixels.  Putting
+// pixels on N gives 256-wide MMAs for every layer (also the 128-channel ones),
+// which keeps the tensor pipe at its full rate, and makes every TMEM lane one
+// output channel, so each epilogue store instruction writes 32 consecutive
+// channels of one pixel: fully coalesced, with residual reads batched 32 deep.
+//
+// Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
+// warps 2..5 epilogue.  A weight stage holds the three taps of one kernel row,
+// so each stage wait is followed by ~1500 cycles of MMA work.  Waits are
+// bounded (ptx.cuh).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "conv.h"
+#include "epilogue.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace vd {
+
+namespace {
+
+constexpr int kThreadsT = 192;
+constexpr int kMaxWStages = 4;
+constexpr int kPipeBytesT = 212 * 1024;
+
+struct HaloTParams {
+  CUtensorMap tmX;               // activations 5D (Cin, W, H, T, B), box (BK, half, 1, 1, 1)
+  CUtensorMap tmW;               // weights 3D (Cin, ntaps_w, rows), box (BK, 1, 128)
+  ConvGeom g;
+  int R;                         // output rows per CTA
+  int npx;                       // pixels per tile (MMA N)
+  int half;                      // pixels per staging box (two boxes per staged row)
+  int tiles_x, tiles_y, n_mtiles, n_kchunks, ndt, nw;
+  uint32_t row_bytes, x_stage_bytes, w_tap_bytes, w_stage_bytes, tmem_cols;
+  const float* bias;
+  const void* residual;
+  void* out;
+  __nv_bfloat16* out2;
+  int* status;
+};
+
+template <int BK>
+struct SwzT {
+  static constexpr uint32_t kSbo = BK * 2 * 8;
+  static constexpr uint32_t kMode = BK == 64 ? 2u : (BK == 32 ? 4u : 6u);
+};
+
+template <int BK>
+__global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_constant__ HaloTParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t x_full[2], x_empty[2];
+  __shared__ __align__(8) uint64_t w_full[kMaxWStages], w_empty[kMaxWStages];
+  __shared__ __align__(8) uint64_t accum_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+
+  const ConvGeom& g = p.g;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smX = smem;
+  uint8_t* smW = smem + 2 * p.x_stage_bytes;
+
+  int bid = blockIdx.x;
+  const int mtile = bid % p.n_mtiles;
+  bid /= p.n_mtiles;
+  const int phase = bid % g.nphase;
+  bid /= g.nphase;
+  const int tx = bid % p.tiles_x;
+  bid /= p.tiles_x;
+  const int ty = bid % p.tiles_y;
+  bid /= p.tiles_y;
+  const int tt = bid % g.T;
+  const int bb = bid / g.T;
+  const int x0 = tx * p.npx, y0 = ty * p.R, m0 = mtile * 128;
+  const int nsp = g.ntaps / p.ndt;   // 9 spatial taps per causal frame, in three kernel rows of 3
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_empty[i], 1);
+    }
+    for (int i = 0; i < p.nw; ++i) {
+      mbar_init(&w_full[i], 1);
+      mbar_init(&w_empty[i], 1);
+    }
+    mbar_init(&accum_bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmX);
+    tma_prefetch_desc(&p.tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int nac = p.ndt * p.n_kchunks;   // staged activation chunks
+  const int ngrp = nsp / 3;              // weight stages per chunk (kernel rows)
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint32_t x_tx = static_cast<uint32_t>((p.R + 2) * 2 * p.half * BK * 2);
+      const uint32_t w_tx = static_cast<uint32_t>(3 * 128 * BK * 2);
+      int kb = 0, issued_x = 0, issued_w = 0;
+      for (int ac = 0; ac < nac && !abort_flag; ++ac) {
+        const int dti = ac / p.n_kchunks;
+        const int kc = ac - dti * p.n_kchunks;
+        const int dt = g.taps[phase][dti * nsp].dt;
+        const int sx = ac & 1;
+        if (ac >= 2 && !mbar_wait(&x_empty[sx], (static_cast<uint32_t>(ac >> 1) & 1u) ^ 1u, p.status,
+                                  kErrTimeoutEmpty, &abort_flag))
+          break;
+        mbar_arrive_expect_tx(&x_full[sx], x_tx);
+        uint8_t* xs = smX + sx * p.x_stage_bytes;
+        for (int rb = 0; rb < p.R + 2; ++rb) {
+          tma_load_5d(xs + rb * p.row_bytes, &p.tmX, &x_full[sx], kc * BK, x0 - 1, y0 - 1 + rb, tt + dt, bb);
+          tma_load_5d(xs + rb * p.row_bytes + p.half * BK * 2, &p.tmX, &x_full[sx], kc * BK, x0 - 1 + p.half,
+                      y0 - 1 + rb, tt + dt, bb);
+        }
+        issued_x = ac + 1;
+        for (int gi = 0; gi < ngrp; ++gi, ++kb) {
+          const int sw = kb % p.nw;
+          if (kb >= p.nw && !mbar_wait(&w_empty[sw], (static_cast<uint32_t>(kb / p.nw) & 1u) ^ 1u, p.status,
+                                       kErrTimeoutEmpty, &abort_flag))
+            break;
+          mbar_arrive_expect_tx(&w_full[sw], w_tx);
+          uint8_t* ws = smW + sw * p.w_stage_bytes;
+          for (int t = 0; t < 3; ++t)
+            tma_load_3d(ws + t * p.w_tap_bytes, &p.tmW, &w_full[sw], kc * BK,
+                        g.taps[phase][dti * nsp + gi * 3 + t].wtap, m0);
+          issued_w = kb + 1;
+        }
+      }
+      if (abort_flag) {
+        int dummy = 0;
+        volatile int no_abort = 0;
+        for (int ac = max(0, issued_x - 2); ac < issued_x; ++ac)
+          mbar_wait(&x_full[ac & 1], static_cast<uint32_t>(ac >> 1) & 1u, &dummy, 0, &no_abort);
+        for (int k = max(0, issued_w - p.nw); k < issued_w; ++k)
+          mbar_wait(&w_full[k % p.nw], static_cast<uint32_t>(k / p.nw) & 1u, &dummy, 0, &no_abort);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, p.npx);
+      const uint32_t x_base0 = smem_u32(smX), w_base0 = smem_u32(smW);
+      int kb = 0;
+      bool ok = true;
+      for (int ac = 0; ac < nac && ok; ++ac) {
+        const int dti = ac / p.n_kchunks;
+        const int sx = ac & 1;
+        if (!mbar_wait(&x_full[sx], static_cast<uint32_t>(ac >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t xb = x_base0 + sx * p.x_stage_bytes;
+        for (int gi = 0; gi < ngrp; ++gi, ++kb) {
+          const int sw = kb % p.nw;
+          if (!mbar_wait(&w_full[sw], static_cast<uint32_t>(kb / p.nw) & 1u, p.status, kErrTimeoutFull,
+                         &abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t wb = w_base0 + sw * p.w_stage_bytes;
+          for (int t = 0; t < 3; ++t) {
+            const ConvTap tp = g.taps[phase][dti * nsp + gi * 3 + t];
+            const uint32_t wa = wb + t * p.w_tap_bytes;
+            for (int r = 0; r < p.R; ++r) {
+              const uint32_t xa = xb + (r + tp.dy + 1) * p.row_bytes + static_cast<uint32_t>((tp.dx + 1) * BK * 2);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                const uint64_t da = smem_desc_kmajor(wa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
+                const uint64_t db = smem_desc_kmajor(xa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
+                tc_mma_bf16(tmem + static_cast<uint32_t>(r * p.npx), da, db, idesc, (ac | gi | t | k) != 0 ? 1u : 0u);
+              }
+            }
+          }
+          tc_commit(&w_empty[sw]);
+        }
+        tc_commit(&x_empty[sx]);
+      }
+      tc_commit(&accum_bar);
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: TMEM lane = output channel; columns = pixels of the tile row
+    const int q = warp & 3;
+    const int co = m0 + q * 32 + lane;
+    const bool cvalid = co < g.Cout;
+    const float bias = (p.bias != nullptr && cvalid) ? p.bias[co] : 0.f;
+    const bool ok = mbar_wait(&accum_bar, 0, p.status, kErrTimeoutAccum, &abort_flag);
+    tc_fence_after();
+    const bool go = __all_sync(0xffffffffu, ok && !abort_flag);
+    if (go) {
+      const int py = phase >> 1, px = phase & 1;
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      const bool res_f32 = g.res_f32 != 0;
+      for (int r = 0; r < p.R; ++r) {
+        const int y = y0 + r;
+        if (y >= g.H) break;   // uniform across the warp
+        const int yo = y * g.osy + (g.nphase > 1 ? py : 0);
+        const long long row_pix = ((static_cast<long long>(bb) * g.oT + tt) * g.oH + yo) * static_cast<long long>(g.oW);
+        for (int c0 = 0; c0 < p.npx; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld_32x32b_x32(lane_addr + static_cast<uint32_t>(r * p.npx + c0), rr);
+          tmem_ld_wait();
+          const int nvalid = min(32, min(p.npx - c0, g.W - (x0 + c0)));
+          if (nvalid <= 0) break;
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]) * g.scale + bias;
+          // element offset of (pixel x0 + c0 + j, channel co)
+          const long long px0 = row_pix + static_cast<long long>(x0 + c0) * g.osx + (g.nphase > 1 ? px : 0);
+          const long long stride = static_cast<long long>(g.osx) * g.oC;
+          const long long e0 = px0 * g.oC + co;
+          if (p.residual != nullptr && cvalid) {
+            if (res_f32) {
+              const float* rp = reinterpret_cast<const float*>(p.residual) + e0;
+              float rv[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) rv[j] = (j < nvalid) ? rp[j * stride] : 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += rv[j];
+            } else {
+              const __nv_bfloat16* rp = reinterpret_cast<const __nv_bfloat16*>(p.residual) + e0;
+              float rv[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) rv[j] = (j < nvalid) ? __bfloat162float(rp[j * stride]) : 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += rv[j];
+            }
+          }
+          if (cvalid) {
+            if (g.out_f32) {
+              float* op = reinterpret_cast<float*>(p.out) + e0;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < nvalid) op[j * stride] = v[j];
+            } else {
+              __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(p.out) + e0;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < nvalid) op[j * stride] = __float2bfloat16_rn(v[j]);
+            }
+            if (p.out2 != nullptr) {
+              __nv_bfloat16* op = p.out2 + e0;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < nvalid) op[j * stride] = __float2bfloat16_rn(v[j]);
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+int round_up_t(int a, int b) { return (a + b - 1) / b * b; }
+
+}  // namespace
+
+// Channel-major halo kernel: 3x3 spatial taps (in groups of three per kernel row,
+// optionally per causal frame or per upsample phase), channels-last output, and
+// rows wide enough for at least 96-pixel tiles.
+bool conv_halo_t_applicable(const ConvGeom& g) {
+  if (g.out_chfirst || g.time_up_c > 0) return false;
+  if (g.ntaps != 9 && g.ntaps != 27) return false;
+  if (g.W < 96) return false;
+  if (g.Cout % 16 != 0 || g.Cin % 16 != 0) return false;
+  const int ndt = g.ntaps / 9;
+  for (int ph = 0; ph < g.nphase; ++ph)
+    for (int d = 0; d < ndt; ++d)
+      for (int s = 0; s < 9; ++s) {
+        const ConvTap t = g.taps[ph][d * 9 + s];
+        if (t.dt != g.taps[ph][d * 9].dt) return false;
+        if (t.dy < -1 || t.dy > 1 || t.dx < -1 || t.dx > 1) return false;
+      }
+  return true;
+}
+
+cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
+                               const float* bias, const void* residual, void* out, void* out2, int* status,
+                               cudaStream_t stream, const char** why) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) {
+    *why = "cuTensorMapEncodeTiled unavailable";
+    return cudaErrorNotSupported;
+  }
+  HaloTParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.g = g;
+  // pixel tile: split the row into equal tiles of at most 256 pixels (multiple of 16)
+  const int ntx = (g.W + 255) / 256;
+  p.npx = round_up_t((g.W + ntx - 1) / ntx, 16);
+  p.tiles_x = (g.W + p.npx - 1) / p.npx;
+  p.half = round_up_t(p.npx + 2, 16) / 2;          // two boxes per staged row, multiple of 8 pixels each
+  p.R = std::max(1, std::min(4, 512 / p.npx));
+  while (p.R > 1 && p.R > g.H) --p.R;
+  p.n_mtiles = (g.Cout + 127) / 128;   // weight rows beyond w_rows read as zeros
+  int bk = 0;
+  for (int cand : {64, 32, 16}) {
+    if (g.Cin % cand != 0) continue;
+    const int x_stage = (p.R + 2) * 2 * p.half * cand * 2;
+    const int w_stage = 3 * 128 * cand * 2;
+    if (2 * x_stage + 2 * w_stage <= kPipeBytesT) {
+      bk = cand;
+      break;
+    }
+  }
+  if (bk == 0) {
+    *why = "no channel-major halo tile fits shared memory";
+    return cudaErrorInvalidValue;
+  }
+  p.n_kchunks = g.Cin / bk;
+  p.ndt = g.ntaps / 9;
+  p.row_bytes = static_cast<uint32_t>(2 * p.half * bk * 2);
+  p.x_stage_bytes = static_cast<uint32_t>((p.R + 2) * p.row_bytes);
+  p.w_tap_bytes = static_cast<uint32_t>(128 * bk * 2);
+  p.w_stage_bytes = 3 * p.w_tap_bytes;
+  p.nw = std::min(kMaxWStages, static_cast<int>((kPipeBytesT - 2 * p.x_stage_bytes) / p.w_stage_bytes));
+  p.tiles_y = (g.H + p.R - 1) / p.R;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < static_cast<uint32_t>(p.R * p.npx)) p.tmem_cols <<= 1;
+  p.bias = bias;
+  p.residual = residual;
+  p.out = out;
+  p.out2 = static_cast<__nv_bfloat16*>(out2);
+  p.status = status;
+
+  const cuuint32_t ones[5] = {1, 1, 1, 1, 1};
+  {
+    const cuuint64_t dims[5] = {(cuuint64_t)g.Cin, (cuuint64_t)g.W, (cuuint64_t)g.H, (cuuint64_t)g.T,
+                                (cuuint64_t)g.B};
+    const cuuint64_t strides[4] = {dims[0] * 2, dims[0] * dims[1] * 2, dims[0] * dims[1] * dims[2] * 2,
+                                   dims[0] * dims[1] * dims[2] * dims[3] * 2};
+    const cuuint32_t box[5] = {(cuuint32_t)bk, (cuuint32_t)p.half, 1, 1, 1};
+    if (enc(&p.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(in), dims, strides, box, ones,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      *why = "channel-major halo activation tensor map rejected";
+      return cudaErrorInvalidValue;
+    }
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)g.Cin, (cuuint64_t)ntaps_w, (cuuint64_t)w_rows};
+    const cuuint64_t strides[2] = {dims[0] * 2, dims[0] * dims[1] * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)bk, 1, 128};
+    if (enc(&p.tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(wts), dims, strides, box, ones,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      *why = "channel-major halo weight tensor map rejected";
+      return cudaErrorInvalidValue;
+    }
+  }
+  const long long nblocks = (long long)g.B * g.T * p.tiles_y * p.tiles_x * g.nphase * p.n_mtiles;
+  if (nblocks <= 0) return cudaSuccess;
+  if (nblocks > 0x7fffffffLL) {
+    *why = "grid too large";
+    return cudaErrorInvalidValue;
+  }
+  const size_t smem = 2 * (size_t)p.x_stage_bytes + (size_t)p.nw * p.w_stage_bytes + 1024;
+  cudaError_t e;
+  switch (bk) {
+    case 64:
+      e = cudaFuncSetAttribute(conv_halo_t_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) conv_halo_t_kernel<64><<<(unsigned)nblocks, kThreadsT, smem, stream>>>(p);
+      break;
+    case 32:
+      e = cudaFuncSetAttribute(conv_halo_t_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) conv_halo_t_kernel<32><<<(unsigned)nblocks, kThreadsT, smem, stream>>>(p);
+      break;
+    default:
+      e = cudaFuncSetAttribute(conv_halo_t_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) conv_halo_t_kernel<16><<<(unsigned)nblocks, kThreadsT, smem, stream>>>(p);
+      break;
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace vd

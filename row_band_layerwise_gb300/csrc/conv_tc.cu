@@ -23,8 +23,10 @@
 #include <cstring>
 
 #include "conv.h"
-#include "ptx.cuh"
+#include "epilogue.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
+#include "tma_host.h"
 
 namespace vd {
 
@@ -54,73 +56,6 @@ struct SwizzleOf {
   static constexpr uint32_t kSbo = BK * 2 * 8;
   static constexpr uint32_t kMode = BK == 64 ? 2u : (BK == 32 ? 4u : 6u);
 };
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// 16 consecutive channels of one pixel: 64-byte (fp32) or 32-byte (bf16) vector
-// accesses when all 16 are valid, scalar otherwise.
-__device__ __forceinline__ void add_f32x16(float (&v)[16], const float* r, int n) {
-  if (n == 16) {
-    const float4* r4 = reinterpret_cast<const float4*>(r);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float4 a = r4[j];
-      v[4 * j] += a.x;
-      v[4 * j + 1] += a.y;
-      v[4 * j + 2] += a.z;
-      v[4 * j + 3] += a.w;
-    }
-  } else {
-    for (int j = 0; j < n; ++j) v[j] += r[j];
-  }
-}
-
-__device__ __forceinline__ void add_bf16x16(float (&v)[16], const __nv_bfloat16* r, int n) {
-  if (n == 16) {
-    const uint4* rp = reinterpret_cast<const uint4*>(r);
-    uint4 r0 = rp[0], r1 = rp[1];
-    const __nv_bfloat16* h0 = reinterpret_cast<const __nv_bfloat16*>(&r0);
-    const __nv_bfloat16* h1 = reinterpret_cast<const __nv_bfloat16*>(&r1);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      v[j] += __bfloat162float(h0[j]);
-      v[8 + j] += __bfloat162float(h1[j]);
-    }
-  } else {
-    for (int j = 0; j < n; ++j) v[j] += __bfloat162float(r[j]);
-  }
-}
-
-__device__ __forceinline__ void store_f32x16(float* o, const float (&v)[16], int n) {
-  if (n == 16) {
-    float4* o4 = reinterpret_cast<float4*>(o);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-  } else {
-    for (int j = 0; j < n; ++j) o[j] = v[j];
-  }
-}
-
-__device__ __forceinline__ void store_bf16x16(__nv_bfloat16* o, const float (&v)[16], int n) {
-  if (n == 16) {
-    uint4 w0, w1;
-    w0.x = pack_bf16x2(v[0], v[1]);
-    w0.y = pack_bf16x2(v[2], v[3]);
-    w0.z = pack_bf16x2(v[4], v[5]);
-    w0.w = pack_bf16x2(v[6], v[7]);
-    w1.x = pack_bf16x2(v[8], v[9]);
-    w1.y = pack_bf16x2(v[10], v[11]);
-    w1.z = pack_bf16x2(v[12], v[13]);
-    w1.w = pack_bf16x2(v[14], v[15]);
-    reinterpret_cast<uint4*>(o)[0] = w0;
-    reinterpret_cast<uint4*>(o)[1] = w1;
-  } else {
-    for (int j = 0; j < n; ++j) o[j] = __float2bfloat16_rn(v[j]);
-  }
-}
 
 template <int BK>
 __global__ void __launch_bounds__(kThreads, 1) conv_tc_kernel(const __grid_constant__ ConvTcParams p) {
@@ -211,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_tc_kernel(const __grid_const
         }
       }
     }
+    __syncwarp();   // reconverge warp 0 before the CTA-wide barrier
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kBM, p.BN);
@@ -259,39 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_tc_kernel(const __grid_const
         float v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) * g.scale * rs + bias_sh[c0 + j];
-        int to = tt, ch0 = co0, oc = g.oC;
-        if (g.time_up_c > 0) {
-          const int half = co0 >= g.time_up_c ? 1 : 0;
-          to = 1 + 2 * tt + half;
-          ch0 = co0 - half * g.time_up_c;
-        }
-        const long long opix = ((static_cast<long long>(bb) * g.oT + to) * g.oH + yo) * g.oW + xo;
-        const int nvalid = min(16, g.Cout - co0);
-        if (!g.out_chfirst) {
-          const long long base = opix * oc + ch0;
-          if (p.residual != nullptr) {
-            if (g.res_f32)
-              add_f32x16(v, reinterpret_cast<const float*>(p.residual) + base, nvalid);
-            else
-              add_bf16x16(v, reinterpret_cast<const __nv_bfloat16*>(p.residual) + base, nvalid);
-          }
-          if (g.out_f32)
-            store_f32x16(reinterpret_cast<float*>(p.out) + base, v, nvalid);
-          else
-            store_bf16x16(reinterpret_cast<__nv_bfloat16*>(p.out) + base, v, nvalid);
-          if (p.out2 != nullptr) store_bf16x16(p.out2 + base, v, nvalid);
-        } else {
-          // channels-first [B][oC][oT][oH][oW]
-          const long long plane = static_cast<long long>(g.oT) * g.oH * g.oW;
-          const long long sp = ((static_cast<long long>(to)) * g.oH + yo) * g.oW + xo;
-          for (int j = 0; j < nvalid; ++j) {
-            const long long a = (static_cast<long long>(bb) * oc + ch0 + j) * plane + sp;
-            if (g.out_f32)
-              reinterpret_cast<float*>(p.out)[a] = v[j];
-            else
-              reinterpret_cast<__nv_bfloat16*>(p.out)[a] = __float2bfloat16_rn(v[j]);
-          }
-        }
+        epilogue_store16(g, v, bb, tt, yo, xo, co0, p.residual, p.out, p.out2);
       }
     }
     tc_fence_before();
@@ -305,12 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1) conv_tc_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------- host side
-namespace {
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 EncodeTiledFn get_encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static bool tried = false;
@@ -329,6 +227,8 @@ EncodeTiledFn get_encode_fn() {
 CUtensorMapSwizzle swizzle_for(int bk) {
   return bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
 }
+
+namespace {
 
 int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
@@ -361,6 +261,14 @@ cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, i
     *why = e;
     return cudaErrorInvalidValue;
   }
+  if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(wts) & 15)) {
+    *why = "conv operands must be 16-byte aligned";
+    return cudaErrorInvalidValue;
+  }
+  if (rowscale == nullptr && conv_halo_t_applicable(g))
+    return launch_conv_halo_t(g, in, wts, ntaps_w, w_rows, bias, residual, out, out2, status, stream, why);
+  if (rowscale == nullptr && conv_halo_applicable(g))
+    return launch_conv_halo(g, in, wts, ntaps_w, w_rows, bias, residual, out, out2, status, stream, why);
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) {
     *why = "cuTensorMapEncodeTiled unavailable";

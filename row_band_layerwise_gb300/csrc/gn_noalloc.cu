@@ -19,7 +19,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/vaedec.h"
+#include "vaedec.h"
 #include "kernels.h"
 
 using namespace vd;

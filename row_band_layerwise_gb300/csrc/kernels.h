@@ -19,6 +19,19 @@ cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, i
                            const float* bias, const void* residual, const float* rowscale, void* out, void* out2,
                            int* status, cudaStream_t stream, const char** why);
 
+// Halo-tile variant (R output rows per CTA, activations staged once per channel
+// chunk for all 3x3 taps); launch_conv_tc dispatches to it when applicable.
+bool conv_halo_applicable(const ConvGeom& g);
+cudaError_t launch_conv_halo(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
+                             const float* bias, const void* residual, void* out, void* out2, int* status,
+                             cudaStream_t stream, const char** why);
+
+// Channel-major halo variant (output channels on M, up to 256 pixels on N).
+bool conv_halo_t_applicable(const ConvGeom& g);
+cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
+                               const float* bias, const void* residual, void* out, void* out2, int* status,
+                               cudaStream_t stream, const char** why);
+
 // CUDA-core fp32 direct convolution over the same ConvGeom (the fp32 path).
 // `wts` is [w_rows][ntaps_w][Cin] fp32.
 cudaError_t launch_conv_simple_f32(const ConvGeom& g, const float* in, const float* wts, int ntaps_w,

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_helpers import Case, max_abs, oracle_op, parse_shape, rel_l2
+from gpu_helpers import Case, assert_bf16_parity, max_abs, oracle_op, parse_shape, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -93,8 +93,7 @@ def test_kl_bf16_decode_matches_oracle(kl_small):
     out = kl_small.decode(3).float().cpu().numpy()
     ref = kl_small.oracle()
     assert out.shape == ref.shape == (1, 3, 96, 160)
-    e_abs, e_rel = max_abs(out, ref), rel_l2(out, ref)
-    assert e_abs <= BF16_MAX_ABS and e_rel <= BF16_REL_L2, (e_abs, e_rel)
+    assert_bf16_parity(out, ref)
 
 
 def test_kl_bf16_band_count_bitwise(kl_small):
@@ -106,11 +105,10 @@ def test_kl_bf16_band_count_bitwise(kl_small):
 def test_kl_bf16_batch2_uneven_bands():
     # batch 2, 10 latent rows in 3 bands (4/3/3): element-count-weighted merge, unequal halos
     case = Case(synth.KL_ZIMAGE, "bf16", (2, 16, 10, 8), zseed=3)
+    assert bool((case.decode(1).cpu() == case.decode(3).cpu()).all())
     out = case.decode(3).float().cpu().numpy()
     ref = case.oracle(3)
-    e_abs, e_rel = max_abs(out, ref), rel_l2(out, ref)
-    assert e_abs <= BF16_MAX_ABS and e_rel <= BF16_REL_L2, (e_abs, e_rel)
-    assert bool((case.decode(1).cpu() == case.decode(3).cpu()).all())
+    assert_bf16_parity(out, ref)
 
 
 # ---------------------------------------------------------------- bf16 Wan path
@@ -128,8 +126,7 @@ def test_wan_bf16_decode_matches_oracle(wan_small):
     out = wan_small.decode(2).float().cpu().numpy()
     ref = wan_small.oracle()
     assert out.shape == ref.shape == (1, 3, 5, 48, 64)
-    e_abs, e_rel = max_abs(out, ref), rel_l2(out, ref)
-    assert e_abs <= BF16_MAX_ABS and e_rel <= BF16_REL_L2, (e_abs, e_rel)
+    assert_bf16_parity(out, ref)
 
 
 def test_wan_bf16_band_count_bitwise(wan_small):
