@@ -62,6 +62,10 @@ struct Act {
   void* ext = nullptr;
   int dt = kBF16;        // element type (kF32 / kBF16)
   int B = 0, T = 1, H = 0, W = 0, C = 0;
+  // GroupNorm chunk moments written by the producing conv: chunks per sample and the
+  // producer's sequence number (they are valid while no later conv overwrote them)
+  int stats_chunks = 0;
+  long long stats_epoch = -1;
   long long pixels() const { return (long long)B * T * H * W; }
 };
 
@@ -192,6 +196,7 @@ class Walker {
   int odt_;   // operand dtype: what the MMAs read (the model dtype)
   int sdt_;   // storage dtype of the residual stream and every pre-norm tensor (fp32)
   int nest_ = 0;
+  long long stats_epoch_ = 0;   // bumped whenever a conv rewrites the moments buffer
 
   bool mixed() const { return odt_ != sdt_; }
 
@@ -322,19 +327,22 @@ class Walker {
   }
 
   // Launch one GEMM/conv described by `g`.
-  void launch(const ConvGeom& g, const void* in, const DevConv& w, const void* wptr, const float* bias,
-              const void* residual, const float* rowscale, void* out, void* out2, const char* what) {
+  int launch(const ConvGeom& g, const void* in, const DevConv& w, const void* wptr, const float* bias,
+             const void* residual, const float* rowscale, void* out, void* out2, const char* what) {
     count();
+    if (g.gn_part != nullptr) ++stats_epoch_;   // the moments buffer is about to be rewritten
+    int gn_chunks = 0;
     if (h_->dtype == kBF16) {
       const char* why = nullptr;
       cudaError_t e = launch_conv_tc(g, in, wptr, w.ntaps, w.rows, bias, residual, rowscale, out, out2, h_->status,
-                                     st_, &why);
+                                     st_, &why, &gn_chunks);
       if (e != cudaSuccess) set_err(VAEDEC_ERR_CUDA, std::string(what) + ": " + (why ? why : cudaGetErrorString(e)));
     } else {
       check(launch_conv_simple_f32(g, static_cast<const float*>(in), static_cast<const float*>(wptr), w.ntaps, bias,
                                    static_cast<const float*>(residual), rowscale, static_cast<float*>(out), st_),
             what);
     }
+    return gn_chunks;
   }
 
   static void fill_taps(ConvGeom& g, ConvKind kind, const DevConv& w) {
@@ -377,8 +385,10 @@ class Walker {
   // conv op: x (operand dtype) -> y (`out_dt`, channels-last buffer `out_buf`, or the
   // final channels-first output).  `copy` (optional) receives a bf16 copy of y.
   Act conv(const Act& x, const std::string& name, ConvKind kind, const Act* res, int out_buf, int out_dt,
-           void* final_out = nullptr, Act* copy = nullptr, int copy_buf = -1) {
+           void* final_out = nullptr, Act* copy = nullptr, int copy_buf = -1, bool want_stats = false) {
     Act y = x;
+    y.stats_chunks = 0;
+    y.stats_epoch = -1;
     const DevConv* w = W(name);
     if (!w || !live()) return y;
     if (w->cin != x.C) {
@@ -452,7 +462,17 @@ class Walker {
                  name.c_str());
         }
       } else {
-        launch(g, in, *w, w->w, w->b, res ? ptr(*res) : nullptr, nullptr, ptr(y), out2, name.c_str());
+        // moments for a following GroupNorm, when the kernel can write them in its epilogue
+        if (want_stats && h_->cfg.family == VAEDEC_FAMILY_KL2D && h_->dtype == kBF16 && y.dt == kF32) {
+          g.gn_part = h_->gn_part;
+          g.gn_groups = h_->cfg.norm_groups;
+        }
+        const int chunks = launch(g, in, *w, w->w, w->b, res ? ptr(*res) : nullptr, nullptr, ptr(y), out2,
+                                  name.c_str());
+        if (chunks > 0) {
+          y.stats_chunks = chunks;
+          y.stats_epoch = ++stats_epoch_;
+        }
       }
     }
     end(&x, res, y);
@@ -477,12 +497,18 @@ class Walker {
     Act y = x;
     y.buf = out_buf;
     y.dt = odt_;
+    y.stats_chunks = 0;
+    y.stats_epoch = -1;
     const DevNorm* n = N(prefix);
     if (!n || !live()) return y;
     const int G = h_->cfg.norm_groups;
     const int rows = x.T * x.H;
+    // moments from the producing conv's epilogue, if they are still the newest ones
+    const bool have = x.stats_chunks > 0 && x.stats_epoch == stats_epoch_;
+    const int n_chunks = have ? x.stats_chunks : rows;
     if (plan) {
-      plan->part = std::max(plan->part, (size_t)x.B * rows * G);
+      // fused chunks: at most 2 phase columns x ceil(W / 96) + 1 pixel tiles per output row
+      plan->part = std::max(plan->part, (size_t)x.B * rows * (size_t)(2 * (x.W / 96 + 2)) * G);
       plan->sc = std::max(plan->sc, (size_t)x.B * x.C);
     }
     note_act(y);
@@ -495,11 +521,14 @@ class Walker {
       *raw = yr;
     }
     if (begin("kind=groupnorm name=" + prefix + io(x, nullptr, y) + " silu=" + (silu ? "1" : "0") +
-              " groups=" + std::to_string(G))) {
-      count(3);
-      check(launch_gn_partials(x.dt, ptr(x), x.B, rows, x.W, x.C, G, 1, h_->gn_part, st_), "gn partials");
-      check(launch_gn_finalize(h_->gn_part, x.B, rows, x.C, G, n->g, n->b, h_->cfg.eps, h_->gn_scale, h_->gn_shift,
-                               st_),
+              " groups=" + std::to_string(G) + " fused_stats=" + (have ? "1" : "0"))) {
+      count(have ? 2 : 3);
+      if (!have) {
+        check(launch_gn_partials(x.dt, ptr(x), x.B, rows, x.W, x.C, G, 1, h_->gn_part, st_), "gn partials");
+        ++stats_epoch_;
+      }
+      check(launch_gn_finalize(h_->gn_part, x.B, n_chunks, x.C, G, n->g, n->b, h_->cfg.eps, h_->gn_scale,
+                               h_->gn_shift, st_),
             "gn finalize");
       check(launch_gn_apply(x.dt, y.dt, ptr(x), ptr(y), raw ? ptr(yr) : nullptr, (long long)x.T * x.H * x.W, x.B,
                             x.C, h_->gn_scale, h_->gn_shift, silu ? 1 : 0, st_),
@@ -512,6 +541,8 @@ class Walker {
   Act rms_norm(const Act& x, const std::string& prefix, bool silu, int out_buf, Act* raw = nullptr,
                int raw_buf = -1) {
     Act y = x;
+    y.stats_chunks = 0;
+    y.stats_epoch = -1;
     y.buf = out_buf;
     y.dt = odt_;
     const DevNorm* n = N(prefix);
@@ -542,6 +573,8 @@ class Walker {
     Act y = x;
     y.buf = o_buf;
     y.dt = sdt_;
+    y.stats_chunks = 0;
+    y.stats_epoch = -1;
     const int C = x.C;
     const long long Ntok = (long long)x.H * x.W;
     const int F = x.B * x.T;   // sequences
@@ -692,7 +725,7 @@ class Walker {
     Act t = wan ? rms_norm(x, p + ".norm1", true, tb, need_raw ? &xb : nullptr, rb)
                 : group_norm(x, p + ".norm1", true, tb, need_raw ? &xb : nullptr, rb);
     const int hb = pick({x.buf, tb, rb});
-    Act hh = conv(t, p + ".conv1", wan ? C3 : K3, nullptr, hb, sdt_);
+    Act hh = conv(t, p + ".conv1", wan ? C3 : K3, nullptr, hb, sdt_, nullptr, nullptr, -1, !wan);
     Act t2 = wan ? rms_norm(hh, p + ".norm2", true, tb) : group_norm(hh, p + ".norm2", true, tb);
     Act res = x;
     int scb = -1;
@@ -703,16 +736,16 @@ class Walker {
     const int out_buf = hb;
     if (copy && mixed()) {
       const int cb = sc ? pick({tb, hb, scb}) : pick({x.buf, tb, hb});
-      return conv(t2, p + ".conv2", wan ? C3 : K3, &res, out_buf, sdt_, nullptr, copy, cb);
+      return conv(t2, p + ".conv2", wan ? C3 : K3, &res, out_buf, sdt_, nullptr, copy, cb, !wan);
     }
-    Act y = conv(t2, p + ".conv2", wan ? C3 : K3, &res, out_buf, sdt_);
+    Act y = conv(t2, p + ".conv2", wan ? C3 : K3, &res, out_buf, sdt_, nullptr, nullptr, -1, !wan);
     if (copy) *copy = y;
     return y;
   }
 
   void walk_kl(Act x, void* out) {
     const vaedec_config& c = h_->cfg;
-    x = conv(x, "conv_in", K3, nullptr, pick({x.buf}), sdt_);
+    x = conv(x, "conv_in", K3, nullptr, pick({x.buf}), sdt_, nullptr, nullptr, -1, true);
     x = resnet(x, "mid_block.resnets.0", false, nullptr);
     x = attention(x, "mid_block.attentions.0", false);
     x = resnet(x, "mid_block.resnets.1", false, nullptr);
@@ -723,7 +756,8 @@ class Walker {
         const bool last = (r + 1 == c.stage_resnets[s]) && c.stage_upsample[s];
         x = resnet(x, pre + ".resnets." + std::to_string(r), false, last ? &xc : nullptr);
       }
-      if (c.stage_upsample[s]) x = conv(xc, pre + ".upsamplers.0.conv", UP, nullptr, pick({x.buf, xc.buf}), sdt_);
+      if (c.stage_upsample[s])
+        x = conv(xc, pre + ".upsamplers.0.conv", UP, nullptr, pick({x.buf, xc.buf}), sdt_, nullptr, nullptr, -1, true);
     }
     Act t = group_norm(x, "conv_norm_out", true, pick({x.buf}));
     conv(t, "conv_out", K3, nullptr, -1, odt_, out);

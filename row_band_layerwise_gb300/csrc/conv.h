@@ -40,6 +40,10 @@ struct ConvGeom {
   int out_f32;               // 1: fp32 output, 0: bf16
   int res_f32;               // 1: the residual is fp32, 0: bf16
   float scale;               // v = acc * scale (* rowscale[p]) + bias + residual
+  // Optional GroupNorm chunk moments of the stored output (kernels that support it):
+  // `gn_part` points to {n, mean, M2, pad} float4 records, `gn_groups` groups.
+  void* gn_part;
+  int gn_groups;
 };
 
 }  // namespace vd

@@ -12,8 +12,8 @@
 // output channel, so each epilogue store instruction writes 32 consecutive
 // channels of one pixel: fully coalesced, with residual reads batched 32 deep.
 //
-// Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
-// warps 2..5 epilogue.  A weight stage holds the three taps of one kernel row,
+// Roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
+// warps 2..9 epilogue (two warps per TMEM lane quarter, splitting the rows).  A weight stage holds the three taps of one kernel row,
 // so each stage wait is followed by ~1500 cycles of MMA work.  Waits are
 // bounded (ptx.cuh).
 #include <cuda.h>
@@ -33,7 +33,7 @@ namespace vd {
 
 namespace {
 
-constexpr int kThreadsT = 192;
+constexpr int kThreadsT = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue (two per TMEM lane quarter)
 constexpr int kMaxWStages = 4;
 constexpr int kPipeBytesT = 212 * 1024;
 
@@ -51,6 +51,8 @@ struct HaloTParams {
   void* out;
   __nv_bfloat16* out2;
   int* status;
+  GnPartial* gn_part;            // GroupNorm chunk moments of the output, or null
+  int gn_cg;                     // channels per group (divides 32)
 };
 
 template <int BK>
@@ -58,6 +60,24 @@ struct SwzT {
   static constexpr uint32_t kSbo = BK * 2 * 8;
   static constexpr uint32_t kMode = BK == 64 ? 2u : (BK == 32 ? 4u : 6u);
 };
+
+// Chan's merge of central moments: (n, mean, M2) of part a, then part b.
+__device__ __forceinline__ void moments_merge(float na, float ma, float m2a, float nb, float mb, float m2b, float& n,
+                                              float& m, float& m2) {
+  if (nb == 0.f) {
+    n = na; m = ma; m2 = m2a;
+    return;
+  }
+  if (na == 0.f) {
+    n = nb; m = mb; m2 = m2b;
+    return;
+  }
+  const float nt = na + nb;
+  const float d = mb - ma;
+  m = ma + d * (nb / nt);
+  m2 = m2a + m2b + d * d * (na * nb / nt);
+  n = nt;
+}
 
 template <int BK>
 __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_constant__ HaloTParams p) {
@@ -209,6 +229,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
   } else {
     // ---- epilogue: TMEM lane = output channel; columns = pixels of the tile row
     const int q = warp & 3;
+    const int sub = (warp - 2) >> 2;   // 0 for warps 2..5, 1 for warps 6..9: rows r with r % 2 == sub
     const int co = m0 + q * 32 + lane;
     const bool cvalid = co < g.Cout;
     const float bias = (p.bias != nullptr && cvalid) ? p.bias[co] : 0.f;
@@ -219,11 +240,12 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
       const int py = phase >> 1, px = phase & 1;
       const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
       const bool res_f32 = g.res_f32 != 0;
-      for (int r = 0; r < p.R; ++r) {
+      for (int r = sub; r < p.R; r += 2) {
         const int y = y0 + r;
         if (y >= g.H) break;   // uniform across the warp
         const int yo = y * g.osy + (g.nphase > 1 ? py : 0);
         const long long row_pix = ((static_cast<long long>(bb) * g.oT + tt) * g.oH + yo) * static_cast<long long>(g.oW);
+        float sn = 0.f, smean = 0.f, sm2 = 0.f;   // this channel's moments over the tile row
         for (int c0 = 0; c0 < p.npx; c0 += 32) {
           uint32_t rr[32];
           tmem_ld_32x32b_x32(lane_addr + static_cast<uint32_t>(r * p.npx + c0), rr);
@@ -254,6 +276,19 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
               for (int j = 0; j < 32; ++j) v[j] += rv[j];
             }
           }
+          if (p.gn_part != nullptr) {
+            float cs = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cs += (j < nvalid) ? v[j] : 0.f;
+            const float cm = cs / static_cast<float>(nvalid);
+            float c2 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float d = (j < nvalid) ? v[j] - cm : 0.f;
+              c2 = fmaf(d, d, c2);
+            }
+            moments_merge(sn, smean, sm2, static_cast<float>(nvalid), cm, c2, sn, smean, sm2);
+          }
           if (cvalid) {
             if (g.out_f32) {
               float* op = reinterpret_cast<float*>(p.out) + e0;
@@ -272,6 +307,31 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
               for (int j = 0; j < 32; ++j)
                 if (j < nvalid) op[j * stride] = __float2bfloat16_rn(v[j]);
             }
+          }
+        }
+        if (p.gn_part != nullptr) {
+          // merge the group's channels (gn_cg consecutive lanes), lower lane first
+          for (int off = 1; off < p.gn_cg; off <<= 1) {
+            const float on = __shfl_xor_sync(0xffffffffu, sn, off);
+            const float om = __shfl_xor_sync(0xffffffffu, smean, off);
+            const float o2 = __shfl_xor_sync(0xffffffffu, sm2, off);
+            if (lane & off)
+              moments_merge(on, om, o2, sn, smean, sm2, sn, smean, sm2);
+            else
+              moments_merge(sn, smean, sm2, on, om, o2, sn, smean, sm2);
+          }
+          if (cvalid && (lane % p.gn_cg) == 0) {
+            // chunk = (output row, phase column, pixel tile), fixed by the geometry alone
+            const int npxp = g.nphase > 1 ? 2 : 1;
+            const long long orow = static_cast<long long>(tt) * g.oH + yo;
+            const long long chunk =
+                ((static_cast<long long>(bb) * g.oT * g.oH + orow) * npxp + (g.nphase > 1 ? px : 0)) * p.tiles_x + tx;
+            GnPartial o;
+            o.n = sn;
+            o.mean = smean;
+            o.m2 = sm2;
+            o.pad = 0.f;
+            p.gn_part[chunk * g.gn_groups + co / p.gn_cg] = o;
           }
         }
       }
@@ -311,7 +371,7 @@ bool conv_halo_t_applicable(const ConvGeom& g) {
 
 cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
                                const float* bias, const void* residual, void* out, void* out2, int* status,
-                               cudaStream_t stream, const char** why) {
+                               cudaStream_t stream, const char** why, int* gn_chunks) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) {
     *why = "cuTensorMapEncodeTiled unavailable";
@@ -357,6 +417,14 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
   p.out = out;
   p.out2 = static_cast<__nv_bfloat16*>(out2);
   p.status = status;
+  if (g.gn_part != nullptr && g.gn_groups > 0 && g.out_f32 && g.Cout % g.gn_groups == 0) {
+    const int cg = g.Cout / g.gn_groups;
+    if (cg <= 32 && 32 % cg == 0) {
+      p.gn_part = static_cast<GnPartial*>(g.gn_part);
+      p.gn_cg = cg;
+      if (gn_chunks != nullptr) *gn_chunks = g.oT * g.oH * (g.nphase > 1 ? 2 : 1) * p.tiles_x;
+    }
+  }
 
   const cuuint32_t ones[5] = {1, 1, 1, 1, 1};
   {

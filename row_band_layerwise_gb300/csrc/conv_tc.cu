@@ -58,7 +58,7 @@ struct SwizzleOf {
 };
 
 template <int BK>
-__global__ void __launch_bounds__(kThreads, 1) conv_tc_kernel(const __grid_constant__ ConvTcParams p) {
+__global__ void __launch_bounds__(kThreads) conv_tc_kernel(const __grid_constant__ ConvTcParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[8];
   __shared__ __align__(8) uint64_t empty_bar[8];
@@ -254,8 +254,9 @@ const char* conv_tc_plan(const ConvGeom& g, int* bk_out) {
 
 cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
                            const float* bias, const void* residual, const float* rowscale, void* out, void* out2,
-                           int* status, cudaStream_t stream, const char** why) {
+                           int* status, cudaStream_t stream, const char** why, int* gn_chunks) {
   *why = nullptr;
+  if (gn_chunks != nullptr) *gn_chunks = 0;
   int bk = 64;
   if (const char* e = conv_tc_plan(g, &bk)) {
     *why = e;
@@ -266,7 +267,8 @@ cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, i
     return cudaErrorInvalidValue;
   }
   if (rowscale == nullptr && conv_halo_t_applicable(g))
-    return launch_conv_halo_t(g, in, wts, ntaps_w, w_rows, bias, residual, out, out2, status, stream, why);
+    return launch_conv_halo_t(g, in, wts, ntaps_w, w_rows, bias, residual, out, out2, status, stream, why,
+                              gn_chunks);
   if (rowscale == nullptr && conv_halo_applicable(g))
     return launch_conv_halo(g, in, wts, ntaps_w, w_rows, bias, residual, out, out2, status, stream, why);
   EncodeTiledFn enc = get_encode_fn();
@@ -302,6 +304,10 @@ cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, i
   p.stage_b_bytes = static_cast<uint32_t>(round_up(p.BN * bk * 2, 1024));
   const int stage_bytes = static_cast<int>(p.stage_a_bytes + p.stage_b_bytes);
   p.stages = std::min(8, (200 * 1024) / stage_bytes);
+  // narrow tiles do little MMA work per stage: keep the CTA small so that several
+  // CTAs share an SM and cover each other's stage waits
+  if (p.BN <= 64) p.stages = std::min(p.stages, 4);
+  p.stages = std::min(p.stages, std::max(2, g.ntaps * ((g.Cin + bk - 1) / bk)));
   if (p.stages < 2) {
     *why = "tile does not fit shared memory";
     return cudaErrorInvalidValue;

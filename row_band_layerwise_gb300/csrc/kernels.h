@@ -15,9 +15,12 @@ enum DType : int { kF32 = 1, kBF16 = 2 };
 // `wts` is [w_rows][ntaps_w][Cin] bf16 (K-major per output channel).  `out2`
 // (optional) receives a bf16 copy of a channels-last output.
 const char* conv_tc_plan(const ConvGeom& g, int* bk_out);
+// When g.gn_part is set and the chosen kernel can, the epilogue also writes the
+// GroupNorm central moments of its output in fixed chunks and *gn_chunks receives
+// the number of chunks per sample (0 when no moments were written).
 cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
                            const float* bias, const void* residual, const float* rowscale, void* out, void* out2,
-                           int* status, cudaStream_t stream, const char** why);
+                           int* status, cudaStream_t stream, const char** why, int* gn_chunks = nullptr);
 
 // Halo-tile variant (R output rows per CTA, activations staged once per channel
 // chunk for all 3x3 taps); launch_conv_tc dispatches to it when applicable.
@@ -30,7 +33,7 @@ cudaError_t launch_conv_halo(const ConvGeom& g, const void* in, const void* wts,
 bool conv_halo_t_applicable(const ConvGeom& g);
 cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
                                const float* bias, const void* residual, void* out, void* out2, int* status,
-                               cudaStream_t stream, const char** why);
+                               cudaStream_t stream, const char** why, int* gn_chunks);
 
 // CUDA-core fp32 direct convolution over the same ConvGeom (the fp32 path).
 // `wts` is [w_rows][ntaps_w][Cin] fp32.

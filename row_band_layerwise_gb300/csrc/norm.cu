@@ -146,82 +146,121 @@ __global__ void __launch_bounds__(kGnThreads) gn_partials_kernel(const T* __rest
   }
 }
 
-// One warp per (sample, group): lane l takes chunks l, l+32, ... and applies
-// the weighted rule to its chunks in order; the 32 lane results are then
-// combined with the same rule along a fixed shuffle tree.
-__global__ void gn_finalize_kernel(const GnPartial* __restrict__ part, int B, int n_chunks, int C, int G,
-                                   const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
-                                   float* __restrict__ scale, float* __restrict__ shift) {
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= B * G) return;
-  const int b = wid / G, g = wid % G;
-  // lane-local: N_l = sum n_i, mean_l = sum (n_i/N_l) mean_i, then
-  // var_l = sum (n_i/N_l) (var_i + (mean_i - mean_l)^2)
+// One CTA per (sample, group).  Thread t takes chunks t, t + 256, ... and applies
+// the weighted rule to them in order: N_t = sum n_i, mean_t = sum (n_i/N_t) mean_i,
+// var_t = sum (n_i/N_t)(var_i + (mean_i - mean_t)^2).  The 256 thread results are
+// then combined with the same rule, two parts at a time, along a fixed tree.
+constexpr int kFinThreads = 256;
+
+__global__ void __launch_bounds__(kFinThreads) gn_finalize_kernel(const GnPartial* __restrict__ part, int B,
+                                                                  int n_chunks, int C, int G,
+                                                                  const float* __restrict__ gamma,
+                                                                  const float* __restrict__ beta, float eps,
+                                                                  float* __restrict__ scale,
+                                                                  float* __restrict__ shift) {
+  __shared__ float sn[kFinThreads], sm[kFinThreads], sv[kFinThreads];
+  const int b = blockIdx.x / G, g = blockIdx.x % G;
+  const int t = threadIdx.x;
+  const GnPartial* pp = part + (long long)b * n_chunks * G + g;
   float nl = 0.f;
-  for (int c = lane; c < n_chunks; c += 32) nl += part[((long long)b * n_chunks + c) * G + g].n;
+  for (int c = t; c < n_chunks; c += kFinThreads) nl += pp[(long long)c * G].n;
   float ml = 0.f;
-  for (int c = lane; c < n_chunks; c += 32) {
-    const GnPartial e = part[((long long)b * n_chunks + c) * G + g];
+  for (int c = t; c < n_chunks; c += kFinThreads) {
+    const GnPartial e = pp[(long long)c * G];
     if (e.n > 0.f) ml += (e.n / nl) * e.mean;
   }
   float vl = 0.f;
-  for (int c = lane; c < n_chunks; c += 32) {
-    const GnPartial e = part[((long long)b * n_chunks + c) * G + g];
+  for (int c = t; c < n_chunks; c += kFinThreads) {
+    const GnPartial e = pp[(long long)c * G];
     if (e.n > 0.f) {
       const float d = e.mean - ml;
       vl += (e.n / nl) * (e.m2 / e.n + d * d);
     }
   }
-  // tree over lanes: two-part weighted rule at each node
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float no = __shfl_down_sync(0xffffffffu, nl, off);
-    const float mo = __shfl_down_sync(0xffffffffu, ml, off);
-    const float vo = __shfl_down_sync(0xffffffffu, vl, off);
-    if (lane < off && no > 0.f) {
-      const float nt = nl + no;
-      const float wa = nl / nt, wb = no / nt;
-      const float m = wa * ml + wb * mo;
-      const float da = ml - m, db = mo - m;
-      vl = wa * (vl + da * da) + wb * (vo + db * db);
-      ml = m;
-      nl = nt;
+  sn[t] = nl;
+  sm[t] = ml;
+  sv[t] = vl;
+  __syncthreads();
+  for (int half = kFinThreads / 2; half > 0; half >>= 1) {
+    if (t < half) {
+      const float na = sn[t], nb = sn[t + half];
+      if (nb > 0.f) {
+        const float nt = na + nb;
+        const float wa = na / nt, wb = nb / nt;
+        const float m = wa * sm[t] + wb * sm[t + half];
+        const float da = sm[t] - m, db = sm[t + half] - m;
+        sv[t] = wa * (sv[t] + da * da) + wb * (sv[t + half] + db * db);
+        sm[t] = m;
+        sn[t] = nt;
+      }
     }
+    __syncthreads();
   }
-  const float mean = __shfl_sync(0xffffffffu, ml, 0);
-  const float var = __shfl_sync(0xffffffffu, vl, 0);
-  const float rstd = rsqrtf(var + eps);
+  const float rstd = rsqrtf(sv[0] + eps);
+  const float mean = sm[0];
   const int cg = C / G;
-  for (int c = g * cg + lane; c < (g + 1) * cg; c += 32) {
+  for (int c = g * cg + t; c < (g + 1) * cg; c += kFinThreads) {
     const float a = gamma[c] * rstd;
     scale[(long long)b * C + c] = a;
     shift[(long long)b * C + c] = beta[c] - mean * a;
   }
 }
 
-__device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
+// SiLU(v) = v / (1 + exp(-v)) with CUDA's fast exponential and fast division
+// (the result is rounded to bf16 or feeds fp32 storage; both intrinsics are
+// within a few ulp, and exp(-v) = inf for very negative v gives 0 as it should).
+__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.f + __expf(-v)); }
+
+__device__ __forceinline__ void load8f(const float* p, float (&o)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
 
 template <typename Tin, typename Tout>
-__global__ void gn_apply_kernel(const Tin* __restrict__ x, Tout* __restrict__ y, Tout* __restrict__ y_raw,
-                                long long nvec, long long vec_per_sample, int C, const float* __restrict__ scale,
-                                const float* __restrict__ shift, int silu) {
+__global__ void __launch_bounds__(256) gn_apply_kernel(const Tin* __restrict__ x, Tout* __restrict__ y,
+                                                       Tout* __restrict__ y_raw, long long nvec,
+                                                       long long vec_per_sample, int C,
+                                                       const float* __restrict__ scale,
+                                                       const float* __restrict__ shift, int silu) {
   const int vpp = C / 8;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nvec;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int b = static_cast<int>(i / vec_per_sample);
-    const int c0 = static_cast<int>(i % vpp) * 8;
-    float v[8], o[8];
+  const long long step = (long long)gridDim.x * blockDim.x;
+  // two 8-element vectors per thread and iteration: more loads in flight
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nvec; i += 2 * step) {
+    const long long i2 = i + step;
+    const bool has2 = i2 < nvec;
+    float v[8], w[8];
     Vec8<Tin>::load(x + i * 8, v);
-    if (y_raw != nullptr) Vec8<Tout>::store(y_raw + i * 8, v);
-    const float* a = scale + (long long)b * C + c0;
-    const float* s = shift + (long long)b * C + c0;
+    if (has2) Vec8<Tin>::load(x + i2 * 8, w);
+    {
+      if (y_raw != nullptr) Vec8<Tout>::store(y_raw + i * 8, v);
+      const int b = static_cast<int>(i / vec_per_sample);
+      const int c0 = static_cast<int>(i % vpp) * 8;
+      float a[8], sh[8], o[8];
+      load8f(scale + (long long)b * C + c0, a);
+      load8f(shift + (long long)b * C + c0, sh);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float t = fmaf(v[j], __ldg(a + j), __ldg(s + j));
-      o[j] = silu ? silu_f(t) : t;
+      for (int j = 0; j < 8; ++j) {
+        const float t = fmaf(v[j], a[j], sh[j]);
+        o[j] = silu ? silu_f(t) : t;
+      }
+      Vec8<Tout>::store(y + i * 8, o);
     }
-    Vec8<Tout>::store(y + i * 8, o);
+    if (has2) {
+      if (y_raw != nullptr) Vec8<Tout>::store(y_raw + i2 * 8, w);
+      const int b = static_cast<int>(i2 / vec_per_sample);
+      const int c0 = static_cast<int>(i2 % vpp) * 8;
+      float a[8], sh[8], o[8];
+      load8f(scale + (long long)b * C + c0, a);
+      load8f(shift + (long long)b * C + c0, sh);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float t = fmaf(w[j], a[j], sh[j]);
+        o[j] = silu ? silu_f(t) : t;
+      }
+      Vec8<Tout>::store(y + i2 * 8, o);
+    }
   }
 }
 
@@ -269,7 +308,7 @@ __global__ void rms_norm_kernel(const Tin* __restrict__ x, Tout* __restrict__ y,
 
 int grid_for(long long work, int threads) {
   const long long b = (work + threads - 1) / threads;
-  return static_cast<int>(b < 152LL * 32 ? (b < 1 ? 1 : b) : 152LL * 32);
+  return static_cast<int>(b < 152LL * 8 ? (b < 1 ? 1 : b) : 152LL * 8);
 }
 
 }  // namespace
@@ -291,10 +330,7 @@ cudaError_t launch_gn_partials(int dtype, const void* x, int B, int rows, int W,
 
 cudaError_t launch_gn_finalize(const GnPartial* part, int B, int n_chunks, int C, int G, const float* gamma,
                                const float* beta, float eps, float* scale, float* shift, cudaStream_t stream) {
-  const int warps = B * G;
-  const int threads = 128;
-  const int blocks = (warps * 32 + threads - 1) / threads;
-  gn_finalize_kernel<<<blocks, threads, 0, stream>>>(part, B, n_chunks, C, G, gamma, beta, eps, scale, shift);
+  gn_finalize_kernel<<<B * G, kFinThreads, 0, stream>>>(part, B, n_chunks, C, G, gamma, beta, eps, scale, shift);
   return cudaGetLastError();
 }
 
