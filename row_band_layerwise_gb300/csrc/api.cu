@@ -345,6 +345,19 @@ class Walker {
     return gn_chunks;
   }
 
+  // Launch one channel-major tensor-core GEMM (bf16 path only).
+  void gemm(const GemmArgs& a, const char* what) {
+    count();
+    const char* why = nullptr;
+    cudaError_t e = launch_gemm_cm(a, h_->status, st_, &why);
+    if (e != cudaSuccess) set_err(VAEDEC_ERR_CUDA, std::string(what) + ": " + (why ? why : cudaGetErrorString(e)));
+  }
+
+  // Key-dimension split of the probabilities x values product: a function of the
+  // number of keys only, so every band count sums the same partial products in
+  // the same order.
+  static int pv_splits(long long ntok) { return (int)std::max(1LL, std::min(8LL, (ntok + 4095) / 4096)); }
+
   static void fill_taps(ConvGeom& g, ConvKind kind, const DevConv& w) {
     std::memset(g.taps, 0, sizeof(g.taps));
     g.nphase = 1;
@@ -584,6 +597,8 @@ class Walker {
       int maxrows = 0;
       for (int r : band_rows(x.H, n_bands_)) maxrows = std::max(maxrows, r);
       plan->s = std::max(plan->s, (size_t)maxrows * (size_t)x.W * (size_t)Ntok);
+      if (pv_splits(Ntok) > 1)   // fp32 partials of the split probabilities x values product
+        plan->s = std::max(plan->s, (size_t)pv_splits(Ntok) * (size_t)maxrows * (size_t)x.W * (size_t)C);
       plan->l = std::max(plan->l, (size_t)maxrows * x.W);
     }
     note_act(y);
@@ -662,42 +677,89 @@ class Walker {
         vview.rows = C;
         vview.cout = C;
         const float scale = 1.f / std::sqrt((float)C);
+        const bool tc = h_->dtype == kBF16;
         for (int f = 0; f < F && live(); ++f) {
           int r0 = 0;
           for (int band = 0; band < n_bands_ && live(); ++band) {
             const int nr = rows[band] * x.W;
             const size_t qoff = ((size_t)f * Ntok + (size_t)r0 * x.W) * C;
-            ConvGeom gs;
-            std::memset(&gs, 0, sizeof(gs));
-            gs.B = 1;
-            gs.T = 1;
-            gs.H = 1;
-            gs.W = nr;
-            gs.Cin = C;
-            gs.Cout = (int)Ntok;
-            gs.nphase = 1;
-            gs.ntaps = 1;
-            gs.oT = 1;
-            gs.oH = 1;
-            gs.oW = nr;
-            gs.oC = (int)Ntok;
-            gs.osy = gs.osx = 1;
-            gs.out_f32 = 1;
-            gs.scale = scale;
-            launch(gs, static_cast<char*>(h_->attn_q) + qoff * oes, kview,
-                   static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes, nullptr, nullptr, nullptr,
-                   h_->attn_s, nullptr, "attention scores");
-            count();
-            check(launch_softmax_rows(odt_, h_->attn_s, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
-            ConvGeom go = gs;
-            go.Cin = (int)Ntok;
-            go.Cout = C;
-            go.oC = C;
-            go.out_f32 = odt_ == kF32;
-            go.scale = 1.f;
-            // O overwrites the band's rows of the normalised tensor (no longer needed)
-            launch(go, h_->attn_p, vview, static_cast<char*>(h_->attn_vt) + (size_t)f * C * Ntok * oes, nullptr,
-                   nullptr, h_->attn_l, static_cast<char*>(ptr(hn)) + qoff * oes, nullptr, "attention pv");
+            void* o_band = static_cast<char*>(ptr(hn)) + qoff * oes;   // O overwrites the band's normalised rows
+            if (tc) {
+              // S[q, key] = (K Q^T)[key, q] / sqrt(C), keys on the accumulator lanes
+              GemmArgs sa;
+              sa.A = static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes;
+              sa.lda = C;
+              sa.B = static_cast<char*>(h_->attn_q) + qoff * oes;
+              sa.ldb = C;
+              sa.M = (int)Ntok;
+              sa.N = nr;
+              sa.K = C;
+              sa.out = h_->attn_s;
+              sa.ldo = Ntok;
+              sa.out_f32 = 1;
+              sa.scale = scale;
+              gemm(sa, "attention scores");
+              count();
+              check(launch_softmax_rows(odt_, h_->attn_s, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
+              // O[q, c] = inv_l[q] * (V^T P^T)[c, q], channels on the lanes, keys split
+              const int splits = pv_splits(Ntok);
+              GemmArgs pa;
+              pa.A = static_cast<char*>(h_->attn_vt) + (size_t)f * C * Ntok * oes;
+              pa.lda = Ntok;
+              pa.B = h_->attn_p;
+              pa.ldb = Ntok;
+              pa.M = C;
+              pa.N = nr;
+              pa.K = (int)Ntok;
+              pa.ldo = C;
+              pa.scale_n = h_->attn_l;
+              pa.splits = splits;
+              if (splits > 1) {
+                pa.out = h_->attn_s;   // fp32 partials; the scores are no longer needed
+                pa.out_f32 = 1;
+                pa.split_stride = (long long)nr * C;
+                gemm(pa, "attention pv");
+                count();
+                check(launch_splitk_reduce(static_cast<const float*>(h_->attn_s), splits, (long long)nr * C,
+                                           (long long)nr * C, odt_, o_band, st_),
+                      "attention pv reduce");
+              } else {
+                pa.out = o_band;
+                pa.out_f32 = odt_ == kF32;
+                gemm(pa, "attention pv");
+              }
+            } else {
+              ConvGeom gs;
+              std::memset(&gs, 0, sizeof(gs));
+              gs.B = 1;
+              gs.T = 1;
+              gs.H = 1;
+              gs.W = nr;
+              gs.Cin = C;
+              gs.Cout = (int)Ntok;
+              gs.nphase = 1;
+              gs.ntaps = 1;
+              gs.oT = 1;
+              gs.oH = 1;
+              gs.oW = nr;
+              gs.oC = (int)Ntok;
+              gs.osy = gs.osx = 1;
+              gs.out_f32 = 1;
+              gs.scale = scale;
+              launch(gs, static_cast<char*>(h_->attn_q) + qoff * oes, kview,
+                     static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes, nullptr, nullptr, nullptr,
+                     h_->attn_s, nullptr, "attention scores");
+              count();
+              check(launch_softmax_rows(odt_, h_->attn_s, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
+              ConvGeom go = gs;
+              go.Cin = (int)Ntok;
+              go.Cout = C;
+              go.oC = C;
+              go.out_f32 = odt_ == kF32;
+              go.scale = 1.f;
+              launch(go, h_->attn_p, vview, static_cast<char*>(h_->attn_vt) + (size_t)f * C * Ntok * oes, nullptr,
+                     nullptr, h_->attn_l, o_band, nullptr, "attention pv");
+            }
             r0 += rows[band];
           }
         }

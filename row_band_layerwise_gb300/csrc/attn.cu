@@ -68,6 +68,65 @@ __global__ void __launch_bounds__(kSmThreads) softmax_rows_kernel(const float* _
   if (threadIdx.x == 0) inv_l[row] = 1.f / l;
 }
 
+// Single-read variant: the row stays in registers (NV float4 per thread, rows of
+// at most 1024 * NV scores, nk a multiple of 4), so S is read from memory once.
+// Same definition as softmax_rows_kernel (max, exp of the difference, sum of the
+// stored values, one reciprocal); the sum is taken four values at a time.
+template <typename P>
+__device__ __forceinline__ float store_p4(P* p, float4 v);
+template <>
+__device__ __forceinline__ float store_p4<float>(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+  return (v.x + v.y) + (v.z + v.w);
+}
+template <>
+__device__ __forceinline__ float store_p4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&lo);
+  u.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+  const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+  return (a.x + a.y) + (b.x + b.y);
+}
+
+template <typename P, int NV>
+__global__ void __launch_bounds__(kSmThreads) softmax_rows_reg_kernel(const float* __restrict__ S, P* __restrict__ Pm,
+                                                                      float* __restrict__ inv_l, int nk) {
+  __shared__ float red[32];
+  const long long row = blockIdx.x;
+  const float4* s4 = reinterpret_cast<const float4*>(S + row * nk);
+  P* p = Pm + row * nk;
+  const int n4 = nk >> 2;
+  float4 v[NV];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int idx = threadIdx.x + i * kSmThreads;
+    if (idx < n4) {
+      v[i] = __ldcs(s4 + idx);
+      m = fmaxf(m, fmaxf(fmaxf(v[i].x, v[i].y), fmaxf(v[i].z, v[i].w)));
+    }
+  }
+  m = block_reduce_max(m, red);
+  float l = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int idx = threadIdx.x + i * kSmThreads;
+    if (idx < n4) {
+      float4 e;
+      e.x = __expf(v[i].x - m);
+      e.y = __expf(v[i].y - m);
+      e.z = __expf(v[i].z - m);
+      e.w = __expf(v[i].w - m);
+      l += store_p4<P>(p + 4 * idx, e);
+    }
+  }
+  l = block_reduce_sum(l, red);
+  if (threadIdx.x == 0) inv_l[row] = 1.f / l;
+}
+
 template <typename T>
 __global__ void to_channels_last_kernel(const T* __restrict__ x, T* __restrict__ y, int C, long long spatial,
                                         long long total) {
@@ -86,6 +145,24 @@ __global__ void to_channels_last_kernel(const T* __restrict__ x, T* __restrict__
 cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv_l, int rows, int nk,
                                 cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
+  if (nk % 4 == 0 && nk <= 16 * 4 * kSmThreads) {
+    const int nv = (nk + 4 * kSmThreads - 1) / (4 * kSmThreads);
+    const bool bf = p_dtype == kBF16;
+#define VD_SOFTMAX_REG(NV)                                                                                       \
+  if (nv <= NV) {                                                                                                \
+    if (bf)                                                                                                      \
+      softmax_rows_reg_kernel<__nv_bfloat16, NV>                                                                 \
+          <<<rows, kSmThreads, 0, stream>>>(S, static_cast<__nv_bfloat16*>(P), inv_l, nk);                       \
+    else                                                                                                         \
+      softmax_rows_reg_kernel<float, NV><<<rows, kSmThreads, 0, stream>>>(S, static_cast<float*>(P), inv_l, nk); \
+    return cudaGetLastError();                                                                                   \
+  }
+    VD_SOFTMAX_REG(2)
+    VD_SOFTMAX_REG(4)
+    VD_SOFTMAX_REG(8)
+    VD_SOFTMAX_REG(16)
+#undef VD_SOFTMAX_REG
+  }
   if (p_dtype == kBF16)
     softmax_rows_kernel<__nv_bfloat16><<<rows, kSmThreads, 0, stream>>>(S, static_cast<__nv_bfloat16*>(P), inv_l, nk);
   else

@@ -1,0 +1,362 @@
+// Channel-major GEMM on tcgen05 tensor cores:  D[m, n] = sum_k A[m, k] * B[n, k],
+// stored at out[n * ldo + m].
+//
+// Used for the attention products (scores = keys x queries, probabilities x
+// values with the sum over keys split across CTAs) and the 1x1 projections.  A
+// CTA computes a 128 (m) x NB (n, up to 256) tile; every TMEM lane is one m, so
+// each epilogue store instruction writes 32 consecutive m of one n: coalesced.
+//
+// Roles (352 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
+// warp 2 stage waiter, warps 3..10 epilogue.  The waiter polls the stage
+// mbarriers and hands each landed stage to the MMA warp through one hardware
+// named barrier that both warps sync on once per stage, so the MMA-issuing thread
+// never polls shared memory while the tensor pipe is busy (it sleeps in the
+// barrier instead), and the waiter polls stage i+1 while the MMAs of stage i run.
+// Both warps pass the barrier exactly once per stage, also after a timeout, so
+// neither can block on it.  Every mbarrier wait is bounded.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace vd {
+
+namespace {
+
+constexpr int kGThreads = 352;
+constexpr int kGMaxStages = 4;
+constexpr int kGBK = 64;   // K chunk (128B swizzle)
+constexpr int kGCols = 16; // accumulator columns per epilogue step
+
+struct GemmParams {
+  CUtensorMap tmA;   // (K, M) box (64, 128)
+  CUtensorMap tmB;   // (K, N) box (64, NB)
+  int M, N, K, NB, n_mtiles, n_ntiles, nk, splits, nb;
+  uint32_t a_stage, b_stage, tmem_cols;
+  void* out;
+  long long ldo, split_stride;
+  int out_f32, res_f32;
+  const float* bias_m;
+  const float* bias_n;
+  const float* scale_n;
+  float scale;
+  const void* residual;
+  __nv_bfloat16* out2;
+  int* status;
+};
+
+// Named barrier 1, shared by the waiter warp and the MMA warp (64 threads).
+__device__ __forceinline__ void stage_handoff() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kGMaxStages], empty_bar[kGMaxStages];
+  __shared__ __align__(8) uint64_t accum_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + p.nb * p.a_stage;
+
+  const int mt = blockIdx.x % p.n_mtiles;
+  const int nt = blockIdx.x / p.n_mtiles;
+  const int split = blockIdx.y;
+  const int m0 = mt * 128, n0 = nt * p.NB;
+  const int k_begin = static_cast<int>((long long)split * p.nk / p.splits);
+  const int k_end = static_cast<int>((long long)(split + 1) * p.nk / p.splits);
+  const int nks = k_end - k_begin;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.nb; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(&accum_bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint32_t tx = p.a_stage + static_cast<uint32_t>(p.NB * kGBK * 2);
+      int issued = 0;
+      for (int i = 0; i < nks && !abort_flag; ++i) {
+        const int s = i % p.nb;
+        if (i >= p.nb && !mbar_wait(&empty_bar[s], (static_cast<uint32_t>(i / p.nb) & 1u) ^ 1u, p.status,
+                                    kErrTimeoutEmpty, &abort_flag))
+          break;
+        mbar_arrive_expect_tx(&full_bar[s], tx);
+        const int kc = (k_begin + i) * kGBK;
+        tma_load_3d(smA + s * p.a_stage, &p.tmA, &full_bar[s], kc, m0, 0);
+        tma_load_3d(smB + s * p.b_stage, &p.tmB, &full_bar[s], kc, n0, 0);
+        issued = i + 1;
+      }
+      if (abort_flag) {
+        int dummy = 0;
+        volatile int no_abort = 0;
+        for (int i = max(0, issued - p.nb); i < issued; ++i)
+          mbar_wait(&full_bar[i % p.nb], static_cast<uint32_t>(i / p.nb) & 1u, &dummy, 0, &no_abort);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // waiter: one hand-off per stage, always (also after an abort)
+    for (int i = 0; i < nks; ++i) {
+      if (lane == 0 && !abort_flag)
+        mbar_wait(&full_bar[i % p.nb], static_cast<uint32_t>(i / p.nb) & 1u, p.status, kErrTimeoutFull, &abort_flag);
+      __syncwarp();
+      stage_handoff();
+    }
+  } else if (warp == 1) {
+    const uint32_t idesc = idesc_bf16_f32(128, p.NB);
+    const uint32_t a0 = smem_u32(smA), b0 = smem_u32(smB);
+    for (int i = 0; i < nks; ++i) {
+      const int s = i % p.nb;
+      stage_handoff();
+      tc_fence_after();
+      if (lane == 0) {
+        if (!abort_flag) {
+#pragma unroll
+          for (int k = 0; k < kGBK / 16; ++k) {
+            const uint64_t da = smem_desc_kmajor(a0 + s * p.a_stage + k * 32, 1024, 2);
+            const uint64_t db = smem_desc_kmajor(b0 + s * p.b_stage + k * 32, 1024, 2);
+            tc_mma_bf16(tmem, da, db, idesc, (i | k) != 0 ? 1u : 0u);
+          }
+        }
+        tc_commit(&empty_bar[s]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) tc_commit(&accum_bar);
+    __syncwarp();
+  } else {
+    // epilogue warps 3..10: quarter q of the TMEM lanes, half `sub` of the column chunks
+    const int q = warp & 3;
+    const int sub = (warp - 3) >> 2;
+    const int m = m0 + q * 32 + lane;
+    const bool mvalid = m < p.M;
+    const float bm = (p.bias_m != nullptr && mvalid) ? p.bias_m[m] : 0.f;
+    const bool ok = mbar_wait(&accum_bar, 0, p.status, kErrTimeoutAccum, &abort_flag);
+    tc_fence_after();
+    const bool go = __all_sync(0xffffffffu, ok && !abort_flag) && nks > 0;
+    if (go) {
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      char* outp = static_cast<char*>(p.out) + (p.out_f32 ? 4 : 2) * split * p.split_stride;
+      for (int c0 = sub * kGCols; c0 < p.NB; c0 += 2 * kGCols) {
+        const int nvalid = min(kGCols, p.N - (n0 + c0));
+        if (nvalid <= 0) break;
+        uint32_t rr[kGCols];
+        tmem_ld_16x_32x32b(lane_addr + static_cast<uint32_t>(c0), rr);
+        tmem_ld_wait();
+        float v[kGCols];
+#pragma unroll
+        for (int j = 0; j < kGCols; ++j) {
+          const int n = n0 + c0 + j;
+          float sc = p.scale;
+          float bn = 0.f;
+          if (j < nvalid) {
+            if (p.scale_n != nullptr) sc *= __ldg(p.scale_n + n);
+            if (p.bias_n != nullptr) bn = __ldg(p.bias_n + n);
+          }
+          v[j] = __uint_as_float(rr[j]) * sc + bm + bn;
+        }
+        const long long e0 = static_cast<long long>(n0 + c0) * p.ldo + m;
+        if (mvalid) {
+          if (p.residual != nullptr) {
+            if (p.res_f32) {
+              const float* rp = static_cast<const float*>(p.residual) + e0;
+#pragma unroll
+              for (int j = 0; j < kGCols; ++j)
+                if (j < nvalid) v[j] += rp[j * p.ldo];
+            } else {
+              const __nv_bfloat16* rp = static_cast<const __nv_bfloat16*>(p.residual) + e0;
+#pragma unroll
+              for (int j = 0; j < kGCols; ++j)
+                if (j < nvalid) v[j] += __bfloat162float(rp[j * p.ldo]);
+            }
+          }
+          if (p.out_f32) {
+            float* op = reinterpret_cast<float*>(outp) + e0;
+#pragma unroll
+            for (int j = 0; j < kGCols; ++j)
+              if (j < nvalid) op[j * p.ldo] = v[j];
+          } else {
+            __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(outp) + e0;
+#pragma unroll
+            for (int j = 0; j < kGCols; ++j)
+              if (j < nvalid) op[j * p.ldo] = __float2bfloat16_rn(v[j]);
+          }
+          if (p.out2 != nullptr) {
+            __nv_bfloat16* op = p.out2 + e0;
+#pragma unroll
+            for (int j = 0; j < kGCols; ++j)
+              if (j < nvalid) op[j * p.ldo] = __float2bfloat16_rn(v[j]);
+          }
+        }
+        __syncwarp();   // reconverge before the next warp-wide TMEM load
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+int round_up_g(int a, int b) { return (a + b - 1) / b * b; }
+
+// out[i] = sum over splits s (in order) of part[s * stride + i]; four values per thread.
+template <typename O>
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, long long stride, long long n4,
+                                     O* __restrict__ out) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    float4 acc = reinterpret_cast<const float4*>(part)[i];
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = reinterpret_cast<const float4*>(part + s * stride)[i];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if constexpr (sizeof(O) == 4) {
+      reinterpret_cast<float4*>(out)[i] = acc;
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(out)[i] = u;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_splitk_reduce(const float* part, int splits, long long split_stride, long long count,
+                                 int out_dtype, void* out, cudaStream_t stream) {
+  if (count <= 0) return cudaSuccess;
+  if ((count % 4) || (split_stride % 4)) return cudaErrorInvalidValue;
+  const long long n4 = count / 4;
+  long long blocks = (n4 + 255) / 256;
+  if (blocks > 152LL * 8) blocks = 152LL * 8;
+  if (out_dtype == kBF16)
+    splitk_reduce_kernel<__nv_bfloat16><<<(int)blocks, 256, 0, stream>>>(part, splits, split_stride, n4,
+                                                                          static_cast<__nv_bfloat16*>(out));
+  else
+    splitk_reduce_kernel<float><<<(int)blocks, 256, 0, stream>>>(part, splits, split_stride, n4,
+                                                                  static_cast<float*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, const char** why) {
+  *why = nullptr;
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) {
+    *why = "cuTensorMapEncodeTiled unavailable";
+    return cudaErrorNotSupported;
+  }
+  if (a.M < 1 || a.N < 1 || a.K < 1 || a.splits < 1) return cudaSuccess;
+  if ((a.lda % 8) || (a.ldb % 8) || a.lda < a.K || a.ldb < a.K) {
+    *why = "GEMM operand rows must be 16-byte aligned and at least K long";
+    return cudaErrorInvalidValue;
+  }
+  if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) & 15) {
+    *why = "GEMM operands must be 16-byte aligned";
+    return cudaErrorInvalidValue;
+  }
+  if (a.splits > 1 && !a.out_f32) {
+    *why = "split-K GEMM needs fp32 partial output";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.NB = std::min(256, round_up_g(a.N, 16));
+  p.n_mtiles = (a.M + 127) / 128;
+  p.n_ntiles = (a.N + p.NB - 1) / p.NB;
+  p.nk = (a.K + kGBK - 1) / kGBK;
+  p.splits = std::min(a.splits, p.nk);
+  p.a_stage = 128 * kGBK * 2;
+  p.b_stage = static_cast<uint32_t>(round_up_g(p.NB * kGBK * 2, 1024));
+  // one CTA per SM with a deep pipeline, or (two_per_sm) a pipeline small enough
+  // that a second CTA's MMAs overlap this CTA's epilogue
+  const int budget = a.two_per_sm ? 110 * 1024 : 200 * 1024;
+  p.nb = std::min(kGMaxStages, static_cast<int>(budget / (p.a_stage + p.b_stage)));
+  if (p.nb < 2) {
+    *why = "GEMM tile does not fit two pipeline stages";
+    return cudaErrorInvalidValue;
+  }
+  p.tmem_cols = 32;
+  while (p.tmem_cols < static_cast<uint32_t>(p.NB)) p.tmem_cols <<= 1;
+  p.out = a.out;
+  p.ldo = a.ldo;
+  p.split_stride = a.split_stride;
+  p.out_f32 = a.out_f32;
+  p.res_f32 = a.res_f32;
+  p.bias_m = a.bias_m;
+  p.bias_n = a.bias_n;
+  p.scale_n = a.scale_n;
+  p.scale = a.scale;
+  p.residual = a.residual;
+  p.out2 = static_cast<__nv_bfloat16*>(a.out2);
+  p.status = status;
+  const cuuint32_t ones[3] = {1, 1, 1};
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)a.K, (cuuint64_t)a.M, 1};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.lda * 2, (cuuint64_t)a.lda * 2 * a.M};
+    const cuuint32_t box[3] = {kGBK, 128, 1};
+    if (enc(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.A), dims, strides, box, ones,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      *why = "GEMM A tensor map rejected";
+      return cudaErrorInvalidValue;
+    }
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)a.K, (cuuint64_t)a.N, 1};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.ldb * 2, (cuuint64_t)a.ldb * 2 * a.N};
+    const cuuint32_t box[3] = {kGBK, (cuuint32_t)p.NB, 1};
+    if (enc(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.B), dims, strides, box, ones,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      *why = "GEMM B tensor map rejected";
+      return cudaErrorInvalidValue;
+    }
+  }
+  const size_t smem = (size_t)p.nb * (p.a_stage + p.b_stage) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(gemm_cm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_mtiles * p.n_ntiles, p.splits);
+  gemm_cm_kernel<<<grid, kGThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace vd

@@ -67,6 +67,37 @@ cudaError_t launch_gn_apply(int in_dtype, int out_dtype, const void* x, void* y,
 cudaError_t launch_rms_norm(int in_dtype, int out_dtype, const void* x, void* y, void* y_raw, long long pixels,
                             int C, const float* gamma, int silu, cudaStream_t stream);
 
+// ---------------------------------------------------------------- GEMM
+// D[m, n] = scale * scale_n[n] * sum_k A[m, k] B[n, k] + bias_m[m] + bias_n[n]
+// (+ residual), stored channel-major: out[n * ldo + m].  A is [M][lda] and B
+// [N][ldb] bf16, K contiguous, rows 16-byte aligned.  With splits > 1 the K range
+// is divided among `splits` CTAs that write fp32 partials to
+// out + s * split_stride (combine them with launch_splitk_reduce).
+struct GemmArgs {
+  const void* A = nullptr;
+  long long lda = 0;
+  const void* B = nullptr;
+  long long ldb = 0;
+  int M = 0, N = 0, K = 0;
+  void* out = nullptr;
+  long long ldo = 0;
+  int out_f32 = 1;
+  int splits = 1;
+  long long split_stride = 0;
+  const float* bias_m = nullptr;
+  const float* bias_n = nullptr;
+  const float* scale_n = nullptr;
+  float scale = 1.f;
+  const void* residual = nullptr;   // same layout and ldo as out
+  int res_f32 = 0;
+  void* out2 = nullptr;             // optional bf16 copy of out
+  int two_per_sm = 0;               // smaller pipeline so two CTAs share an SM
+};
+cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, const char** why);
+// out[i] = sum_s part[s * split_stride + i] for i < count (count, split_stride multiples of 4).
+cudaError_t launch_splitk_reduce(const float* part, int splits, long long split_stride, long long count,
+                                 int out_dtype, void* out, cudaStream_t stream);
+
 // ---------------------------------------------------------------- attention
 // Row softmax numerators: P[r, k] = exp(S[r, k] - max_k S[r, :]) stored as
 // `p_dtype`, inv_l[r] = 1 / sum_k P[r, k] (sum of the stored values).

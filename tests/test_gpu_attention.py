@@ -1,0 +1,46 @@
+"""GPU parity of the attention block at sizes that span many tensor-core tiles.
+
+4608 keys per frame is above the point where the probabilities x values product
+is split along the keys (fp32 partials combined in a fixed order), and 72 rows
+cut into 5 bands gives ragged band heights (15, 15, 14, 14, 14), so query tiles
+end mid-band.  The attention op's output is compared with the oracle's
+attention block applied to the same captured input, and the op output must not
+depend on the band count at all (band-local queries against global keys).
+"""
+import numpy as np
+import pytest
+
+import synth
+from gpu_helpers import Case, oracle_op, parse_shape, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+ATTN_REL = 1.2e-2   # bf16 Q/K/V/P operands and one bf16 rounding of the output
+
+
+def _attention_op(case, n_bands):
+    for op in range(case.dec.num_ops(case.shape, n_bands)):
+        d = case.dec.op_desc(case.shape, n_bands, op)
+        if d["kind"] == "attention":
+            return op
+    raise AssertionError("no attention op")
+
+
+def _check(case, bands):
+    outs = []
+    for nb in bands:
+        d, x, aux, y = case.capture(nb, _attention_op(case, nb))
+        ref = oracle_op(d, case.W, case.arch, x.reshape(parse_shape(d["in"])), aux)
+        err = rel_l2(y.reshape(ref.shape), ref)
+        assert err <= ATTN_REL, f"bands {nb}: rel-L2 {err:.3e}"
+        outs.append(y)
+    for y in outs[1:]:
+        np.testing.assert_array_equal(y, outs[0])
+
+
+def test_kl_attention_4608_keys():
+    _check(Case(synth.KL_ZIMAGE, "bf16", (1, 16, 72, 64)), (1, 5))
+
+
+def test_wan_attention_two_frames_4608_keys():
+    _check(Case(synth.WAN, "bf16", (1, 16, 2, 48, 96)), (1, 3))
