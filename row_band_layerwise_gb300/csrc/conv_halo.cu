@@ -163,12 +163,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1) conv_halo_kernel(const __grid
       }
       if (abort_flag) {
         // drain: every stage this thread filled lands before the CTA exits (bounded)
-        int dummy = 0;
-        volatile int no_abort = 0;
         for (int ac = max(0, issued_a - 2); ac < issued_a; ++ac)
-          mbar_wait(&a_full[ac & 1], static_cast<uint32_t>(ac >> 1) & 1u, &dummy, 0, &no_abort);
+          mbar_drain(&a_full[ac & 1], static_cast<uint32_t>(ac >> 1) & 1u);
         for (int k = max(0, issued_b - p.nb); k < issued_b; ++k)
-          mbar_wait(&b_full[k % p.nb], static_cast<uint32_t>(k / p.nb) & 1u, &dummy, 0, &no_abort);
+          mbar_drain(&b_full[k % p.nb], static_cast<uint32_t>(k / p.nb) & 1u);
       }
     }
     __syncwarp();   // reconverge warp 0 before the CTA-wide barrier

@@ -34,6 +34,7 @@ namespace vd {
 namespace {
 
 constexpr int kThreadsT = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue (two per TMEM lane quarter)
+constexpr int kEpiWarpsT = 8;
 constexpr int kMaxWStages = 4;
 constexpr int kPipeBytesT = 212 * 1024;
 
@@ -44,7 +45,10 @@ struct HaloTParams {
   int R;                         // output rows per CTA
   int npx;                       // pixels per tile (MMA N)
   int half;                      // pixels per staging box (two boxes per staged row)
-  int tiles_x, tiles_y, n_mtiles, n_kchunks, ndt, nw;
+  int tiles_x, tiles_y, n_mtiles, n_kchunks, ndt, nw, ntiles;
+  int nbuf;                      // accumulator buffers in TMEM (2: a tile's epilogue overlaps the next tile's MMAs)
+  int acc_cols;                  // TMEM columns per buffer
+  int csplit;                    // 2: the two epilogue warp halves split a row's pixels (R == 1), else 1
   uint32_t row_bytes, x_stage_bytes, w_tap_bytes, w_stage_bytes, tmem_cols;
   const float* bias;
   const void* residual;
@@ -79,12 +83,34 @@ __device__ __forceinline__ void moments_merge(float na, float ma, float m2a, flo
   n = nt;
 }
 
+struct TileT {
+  int mtile, phase, tx, ty, tt, bb, x0, y0, m0;
+};
+
+__device__ __forceinline__ TileT decode_tile(const HaloTParams& p, int t) {
+  TileT d;
+  d.mtile = t % p.n_mtiles;
+  t /= p.n_mtiles;
+  d.phase = t % p.g.nphase;
+  t /= p.g.nphase;
+  d.tx = t % p.tiles_x;
+  t /= p.tiles_x;
+  d.ty = t % p.tiles_y;
+  t /= p.tiles_y;
+  d.tt = t % p.g.T;
+  d.bb = t / p.g.T;
+  d.x0 = d.tx * p.npx;
+  d.y0 = d.ty * p.R;
+  d.m0 = d.mtile * 128;
+  return d;
+}
+
 template <int BK>
 __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_constant__ HaloTParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t x_full[2], x_empty[2];
   __shared__ __align__(8) uint64_t w_full[kMaxWStages], w_empty[kMaxWStages];
-  __shared__ __align__(8) uint64_t accum_bar;
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -94,31 +120,20 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smX = smem;
   uint8_t* smW = smem + 2 * p.x_stage_bytes;
-
-  int bid = blockIdx.x;
-  const int mtile = bid % p.n_mtiles;
-  bid /= p.n_mtiles;
-  const int phase = bid % g.nphase;
-  bid /= g.nphase;
-  const int tx = bid % p.tiles_x;
-  bid /= p.tiles_x;
-  const int ty = bid % p.tiles_y;
-  bid /= p.tiles_y;
-  const int tt = bid % g.T;
-  const int bb = bid / g.T;
-  const int x0 = tx * p.npx, y0 = ty * p.R, m0 = mtile * 128;
   const int nsp = g.ntaps / p.ndt;   // 9 spatial taps per causal frame, in three kernel rows of 3
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&x_full[i], 1);
       mbar_init(&x_empty[i], 1);
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiWarpsT);
     }
     for (int i = 0; i < p.nw; ++i) {
       mbar_init(&w_full[i], 1);
       mbar_init(&w_empty[i], 1);
     }
-    mbar_init(&accum_bar, 1);
+    mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -135,161 +150,210 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const int nac = p.ndt * p.n_kchunks;   // staged activation chunks
+  const int nac = p.ndt * p.n_kchunks;   // staged activation chunks per tile
   const int ngrp = nsp / 3;              // weight stages per chunk (kernel rows)
 
   if (warp == 0) {
+    // ---- TMA producer: activation chunks (R + 2 rows) and weight stages (3 taps), tile after tile
     if (lane == 0) {
       const uint32_t x_tx = static_cast<uint32_t>((p.R + 2) * 2 * p.half * BK * 2);
       const uint32_t w_tx = static_cast<uint32_t>(3 * 128 * BK * 2);
-      int kb = 0, issued_x = 0, issued_w = 0;
-      for (int ac = 0; ac < nac && !abort_flag; ++ac) {
-        const int dti = ac / p.n_kchunks;
-        const int kc = ac - dti * p.n_kchunks;
-        const int dt = g.taps[phase][dti * nsp].dt;
-        const int sx = ac & 1;
-        if (ac >= 2 && !mbar_wait(&x_empty[sx], (static_cast<uint32_t>(ac >> 1) & 1u) ^ 1u, p.status,
-                                  kErrTimeoutEmpty, &abort_flag))
-          break;
-        mbar_arrive_expect_tx(&x_full[sx], x_tx);
-        uint8_t* xs = smX + sx * p.x_stage_bytes;
-        for (int rb = 0; rb < p.R + 2; ++rb) {
-          tma_load_5d(xs + rb * p.row_bytes, &p.tmX, &x_full[sx], kc * BK, x0 - 1, y0 - 1 + rb, tt + dt, bb);
-          tma_load_5d(xs + rb * p.row_bytes + p.half * BK * 2, &p.tmX, &x_full[sx], kc * BK, x0 - 1 + p.half,
-                      y0 - 1 + rb, tt + dt, bb);
-        }
-        issued_x = ac + 1;
-        for (int gi = 0; gi < ngrp; ++gi, ++kb) {
-          const int sw = kb % p.nw;
-          if (kb >= p.nw && !mbar_wait(&w_empty[sw], (static_cast<uint32_t>(kb / p.nw) & 1u) ^ 1u, p.status,
-                                       kErrTimeoutEmpty, &abort_flag))
+      int acg = 0, kbg = 0;   // chunks / weight stages issued so far (all tiles)
+      for (int t = blockIdx.x; t < p.ntiles && !abort_flag; t += gridDim.x) {
+        const TileT d = decode_tile(p, t);
+        for (int ac = 0; ac < nac && !abort_flag; ++ac) {
+          const int dti = ac / p.n_kchunks;
+          const int kc = ac - dti * p.n_kchunks;
+          const int dt = g.taps[d.phase][dti * nsp].dt;
+          const int sx = acg & 1;
+          if (acg >= 2 && !mbar_wait(&x_empty[sx], (static_cast<uint32_t>(acg >> 1) & 1u) ^ 1u, p.status,
+                                     kErrTimeoutEmpty, &abort_flag))
             break;
-          mbar_arrive_expect_tx(&w_full[sw], w_tx);
-          uint8_t* ws = smW + sw * p.w_stage_bytes;
-          for (int t = 0; t < 3; ++t)
-            tma_load_3d(ws + t * p.w_tap_bytes, &p.tmW, &w_full[sw], kc * BK,
-                        g.taps[phase][dti * nsp + gi * 3 + t].wtap, m0);
-          issued_w = kb + 1;
+          mbar_arrive_expect_tx(&x_full[sx], x_tx);
+          uint8_t* xs = smX + sx * p.x_stage_bytes;
+          for (int rb = 0; rb < p.R + 2; ++rb) {
+            tma_load_5d(xs + rb * p.row_bytes, &p.tmX, &x_full[sx], kc * BK, d.x0 - 1, d.y0 - 1 + rb, d.tt + dt,
+                        d.bb);
+            tma_load_5d(xs + rb * p.row_bytes + p.half * BK * 2, &p.tmX, &x_full[sx], kc * BK, d.x0 - 1 + p.half,
+                        d.y0 - 1 + rb, d.tt + dt, d.bb);
+          }
+          ++acg;
+          for (int gi = 0; gi < ngrp; ++gi) {
+            const int sw = kbg % p.nw;
+            if (kbg >= p.nw && !mbar_wait(&w_empty[sw], (static_cast<uint32_t>(kbg / p.nw) & 1u) ^ 1u, p.status,
+                                          kErrTimeoutEmpty, &abort_flag))
+              break;
+            mbar_arrive_expect_tx(&w_full[sw], w_tx);
+            uint8_t* ws = smW + sw * p.w_stage_bytes;
+            for (int tp = 0; tp < 3; ++tp)
+              tma_load_3d(ws + tp * p.w_tap_bytes, &p.tmW, &w_full[sw], kc * BK,
+                          g.taps[d.phase][dti * nsp + gi * 3 + tp].wtap, d.m0);
+            ++kbg;
+          }
         }
       }
       if (abort_flag) {
-        int dummy = 0;
-        volatile int no_abort = 0;
-        for (int ac = max(0, issued_x - 2); ac < issued_x; ++ac)
-          mbar_wait(&x_full[ac & 1], static_cast<uint32_t>(ac >> 1) & 1u, &dummy, 0, &no_abort);
-        for (int k = max(0, issued_w - p.nw); k < issued_w; ++k)
-          mbar_wait(&w_full[k % p.nw], static_cast<uint32_t>(k / p.nw) & 1u, &dummy, 0, &no_abort);
+        // let the copies already issued land before the CTA exits
+        for (int i = max(0, acg - 2); i < acg; ++i)
+          mbar_drain(&x_full[i & 1], static_cast<uint32_t>(i >> 1) & 1u);
+        for (int k = max(0, kbg - p.nw); k < kbg; ++k)
+          mbar_drain(&w_full[k % p.nw], static_cast<uint32_t>(k / p.nw) & 1u);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ---- MMA issuer: tile i accumulates into TMEM buffer i % nbuf
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, p.npx);
       const uint32_t x_base0 = smem_u32(smX), w_base0 = smem_u32(smW);
-      int kb = 0;
+      int acg = 0, kbg = 0, it = 0;
       bool ok = true;
-      for (int ac = 0; ac < nac && ok; ++ac) {
-        const int dti = ac / p.n_kchunks;
-        const int sx = ac & 1;
-        if (!mbar_wait(&x_full[sx], static_cast<uint32_t>(ac >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag)) {
-          ok = false;
+      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x, ++it) {
+        const int phase = decode_tile(p, t).phase;
+        const int buf = it % p.nbuf;
+        if (it >= p.nbuf && !mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it / p.nbuf) & 1u) ^ 1u, p.status,
+                                       kErrTimeoutEmpty, &abort_flag))
           break;
-        }
         tc_fence_after();
-        const uint32_t xb = x_base0 + sx * p.x_stage_bytes;
-        for (int gi = 0; gi < ngrp; ++gi, ++kb) {
-          const int sw = kb % p.nw;
-          if (!mbar_wait(&w_full[sw], static_cast<uint32_t>(kb / p.nw) & 1u, p.status, kErrTimeoutFull,
-                         &abort_flag)) {
+        const uint32_t dbase = tmem + static_cast<uint32_t>(buf * p.acc_cols);
+        for (int ac = 0; ac < nac && ok; ++ac) {
+          const int dti = ac / p.n_kchunks;
+          const int sx = acg & 1;
+          if (!mbar_wait(&x_full[sx], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t wb = w_base0 + sw * p.w_stage_bytes;
-          for (int t = 0; t < 3; ++t) {
-            const ConvTap tp = g.taps[phase][dti * nsp + gi * 3 + t];
-            const uint32_t wa = wb + t * p.w_tap_bytes;
-            for (int r = 0; r < p.R; ++r) {
-              const uint32_t xa = xb + (r + tp.dy + 1) * p.row_bytes + static_cast<uint32_t>((tp.dx + 1) * BK * 2);
+          const uint32_t xb = x_base0 + sx * p.x_stage_bytes;
+          for (int gi = 0; gi < ngrp; ++gi, ++kbg) {
+            const int sw = kbg % p.nw;
+            if (!mbar_wait(&w_full[sw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
+                           &abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t wb = w_base0 + sw * p.w_stage_bytes;
+            for (int tp = 0; tp < 3; ++tp) {
+              const ConvTap tap = g.taps[phase][dti * nsp + gi * 3 + tp];
+              const uint32_t wa = wb + tp * p.w_tap_bytes;
+              for (int r = 0; r < p.R; ++r) {
+                const uint32_t xa =
+                    xb + (r + tap.dy + 1) * p.row_bytes + static_cast<uint32_t>((tap.dx + 1) * BK * 2);
 #pragma unroll
-              for (int k = 0; k < BK / 16; ++k) {
-                const uint64_t da = smem_desc_kmajor(wa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
-                const uint64_t db = smem_desc_kmajor(xa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
-                tc_mma_bf16(tmem + static_cast<uint32_t>(r * p.npx), da, db, idesc, (ac | gi | t | k) != 0 ? 1u : 0u);
+                for (int k = 0; k < BK / 16; ++k) {
+                  const uint64_t da = smem_desc_kmajor(wa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
+                  const uint64_t db = smem_desc_kmajor(xa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
+                  tc_mma_bf16(dbase + static_cast<uint32_t>(r * p.npx), da, db, idesc,
+                              (ac | gi | tp | k) != 0 ? 1u : 0u);
+                }
               }
             }
+            tc_commit(&w_empty[sw]);
           }
-          tc_commit(&w_empty[sw]);
+          if (!ok) break;
+          tc_commit(&x_empty[sx]);
+          ++acg;
         }
-        tc_commit(&x_empty[sx]);
+        if (ok) tc_commit(&acc_full[buf]);
       }
-      tc_commit(&accum_bar);
+      // every MMA issued has completed before the CTA releases TMEM (also after a timeout)
+      tc_commit(&mma_done);
+      mbar_drain(&mma_done, 0);
     }
     __syncwarp();
   } else {
-    // ---- epilogue: TMEM lane = output channel; columns = pixels of the tile row
+    // ---- epilogue (warps 2..9): TMEM lane = output channel; columns = pixels of a tile row
     const int q = warp & 3;
-    const int sub = (warp - 2) >> 2;   // 0 for warps 2..5, 1 for warps 6..9: rows r with r % 2 == sub
-    const int co = m0 + q * 32 + lane;
-    const bool cvalid = co < g.Cout;
-    const float bias = (p.bias != nullptr && cvalid) ? p.bias[co] : 0.f;
-    const bool ok = mbar_wait(&accum_bar, 0, p.status, kErrTimeoutAccum, &abort_flag);
-    tc_fence_after();
-    const bool go = __all_sync(0xffffffffu, ok && !abort_flag);
-    if (go) {
-      const int py = phase >> 1, px = phase & 1;
-      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      const bool res_f32 = g.res_f32 != 0;
-      for (int r = sub; r < p.R; r += 2) {
-        const int y = y0 + r;
-        if (y >= g.H) break;   // uniform across the warp
-        const int yo = y * g.osy + (g.nphase > 1 ? py : 0);
-        const long long row_pix = ((static_cast<long long>(bb) * g.oT + tt) * g.oH + yo) * static_cast<long long>(g.oW);
-        float sn = 0.f, smean = 0.f, sm2 = 0.f;   // this channel's moments over the tile row
-        for (int c0 = 0; c0 < p.npx; c0 += 32) {
+    const int sub = (warp - 2) >> 2;   // csplit 1: rows r with r % 2 == sub; csplit 2: half `sub` of the row
+    const int hc = p.csplit == 2 ? (((p.npx + 1) / 2 + 31) & ~31) : p.npx;
+    const int r_begin = p.csplit == 2 ? 0 : sub, r_step = p.csplit == 2 ? 1 : 2;
+    const int c_begin = p.csplit == 2 ? sub * hc : 0, c_end = p.csplit == 2 ? min(p.npx, (sub + 1) * hc) : p.npx;
+    const long long stride = static_cast<long long>(g.osx) * g.oC;   // elements between neighbouring pixels
+    const bool res_f32 = g.res_f32 != 0;
+    const int rsize = res_f32 ? 4 : 2;
+    int it = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
+      const TileT d = decode_tile(p, t);
+      const int buf = it % p.nbuf;
+      const int co = d.m0 + q * 32 + lane;
+      const bool cvalid = co < g.Cout;
+      const float bias = (p.bias != nullptr && cvalid) ? p.bias[co] : 0.f;
+      const int py = d.phase >> 1, px = d.phase & 1;
+      auto row_first = [&](int r) -> long long {   // element (first pixel of the tile row, channel 0)
+        const int yo = (d.y0 + r) * g.osy + (g.nphase > 1 ? py : 0);
+        const long long row_pix =
+            ((static_cast<long long>(d.bb) * g.oT + d.tt) * g.oH + yo) * static_cast<long long>(g.oW);
+        return (row_pix + static_cast<long long>(d.x0) * g.osx + (g.nphase > 1 ? px : 0)) * g.oC;
+      };
+      if (p.residual != nullptr && warp == 2 && lane == 0) {
+        // pull this tile's residual rows into L2 while its MMAs run (whole pixels, all channels: contiguous)
+        const int nv = min(p.npx, g.W - d.x0);
+        for (int r = 0; r < p.R && d.y0 + r < g.H; ++r) {
+          const char* base = static_cast<const char*>(p.residual) + row_first(r) * rsize;
+          const long long bytes = (static_cast<long long>(nv - 1) * stride + g.oC) * rsize;
+          for (long long off = 0; off < bytes; off += 32768)
+            l2_prefetch_bulk(base + off, static_cast<uint32_t>(min(32768LL, bytes - off)));
+        }
+      }
+      const bool ok = mbar_wait(&acc_full[buf], static_cast<uint32_t>(it / p.nbuf) & 1u, p.status, kErrTimeoutAccum,
+                                &abort_flag);
+      tc_fence_after();
+      if (!__all_sync(0xffffffffu, ok && !abort_flag)) break;
+      const uint32_t lane_addr = tmem + static_cast<uint32_t>(buf * p.acc_cols) + (static_cast<uint32_t>(q * 32) << 16);
+      const bool has_res = p.residual != nullptr && cvalid;
+      for (int r = r_begin; r < p.R; r += r_step) {
+        if (d.y0 + r >= g.H) break;   // uniform across the warp
+        const long long erow = row_first(r) + co;
+        // residual of chunk c0 in rv; the next chunk's loads are issued before this one is used
+        float rv[32], rn[32];
+        auto load_res = [&](int c0, float (&dst)[32]) {
+          const int nvalid = min(32, min(c_end - c0, g.W - (d.x0 + c0)));
+          const long long e0 = erow + static_cast<long long>(c0) * stride;
+          if (res_f32) {
+            const float* rp = static_cast<const float*>(p.residual) + e0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[j] = (j < nvalid) ? rp[j * stride] : 0.f;
+          } else {
+            const __nv_bfloat16* rp = static_cast<const __nv_bfloat16*>(p.residual) + e0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[j] = (j < nvalid) ? __bfloat162float(rp[j * stride]) : 0.f;
+          }
+        };
+        if (has_res && c_begin < c_end && d.x0 + c_begin < g.W) load_res(c_begin, rv);
+        // GroupNorm moments of this channel over the tile row: sums shifted by the row's first value
+        float kshift = 0.f, s1 = 0.f, s2 = 0.f, cnt = 0.f;
+        for (int c0 = c_begin; c0 < c_end; c0 += 32) {
+          const int nvalid = min(32, min(c_end - c0, g.W - (d.x0 + c0)));
+          if (nvalid <= 0) break;   // uniform across the warp
           uint32_t rr[32];
           tmem_ld_32x32b_x32(lane_addr + static_cast<uint32_t>(r * p.npx + c0), rr);
+          if (has_res && c0 + 32 < c_end && d.x0 + c0 + 32 < g.W) load_res(c0 + 32, rn);
           tmem_ld_wait();
-          const int nvalid = min(32, min(p.npx - c0, g.W - (x0 + c0)));
-          if (nvalid <= 0) break;
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]) * g.scale + bias;
-          // element offset of (pixel x0 + c0 + j, channel co)
-          const long long px0 = row_pix + static_cast<long long>(x0 + c0) * g.osx + (g.nphase > 1 ? px : 0);
-          const long long stride = static_cast<long long>(g.osx) * g.oC;
-          const long long e0 = px0 * g.oC + co;
-          if (p.residual != nullptr && cvalid) {
-            if (res_f32) {
-              const float* rp = reinterpret_cast<const float*>(p.residual) + e0;
-              float rv[32];
+          if (has_res) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) rv[j] = (j < nvalid) ? rp[j * stride] : 0.f;
+            for (int j = 0; j < 32; ++j) v[j] += rv[j];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] += rv[j];
-            } else {
-              const __nv_bfloat16* rp = reinterpret_cast<const __nv_bfloat16*>(p.residual) + e0;
-              float rv[32];
-#pragma unroll
-              for (int j = 0; j < 32; ++j) rv[j] = (j < nvalid) ? __bfloat162float(rp[j * stride]) : 0.f;
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] += rv[j];
-            }
+            for (int j = 0; j < 32; ++j) rv[j] = rn[j];
           }
           if (p.gn_part != nullptr) {
-            float cs = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) cs += (j < nvalid) ? v[j] : 0.f;
-            const float cm = cs / static_cast<float>(nvalid);
-            float c2 = 0.f;
+            if (c0 == c_begin) kshift = v[0];
+            float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              const float d = (j < nvalid) ? v[j] - cm : 0.f;
-              c2 = fmaf(d, d, c2);
+              const float dv = (j < nvalid) ? v[j] - kshift : 0.f;
+              a1[j & 3] += dv;
+              a2[j & 3] = fmaf(dv, dv, a2[j & 3]);
             }
-            moments_merge(sn, smean, sm2, static_cast<float>(nvalid), cm, c2, sn, smean, sm2);
+            s1 += (a1[0] + a1[1]) + (a1[2] + a1[3]);
+            s2 += (a2[0] + a2[1]) + (a2[2] + a2[3]);
+            cnt += static_cast<float>(nvalid);
           }
           if (cvalid) {
+            const long long e0 = erow + static_cast<long long>(c0) * stride;
             if (g.out_f32) {
               float* op = reinterpret_cast<float*>(p.out) + e0;
 #pragma unroll
@@ -308,8 +372,16 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
                 if (j < nvalid) op[j * stride] = __float2bfloat16_rn(v[j]);
             }
           }
+          __syncwarp();   // reconverge before the next warp-wide TMEM load
         }
         if (p.gn_part != nullptr) {
+          // this channel's (count, mean, centred sum of squares) over the row
+          float sn = cnt, smean = 0.f, sm2 = 0.f;
+          if (cnt > 0.f) {
+            const float d1 = s1 / cnt;
+            smean = kshift + d1;
+            sm2 = fmaxf(s2 - s1 * d1, 0.f);
+          }
           // merge the group's channels (gn_cg consecutive lanes), lower lane first
           for (int off = 1; off < p.gn_cg; off <<= 1) {
             const float on = __shfl_xor_sync(0xffffffffu, sn, off);
@@ -321,11 +393,13 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
               moments_merge(sn, smean, sm2, on, om, o2, sn, smean, sm2);
           }
           if (cvalid && (lane % p.gn_cg) == 0) {
-            // chunk = (output row, phase column, pixel tile), fixed by the geometry alone
+            // chunk = (output row, phase column, pixel tile, column half), fixed by the geometry alone
+            const int yo = (d.y0 + r) * g.osy + (g.nphase > 1 ? py : 0);
             const int npxp = g.nphase > 1 ? 2 : 1;
-            const long long orow = static_cast<long long>(tt) * g.oH + yo;
-            const long long chunk =
-                ((static_cast<long long>(bb) * g.oT * g.oH + orow) * npxp + (g.nphase > 1 ? px : 0)) * p.tiles_x + tx;
+            const long long orow = static_cast<long long>(d.tt) * g.oH + yo;
+            const long long chunk = (((static_cast<long long>(d.bb) * g.oT * g.oH + orow) * npxp +
+                                      (g.nphase > 1 ? px : 0)) * p.tiles_x + d.tx) * p.csplit +
+                                    (p.csplit == 2 ? sub : 0);
             GnPartial o;
             o.n = sn;
             o.mean = smean;
@@ -335,8 +409,11 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
           }
         }
       }
+      // hand the accumulator buffer back to the MMA issuer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
-    tc_fence_before();
   }
 
   __syncthreads();
@@ -380,13 +457,27 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
   HaloTParams p;
   std::memset(&p, 0, sizeof(p));
   p.g = g;
-  // pixel tile: split the row into equal tiles of at most 256 pixels (multiple of 16)
+  // pixel tile: split the row into equal tiles of at most 256 pixels (multiple of 16).  Where the
+  // epilogue is heavy next to the MMA work (128 input channels, or up to 256 with a residual to
+  // read) and tiles have at least 192 pixels, a tile is one row in one of two 256-column
+  // accumulator buffers, so its epilogue overlaps the next tile's MMAs.  Otherwise R rows share
+  // one buffer of up to 512 columns: twice the pixels per weight fetch, which wins when the MMA
+  // work dominates (and keeps the MMAs wide: narrower ones are shared-memory bound).
   const int ntx = (g.W + 255) / 256;
   p.npx = round_up_t((g.W + ntx - 1) / ntx, 16);
   p.tiles_x = (g.W + p.npx - 1) / p.npx;
   p.half = round_up_t(p.npx + 2, 16) / 2;          // two boxes per staged row, multiple of 8 pixels each
-  p.R = std::max(1, std::min(4, 512 / p.npx));
+  const bool heavy_epilogue = g.Cin <= 128 || (g.Cin <= 256 && residual != nullptr);
+  if (p.npx >= 192 && heavy_epilogue) {
+    p.nbuf = 2;
+    p.R = 1;
+  } else {
+    p.nbuf = 1;
+    p.R = std::max(1, std::min(4, 512 / p.npx));
+  }
+  p.acc_cols = 512 / p.nbuf;
   while (p.R > 1 && p.R > g.H) --p.R;
+  p.csplit = p.R == 1 ? 2 : 1;
   p.n_mtiles = (g.Cout + 127) / 128;   // weight rows beyond w_rows read as zeros
   int bk = 0;
   for (int cand : {64, 32, 16}) {
@@ -410,8 +501,7 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
   p.w_stage_bytes = 3 * p.w_tap_bytes;
   p.nw = std::min(kMaxWStages, static_cast<int>((kPipeBytesT - 2 * p.x_stage_bytes) / p.w_stage_bytes));
   p.tiles_y = (g.H + p.R - 1) / p.R;
-  p.tmem_cols = 32;
-  while (p.tmem_cols < static_cast<uint32_t>(p.R * p.npx)) p.tmem_cols <<= 1;
+  p.tmem_cols = 512;
   p.bias = bias;
   p.residual = residual;
   p.out = out;
@@ -422,7 +512,7 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
     if (cg <= 32 && 32 % cg == 0) {
       p.gn_part = static_cast<GnPartial*>(g.gn_part);
       p.gn_cg = cg;
-      if (gn_chunks != nullptr) *gn_chunks = g.oT * g.oH * (g.nphase > 1 ? 2 : 1) * p.tiles_x;
+      if (gn_chunks != nullptr) *gn_chunks = g.oT * g.oH * (g.nphase > 1 ? 2 : 1) * p.tiles_x * p.csplit;
     }
   }
 
@@ -451,12 +541,19 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
       return cudaErrorInvalidValue;
     }
   }
-  const long long nblocks = (long long)g.B * g.T * p.tiles_y * p.tiles_x * g.nphase * p.n_mtiles;
-  if (nblocks <= 0) return cudaSuccess;
-  if (nblocks > 0x7fffffffLL) {
+  const long long ntiles = (long long)g.B * g.T * p.tiles_y * p.tiles_x * g.nphase * p.n_mtiles;
+  if (ntiles <= 0) return cudaSuccess;
+  if (ntiles > 0x7fffffffLL) {
     *why = "grid too large";
     return cudaErrorInvalidValue;
   }
+  p.ntiles = static_cast<int>(ntiles);
+  // persistent: one CTA per SM (the pipeline fills shared memory), tiles dealt round-robin
+  int dev = 0, sms = 0;
+  cudaError_t ea = cudaGetDevice(&dev);
+  if (ea == cudaSuccess) ea = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ea != cudaSuccess) return ea;
+  const long long nblocks = std::min<long long>(ntiles, std::max(1, sms));
   const size_t smem = 2 * (size_t)p.x_stage_bytes + (size_t)p.nw * p.w_stage_bytes + 1024;
   cudaError_t e;
   switch (bk) {

@@ -138,11 +138,9 @@ __global__ void __launch_bounds__(kThreads) conv_tc_kernel(const __grid_constant
       }
       if (abort_flag) {
         // Drain: wait (bounded) until every stage this thread filled has landed.
-        int dummy = 0;
-        volatile int no_abort = 0;
         for (int ks = max(0, issued - p.stages); ks < issued; ++ks) {
           const int s = ks % p.stages;
-          mbar_wait(&full_bar[s], static_cast<uint32_t>(ks / p.stages) & 1u, &dummy, 0, &no_abort);
+          mbar_drain(&full_bar[s], static_cast<uint32_t>(ks / p.stages) & 1u);
         }
       }
     }

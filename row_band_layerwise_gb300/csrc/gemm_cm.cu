@@ -114,10 +114,8 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
         issued = i + 1;
       }
       if (abort_flag) {
-        int dummy = 0;
-        volatile int no_abort = 0;
         for (int i = max(0, issued - p.nb); i < issued; ++i)
-          mbar_wait(&full_bar[i % p.nb], static_cast<uint32_t>(i / p.nb) & 1u, &dummy, 0, &no_abort);
+          mbar_drain(&full_bar[i % p.nb], static_cast<uint32_t>(i / p.nb) & 1u);
       }
     }
     __syncwarp();
