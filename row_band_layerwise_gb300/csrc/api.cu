@@ -332,6 +332,48 @@ class Walker {
     count();
     if (g.gn_part != nullptr) ++stats_epoch_;   // the moments buffer is about to be rewritten
     int gn_chunks = 0;
+    if (h_->dtype == kBF16 && g.ntaps == 1 && g.nphase == 1 && g.time_up_c == 0 && g.osx == 1 && g.osy == 1 &&
+        rowscale == nullptr && g.gn_part == nullptr && g.oT == g.T && g.oH == g.H && g.oW == g.W &&
+        (!g.out_chfirst || (residual == nullptr && out2 == nullptr))) {
+      // 1x1 convolution = channel-major GEMM: out[pixel][co] = W[co][:] . in[pixel][:]
+      const long long S = (long long)g.H * g.W;
+      GemmArgs a;
+      a.K = g.Cin;
+      a.out_f32 = g.out_f32;
+      a.scale = g.scale;
+      a.residual = residual;
+      a.res_f32 = g.res_f32;
+      a.out2 = out2;
+      if (!g.out_chfirst) {
+        a.A = wptr;
+        a.lda = (long long)w.ntaps * g.Cin;
+        a.M = g.Cout;
+        a.B = in;
+        a.ldb = g.Cin;
+        a.N = (int)((long long)g.B * g.T * S);
+        a.out = out;
+        a.ldo = g.oC;
+        a.bias_m = bias;
+        gemm(a, what, false);
+      } else {
+        // channels-first output: per frame, pixels on M and channels on N
+        const size_t ies = esz(h_->dtype), oes = g.out_f32 ? 4 : 2;
+        for (long long f = 0; f < (long long)g.B * g.T && live(); ++f) {
+          GemmArgs af = a;
+          af.A = static_cast<const char*>(in) + (size_t)(f * S * g.Cin) * ies;
+          af.lda = g.Cin;
+          af.M = (int)S;
+          af.B = wptr;
+          af.ldb = (long long)w.ntaps * g.Cin;
+          af.N = g.Cout;
+          af.out = static_cast<char*>(out) + (size_t)(f * g.oC * S) * oes;
+          af.ldo = S;
+          af.bias_n = bias;
+          gemm(af, what, f > 0);
+        }
+      }
+      return 0;
+    }
     if (h_->dtype == kBF16) {
       const char* why = nullptr;
       cudaError_t e = launch_conv_tc(g, in, wptr, w.ntaps, w.rows, bias, residual, rowscale, out, out2, h_->status,
@@ -346,8 +388,8 @@ class Walker {
   }
 
   // Launch one channel-major tensor-core GEMM (bf16 path only).
-  void gemm(const GemmArgs& a, const char* what) {
-    count();
+  void gemm(const GemmArgs& a, const char* what, bool count_it = true) {
+    if (count_it) count();
     const char* why = nullptr;
     cudaError_t e = launch_gemm_cm(a, h_->status, st_, &why);
     if (e != cudaSuccess) set_err(VAEDEC_ERR_CUDA, std::string(what) + ": " + (why ? why : cudaGetErrorString(e)));

@@ -2,9 +2,12 @@
 // stored at out[n * ldo + m].
 //
 // Used for the attention products (scores = keys x queries, probabilities x
-// values with the sum over keys split across CTAs) and the 1x1 projections.  A
-// CTA computes a 128 (m) x NB (n, up to 256) tile; every TMEM lane is one m, so
-// each epilogue store instruction writes 32 consecutive m of one n: coalesced.
+// values with the sum over keys split across tiles) and the 1x1 convolutions.  A
+// tile is 128 (m) x NB (n, up to 256); every TMEM lane is one m, so each epilogue
+// store instruction writes 32 consecutive m of one n: coalesced.  The kernel is
+// persistent (one CTA per SM, tiles dealt round-robin) with two accumulator
+// buffers in TMEM: the epilogue of tile i overlaps the MMAs of tile i + 1, and the
+// producer streams the next tile's K chunks while the current one finishes.
 //
 // Roles (352 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
 // warp 2 stage waiter, warps 3..10 epilogue.  The waiter polls the stage
@@ -33,12 +36,13 @@ constexpr int kGThreads = 352;
 constexpr int kGMaxStages = 4;
 constexpr int kGBK = 64;   // K chunk (128B swizzle)
 constexpr int kGCols = 16; // accumulator columns per epilogue step
+constexpr int kGEpiWarps = 8;
 
 struct GemmParams {
   CUtensorMap tmA;   // (K, M) box (64, 128)
   CUtensorMap tmB;   // (K, N) box (64, NB)
-  int M, N, K, NB, n_mtiles, n_ntiles, nk, splits, nb;
-  uint32_t a_stage, b_stage, tmem_cols;
+  int M, N, K, NB, n_mtiles, n_ntiles, nk, splits, nb, ntiles;
+  uint32_t a_stage, b_stage, acc_cols, tmem_cols;
   void* out;
   long long ldo, split_stride;
   int out_f32, res_f32;
@@ -51,13 +55,31 @@ struct GemmParams {
   int* status;
 };
 
+struct GTile {
+  int m0, n0, split, k_begin, nks;
+};
+
+// Tile t: m tile fastest (tiles running at the same time share their B rows), then n tile, then split.
+__device__ __forceinline__ GTile gemm_tile(const GemmParams& p, int t) {
+  GTile d;
+  const int mt = t % p.n_mtiles;
+  t /= p.n_mtiles;
+  const int nt = t % p.n_ntiles;
+  d.split = t / p.n_ntiles;
+  d.m0 = mt * 128;
+  d.n0 = nt * p.NB;
+  d.k_begin = static_cast<int>((long long)d.split * p.nk / p.splits);
+  d.nks = static_cast<int>((long long)(d.split + 1) * p.nk / p.splits) - d.k_begin;
+  return d;
+}
+
 // Named barrier 1, shared by the waiter warp and the MMA warp (64 threads).
 __device__ __forceinline__ void stage_handoff() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kGMaxStages], empty_bar[kGMaxStages];
-  __shared__ __align__(8) uint64_t accum_bar;
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -67,20 +89,16 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
   uint8_t* smA = smem;
   uint8_t* smB = smem + p.nb * p.a_stage;
 
-  const int mt = blockIdx.x % p.n_mtiles;
-  const int nt = blockIdx.x / p.n_mtiles;
-  const int split = blockIdx.y;
-  const int m0 = mt * 128, n0 = nt * p.NB;
-  const int k_begin = static_cast<int>((long long)split * p.nk / p.splits);
-  const int k_end = static_cast<int>((long long)(split + 1) * p.nk / p.splits);
-  const int nks = k_end - k_begin;
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.nb; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
-    mbar_init(&accum_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kGEpiWarps);
+    }
+    mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -99,79 +117,109 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
   const uint32_t tmem = tmem_base_sh;
 
   if (warp == 0) {
+    // ---- TMA producer: K chunks of every tile of this CTA, through the stage ring
     if (lane == 0) {
       const uint32_t tx = p.a_stage + static_cast<uint32_t>(p.NB * kGBK * 2);
-      int issued = 0;
-      for (int i = 0; i < nks && !abort_flag; ++i) {
-        const int s = i % p.nb;
-        if (i >= p.nb && !mbar_wait(&empty_bar[s], (static_cast<uint32_t>(i / p.nb) & 1u) ^ 1u, p.status,
-                                    kErrTimeoutEmpty, &abort_flag))
-          break;
-        mbar_arrive_expect_tx(&full_bar[s], tx);
-        const int kc = (k_begin + i) * kGBK;
-        tma_load_3d(smA + s * p.a_stage, &p.tmA, &full_bar[s], kc, m0, 0);
-        tma_load_3d(smB + s * p.b_stage, &p.tmB, &full_bar[s], kc, n0, 0);
-        issued = i + 1;
+      int g = 0;   // stages issued so far
+      for (int t = blockIdx.x; t < p.ntiles && !abort_flag; t += gridDim.x) {
+        const GTile d = gemm_tile(p, t);
+        for (int i = 0; i < d.nks && !abort_flag; ++i, ++g) {
+          const int s = g % p.nb;
+          if (g >= p.nb && !mbar_wait(&empty_bar[s], (static_cast<uint32_t>(g / p.nb) & 1u) ^ 1u, p.status,
+                                      kErrTimeoutEmpty, &abort_flag))
+            break;
+          mbar_arrive_expect_tx(&full_bar[s], tx);
+          const int kc = (d.k_begin + i) * kGBK;
+          tma_load_3d(smA + s * p.a_stage, &p.tmA, &full_bar[s], kc, d.m0, 0);
+          tma_load_3d(smB + s * p.b_stage, &p.tmB, &full_bar[s], kc, d.n0, 0);
+        }
       }
       if (abort_flag) {
-        for (int i = max(0, issued - p.nb); i < issued; ++i)
-          mbar_drain(&full_bar[i % p.nb], static_cast<uint32_t>(i / p.nb) & 1u);
+        // let the copies already issued land before the CTA exits
+        for (int i = max(0, g - p.nb); i < g; ++i) mbar_drain(&full_bar[i % p.nb], static_cast<uint32_t>(i / p.nb) & 1u);
       }
     }
     __syncwarp();
   } else if (warp == 2) {
-    // waiter: one hand-off per stage, always (also after an abort)
-    for (int i = 0; i < nks; ++i) {
-      if (lane == 0 && !abort_flag)
-        mbar_wait(&full_bar[i % p.nb], static_cast<uint32_t>(i / p.nb) & 1u, p.status, kErrTimeoutFull, &abort_flag);
-      __syncwarp();
-      stage_handoff();
+    // ---- waiter: one hand-off per stage of every tile, always (also after an abort)
+    int g = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+      const int nks = gemm_tile(p, t).nks;
+      for (int i = 0; i < nks; ++i, ++g) {
+        if (lane == 0 && !abort_flag)
+          mbar_wait(&full_bar[g % p.nb], static_cast<uint32_t>(g / p.nb) & 1u, p.status, kErrTimeoutFull,
+                    &abort_flag);
+        __syncwarp();
+        stage_handoff();
+      }
     }
   } else if (warp == 1) {
+    // ---- MMA issuer: tile i accumulates into TMEM buffer i & 1; same stage sequence as the waiter
     const uint32_t idesc = idesc_bf16_f32(128, p.NB);
     const uint32_t a0 = smem_u32(smA), b0 = smem_u32(smB);
-    for (int i = 0; i < nks; ++i) {
-      const int s = i % p.nb;
-      stage_handoff();
+    int g = 0, it = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
+      const int nks = gemm_tile(p, t).nks;
+      const int buf = it & 1;
+      if (lane == 0 && it >= 2 && !abort_flag)
+        mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, p.status, kErrTimeoutEmpty,
+                  &abort_flag);
+      __syncwarp();
       tc_fence_after();
-      if (lane == 0) {
-        if (!abort_flag) {
+      const uint32_t dbase = tmem + static_cast<uint32_t>(buf) * p.acc_cols;
+      for (int i = 0; i < nks; ++i, ++g) {
+        const int s = g % p.nb;
+        stage_handoff();
+        tc_fence_after();
+        if (lane == 0) {
+          if (!abort_flag) {
 #pragma unroll
-          for (int k = 0; k < kGBK / 16; ++k) {
-            const uint64_t da = smem_desc_kmajor(a0 + s * p.a_stage + k * 32, 1024, 2);
-            const uint64_t db = smem_desc_kmajor(b0 + s * p.b_stage + k * 32, 1024, 2);
-            tc_mma_bf16(tmem, da, db, idesc, (i | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kGBK / 16; ++k) {
+              const uint64_t da = smem_desc_kmajor(a0 + s * p.a_stage + k * 32, 1024, 2);
+              const uint64_t db = smem_desc_kmajor(b0 + s * p.b_stage + k * 32, 1024, 2);
+              tc_mma_bf16(dbase, da, db, idesc, (i | k) != 0 ? 1u : 0u);
+            }
           }
+          tc_commit(&empty_bar[s]);
         }
-        tc_commit(&empty_bar[s]);
+        __syncwarp();
       }
+      if (lane == 0) tc_commit(&acc_full[buf]);
       __syncwarp();
     }
-    if (lane == 0) tc_commit(&accum_bar);
+    // every MMA issued has completed before the CTA releases TMEM (also after a timeout)
+    if (lane == 0) {
+      tc_commit(&mma_done);
+      mbar_drain(&mma_done, 0);
+    }
     __syncwarp();
   } else {
-    // epilogue warps 3..10: quarter q of the TMEM lanes, half `sub` of the column chunks
+    // ---- epilogue warps 3..10: quarter q of the TMEM lanes, half `sub` of the column chunks
     const int q = warp & 3;
     const int sub = (warp - 3) >> 2;
-    const int m = m0 + q * 32 + lane;
-    const bool mvalid = m < p.M;
-    const float bm = (p.bias_m != nullptr && mvalid) ? p.bias_m[m] : 0.f;
-    const bool ok = mbar_wait(&accum_bar, 0, p.status, kErrTimeoutAccum, &abort_flag);
-    tc_fence_after();
-    const bool go = __all_sync(0xffffffffu, ok && !abort_flag) && nks > 0;
-    if (go) {
-      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      char* outp = static_cast<char*>(p.out) + (p.out_f32 ? 4 : 2) * split * p.split_stride;
-      for (int c0 = sub * kGCols; c0 < p.NB; c0 += 2 * kGCols) {
-        const int nvalid = min(kGCols, p.N - (n0 + c0));
-        if (nvalid <= 0) break;
+    int it = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
+      const GTile d = gemm_tile(p, t);
+      const int buf = it & 1;
+      const int m = d.m0 + q * 32 + lane;
+      const bool mvalid = m < p.M;
+      const float bm = (p.bias_m != nullptr && mvalid) ? p.bias_m[m] : 0.f;
+      const bool ok = mbar_wait(&acc_full[buf], static_cast<uint32_t>(it >> 1) & 1u, p.status, kErrTimeoutAccum,
+                                &abort_flag);
+      tc_fence_after();
+      if (!__all_sync(0xffffffffu, ok && !abort_flag)) break;
+      const uint32_t lane_addr = tmem + static_cast<uint32_t>(buf) * p.acc_cols + (static_cast<uint32_t>(q * 32) << 16);
+      char* outp = static_cast<char*>(p.out) + (p.out_f32 ? 4 : 2) * d.split * p.split_stride;
+      for (int c0 = sub * kGCols; c0 < p.NB && d.nks > 0; c0 += 2 * kGCols) {
+        const int nvalid = min(kGCols, p.N - (d.n0 + c0));
+        if (nvalid <= 0) break;   // uniform across the warp
         uint32_t rr[kGCols];
         tmem_ld_16x_32x32b(lane_addr + static_cast<uint32_t>(c0), rr);
         tmem_ld_wait();
         float v[kGCols];
 #pragma unroll
         for (int j = 0; j < kGCols; ++j) {
-          const int n = n0 + c0 + j;
+          const int n = d.n0 + c0 + j;
           float sc = p.scale;
           float bn = 0.f;
           if (j < nvalid) {
@@ -180,7 +228,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
           }
           v[j] = __uint_as_float(rr[j]) * sc + bm + bn;
         }
-        const long long e0 = static_cast<long long>(n0 + c0) * p.ldo + m;
+        const long long e0 = static_cast<long long>(d.n0 + c0) * p.ldo + m;
         if (mvalid) {
           if (p.residual != nullptr) {
             if (p.res_f32) {
@@ -215,8 +263,11 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
         }
         __syncwarp();   // reconverge before the next warp-wide TMEM load
       }
+      // hand the accumulator buffer back to the MMA issuer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
-    tc_fence_before();
   }
 
   __syncthreads();
@@ -304,16 +355,11 @@ cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, 
   p.splits = std::min(a.splits, p.nk);
   p.a_stage = 128 * kGBK * 2;
   p.b_stage = static_cast<uint32_t>(round_up_g(p.NB * kGBK * 2, 1024));
-  // one CTA per SM with a deep pipeline, or (two_per_sm) a pipeline small enough
-  // that a second CTA's MMAs overlap this CTA's epilogue
-  const int budget = a.two_per_sm ? 110 * 1024 : 200 * 1024;
-  p.nb = std::min(kGMaxStages, static_cast<int>(budget / (p.a_stage + p.b_stage)));
-  if (p.nb < 2) {
-    *why = "GEMM tile does not fit two pipeline stages";
-    return cudaErrorInvalidValue;
-  }
-  p.tmem_cols = 32;
-  while (p.tmem_cols < static_cast<uint32_t>(p.NB)) p.tmem_cols <<= 1;
+  // one persistent CTA per SM: a deep stage ring and two accumulator buffers
+  p.nb = std::min(kGMaxStages, static_cast<int>((200 * 1024) / (p.a_stage + p.b_stage)));
+  p.acc_cols = 32;
+  while (p.acc_cols < static_cast<uint32_t>(p.NB)) p.acc_cols <<= 1;
+  p.tmem_cols = 2 * p.acc_cols;
   p.out = a.out;
   p.ldo = a.ldo;
   p.split_stride = a.split_stride;
@@ -352,7 +398,17 @@ cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, 
   const size_t smem = (size_t)p.nb * (p.a_stage + p.b_stage) + 1024;
   cudaError_t e = cudaFuncSetAttribute(gemm_cm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_mtiles * p.n_ntiles, p.splits);
+  const long long ntiles = (long long)p.n_mtiles * p.n_ntiles * p.splits;
+  if (ntiles > 0x7fffffffLL) {
+    *why = "GEMM has too many tiles";
+    return cudaErrorInvalidValue;
+  }
+  p.ntiles = static_cast<int>(ntiles);
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(std::min<long long>(ntiles, std::max(1, sms)));
   gemm_cm_kernel<<<grid, kGThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }

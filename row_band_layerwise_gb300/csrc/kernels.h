@@ -91,7 +91,6 @@ struct GemmArgs {
   const void* residual = nullptr;   // same layout and ldo as out
   int res_f32 = 0;
   void* out2 = nullptr;             // optional bf16 copy of out
-  int two_per_sm = 0;               // smaller pipeline so two CTAs share an SM
 };
 cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, const char** why);
 // out[i] = sum_s part[s * split_stride + i] for i < count (count, split_stride multiples of 4).
