@@ -326,15 +326,29 @@ class Walker {
     return y;
   }
 
+  // A 1x1 convolution that runs as the channel-major GEMM (bf16 path).
+  bool gemm_conv(const ConvGeom& g, bool rowscale, bool residual, bool out2) const {
+    return h_->dtype == kBF16 && g.ntaps == 1 && g.nphase == 1 && g.time_up_c == 0 && g.osx == 1 && g.osy == 1 &&
+           !rowscale && g.gn_part == nullptr && g.oT == g.T && g.oH == g.H && g.oW == g.W &&
+           (!g.out_chfirst || (!residual && !out2));
+  }
+
+  // Name of the kernel `launch` will run for a conv op (recorded in the op description).
+  const char* conv_kernel(const ConvGeom& g, bool residual, bool out2) const {
+    if (h_->dtype != kBF16) return "conv_simple_f32";
+    if (gemm_conv(g, false, residual, out2)) return "gemm_cm";
+    if (conv_halo_t_applicable(g)) return "conv_halo_t";
+    if (conv_halo_applicable(g)) return "conv_halo";
+    return "conv_tc";
+  }
+
   // Launch one GEMM/conv described by `g`.
   int launch(const ConvGeom& g, const void* in, const DevConv& w, const void* wptr, const float* bias,
              const void* residual, const float* rowscale, void* out, void* out2, const char* what) {
     count();
     if (g.gn_part != nullptr) ++stats_epoch_;   // the moments buffer is about to be rewritten
     int gn_chunks = 0;
-    if (h_->dtype == kBF16 && g.ntaps == 1 && g.nphase == 1 && g.time_up_c == 0 && g.osx == 1 && g.osy == 1 &&
-        rowscale == nullptr && g.gn_part == nullptr && g.oT == g.T && g.oH == g.H && g.oW == g.W &&
-        (!g.out_chfirst || (residual == nullptr && out2 == nullptr))) {
+    if (gemm_conv(g, rowscale != nullptr, residual != nullptr, out2 != nullptr)) {
       // 1x1 convolution = channel-major GEMM: out[pixel][co] = W[co][:] . in[pixel][:]
       const long long S = (long long)g.H * g.W;
       GemmArgs a;
@@ -472,14 +486,9 @@ class Walker {
       note_act(yc);
       *copy = yc;
     }
-    std::ostringstream d;
-    d << "kind=conv name=" << name << " conv="
-      << (kind == K3 ? "k3" : kind == K1 ? "k1" : kind == C3 ? "causal3" : kind == UP ? "up2x_k3" : "time")
-      << io(x, res, y) << " res=" << (res ? 1 : 0) << " final=" << (final_out ? 1 : 0) << " taps=" << w->ntaps
-      << " flops=" << conv_flops(x, y, *w, kind);
-    if (begin(d.str())) {
-      ConvGeom g;
-      std::memset(&g, 0, sizeof(g));
+    ConvGeom g;
+    std::memset(&g, 0, sizeof(g));
+    {
       g.B = x.B;
       g.T = x.T;
       g.H = x.H;
@@ -497,6 +506,13 @@ class Walker {
       g.out_f32 = y.dt == kF32 ? 1 : 0;
       g.res_f32 = (res && res->dt == kF32) ? 1 : 0;
       g.scale = 1.f;
+    }
+    std::ostringstream d;
+    d << "kind=conv name=" << name << " conv="
+      << (kind == K3 ? "k3" : kind == K1 ? "k1" : kind == C3 ? "causal3" : kind == UP ? "up2x_k3" : "time")
+      << io(x, res, y) << " res=" << (res ? 1 : 0) << " final=" << (final_out ? 1 : 0) << " taps=" << w->ntaps
+      << " flops=" << conv_flops(x, y, *w, kind) << " kernel=" << conv_kernel(g, res != nullptr, copy != nullptr);
+    if (begin(d.str())) {
       const char* in = static_cast<const char*>(ptr(x));
       void* out2 = copy ? ptr(yc) : nullptr;
       if (kind == TIME) {

@@ -37,10 +37,13 @@ constexpr int kGMaxStages = 4;
 constexpr int kGBK = 64;   // K chunk (128B swizzle)
 constexpr int kGCols = 16; // accumulator columns per epilogue step
 constexpr int kGEpiWarps = 8;
+constexpr int kGStageO = 128 * 32 * 4;   // one output staging buffer (32 columns of fp32)
 
 struct GemmParams {
   CUtensorMap tmA;   // (K, M) box (64, 128)
   CUtensorMap tmB;   // (K, N) box (64, NB)
+  CUtensorMap tmO;   // output (M, N, splits) box (128, 32, 1), when tma_out
+  int tma_out;       // 1: the epilogue stages 32-column chunks in shared memory and stores them with TMA
   int M, N, K, NB, n_mtiles, n_ntiles, nk, splits, nb, ntiles;
   uint32_t a_stage, b_stage, acc_cols, tmem_cols;
   void* out;
@@ -76,6 +79,20 @@ __device__ __forceinline__ GTile gemm_tile(const GemmParams& p, int t) {
 // Named barrier 1, shared by the waiter warp and the MMA warp (64 threads).
 __device__ __forceinline__ void stage_handoff() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
+// Named barrier `id` over the 128 threads of one epilogue half (four warps).
+__device__ __forceinline__ void half_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+// The same barrier, returning the AND of `v` over its 128 threads.
+__device__ __forceinline__ bool half_and(int id, bool v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred pv, pr;\n\tsetp.ne.s32 pv, %1, 0;\n\tbar.red.and.pred pr, %2, 128, pv;\n\t"
+      "selp.s32 %0, 1, 0, pr;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<int>(v)), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
 __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kGMaxStages], empty_bar[kGMaxStages];
@@ -88,6 +105,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = smem;
   uint8_t* smB = smem + p.nb * p.a_stage;
+  uint8_t* smO = smB + p.nb * p.b_stage;   // two 16 KB output staging buffers (tma_out)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.nb; ++i) {
@@ -106,6 +124,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB);
+    if (p.tma_out) tma_prefetch_desc(&p.tmO);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, p.tmem_cols);
@@ -197,76 +216,161 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
     // ---- epilogue warps 3..10: quarter q of the TMEM lanes, half `sub` of the column chunks
     const int q = warp & 3;
     const int sub = (warp - 3) >> 2;
-    int it = 0;
-    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
-      const GTile d = gemm_tile(p, t);
-      const int buf = it & 1;
-      const int m = d.m0 + q * 32 + lane;
-      const bool mvalid = m < p.M;
-      const float bm = (p.bias_m != nullptr && mvalid) ? p.bias_m[m] : 0.f;
-      const bool ok = mbar_wait(&acc_full[buf], static_cast<uint32_t>(it >> 1) & 1u, p.status, kErrTimeoutAccum,
-                                &abort_flag);
-      tc_fence_after();
-      if (!__all_sync(0xffffffffu, ok && !abort_flag)) break;
-      const uint32_t lane_addr = tmem + static_cast<uint32_t>(buf) * p.acc_cols + (static_cast<uint32_t>(q * 32) << 16);
-      char* outp = static_cast<char*>(p.out) + (p.out_f32 ? 4 : 2) * d.split * p.split_stride;
-      for (int c0 = sub * kGCols; c0 < p.NB && d.nks > 0; c0 += 2 * kGCols) {
-        const int nvalid = min(kGCols, p.N - (d.n0 + c0));
-        if (nvalid <= 0) break;   // uniform across the warp
-        uint32_t rr[kGCols];
-        tmem_ld_16x_32x32b(lane_addr + static_cast<uint32_t>(c0), rr);
-        tmem_ld_wait();
-        float v[kGCols];
+    if (p.tma_out) {
+      // 32-column chunks: the four warps of a half stage [32 n][128 m] in shared memory, then
+      // one thread stores the chunk with TMA (rows and columns outside the output are clipped)
+      const int bar_id = 2 + sub;
+      const bool leader = q == 0 && lane == 0;
+      const bool per_col = p.scale_n != nullptr || p.bias_n != nullptr;
+      uint8_t* stg = smO + sub * kGStageO;
+      int it = 0;
+      for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
+        const GTile d = gemm_tile(p, t);
+        const int buf = it & 1;
+        const int ml = q * 32 + lane;
+        const int m = d.m0 + ml;
+        const bool mvalid = m < p.M;
+        const float bm = (p.bias_m != nullptr && mvalid) ? p.bias_m[m] : 0.f;
+        const bool ok = mbar_wait(&acc_full[buf], static_cast<uint32_t>(it >> 1) & 1u, p.status, kErrTimeoutAccum,
+                                  &abort_flag);
+        tc_fence_after();
+        if (!half_and(bar_id, ok && !abort_flag)) break;   // the same decision in all four warps
+        const uint32_t lane_addr =
+            tmem + static_cast<uint32_t>(buf) * p.acc_cols + (static_cast<uint32_t>(q * 32) << 16);
+        for (int c0 = sub * 32; c0 < p.NB && d.nks > 0; c0 += 64) {
+          const int nvalid = min(32, p.N - (d.n0 + c0));
+          if (nvalid <= 0) break;   // uniform across the half
+          uint32_t rr[32];
+          tmem_ld_32x32b_x32(lane_addr + static_cast<uint32_t>(c0), rr);
+          tmem_ld_wait();
+          float v[32];
+          if (per_col) {
+            // column j's scale and bias: lane j loads them, a shuffle hands them to every lane
+            const float lsc = (lane < nvalid && p.scale_n != nullptr) ? __ldg(p.scale_n + d.n0 + c0 + lane) : 1.f;
+            const float lbn = (lane < nvalid && p.bias_n != nullptr) ? __ldg(p.bias_n + d.n0 + c0 + lane) : 0.f;
 #pragma unroll
-        for (int j = 0; j < kGCols; ++j) {
-          const int n = d.n0 + c0 + j;
-          float sc = p.scale;
-          float bn = 0.f;
-          if (j < nvalid) {
-            if (p.scale_n != nullptr) sc *= __ldg(p.scale_n + n);
-            if (p.bias_n != nullptr) bn = __ldg(p.bias_n + n);
+            for (int j = 0; j < 32; ++j)
+              v[j] = fmaf(__uint_as_float(rr[j]), p.scale * __shfl_sync(0xffffffffu, lsc, j),
+                          bm + __shfl_sync(0xffffffffu, lbn, j));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = fmaf(__uint_as_float(rr[j]), p.scale, bm);
           }
-          v[j] = __uint_as_float(rr[j]) * sc + bm + bn;
-        }
-        const long long e0 = static_cast<long long>(d.n0 + c0) * p.ldo + m;
-        if (mvalid) {
-          if (p.residual != nullptr) {
+          if (p.residual != nullptr && mvalid) {
+            // all 32 loads issued before the first use
+            const long long e0 = static_cast<long long>(d.n0 + c0) * p.ldo + m;
+            float rv[32];
             if (p.res_f32) {
               const float* rp = static_cast<const float*>(p.residual) + e0;
 #pragma unroll
-              for (int j = 0; j < kGCols; ++j)
-                if (j < nvalid) v[j] += rp[j * p.ldo];
+              for (int j = 0; j < 32; ++j) rv[j] = (j < nvalid) ? __ldg(rp + j * p.ldo) : 0.f;
             } else {
               const __nv_bfloat16* rp = static_cast<const __nv_bfloat16*>(p.residual) + e0;
 #pragma unroll
+              for (int j = 0; j < 32; ++j) rv[j] = (j < nvalid) ? __bfloat162float(rp[j * p.ldo]) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += rv[j];
+          }
+          // the staging buffer is free once the previous store from it has read it
+          if (leader) bulk_wait_group_read0();
+          half_sync(bar_id);
+          if (p.out_f32) {
+            float* sp = reinterpret_cast<float*>(stg) + ml;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sp[j * 128] = v[j];
+          } else {
+            __nv_bfloat16* sp = reinterpret_cast<__nv_bfloat16*>(stg) + ml;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sp[j * 128] = __float2bfloat16_rn(v[j]);
+          }
+          fence_proxy_async_smem();   // make the staged values visible to the TMA unit
+          half_sync(bar_id);
+          if (leader) {
+            tma_store_3d(&p.tmO, stg, d.m0, d.n0 + c0, d.split);
+            bulk_commit_group();
+          }
+          __syncwarp();
+        }
+        // hand the accumulator buffer back to the MMA issuer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      }
+      if (leader) bulk_wait_group0();
+      __syncwarp();
+    } else {
+      int it = 0;
+      for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
+        const GTile d = gemm_tile(p, t);
+        const int buf = it & 1;
+        const int m = d.m0 + q * 32 + lane;
+        const bool mvalid = m < p.M;
+        const float bm = (p.bias_m != nullptr && mvalid) ? p.bias_m[m] : 0.f;
+        const bool ok = mbar_wait(&acc_full[buf], static_cast<uint32_t>(it >> 1) & 1u, p.status, kErrTimeoutAccum,
+                                  &abort_flag);
+        tc_fence_after();
+        if (!__all_sync(0xffffffffu, ok && !abort_flag)) break;
+        const uint32_t lane_addr = tmem + static_cast<uint32_t>(buf) * p.acc_cols + (static_cast<uint32_t>(q * 32) << 16);
+        char* outp = static_cast<char*>(p.out) + (p.out_f32 ? 4 : 2) * d.split * p.split_stride;
+        for (int c0 = sub * kGCols; c0 < p.NB && d.nks > 0; c0 += 2 * kGCols) {
+          const int nvalid = min(kGCols, p.N - (d.n0 + c0));
+          if (nvalid <= 0) break;   // uniform across the warp
+          uint32_t rr[kGCols];
+          tmem_ld_16x_32x32b(lane_addr + static_cast<uint32_t>(c0), rr);
+          tmem_ld_wait();
+          float v[kGCols];
+  #pragma unroll
+          for (int j = 0; j < kGCols; ++j) {
+            const int n = d.n0 + c0 + j;
+            float sc = p.scale;
+            float bn = 0.f;
+            if (j < nvalid) {
+              if (p.scale_n != nullptr) sc *= __ldg(p.scale_n + n);
+              if (p.bias_n != nullptr) bn = __ldg(p.bias_n + n);
+            }
+            v[j] = __uint_as_float(rr[j]) * sc + bm + bn;
+          }
+          const long long e0 = static_cast<long long>(d.n0 + c0) * p.ldo + m;
+          if (mvalid) {
+            if (p.residual != nullptr) {
+              if (p.res_f32) {
+                const float* rp = static_cast<const float*>(p.residual) + e0;
+  #pragma unroll
+                for (int j = 0; j < kGCols; ++j)
+                  if (j < nvalid) v[j] += rp[j * p.ldo];
+              } else {
+                const __nv_bfloat16* rp = static_cast<const __nv_bfloat16*>(p.residual) + e0;
+  #pragma unroll
+                for (int j = 0; j < kGCols; ++j)
+                  if (j < nvalid) v[j] += __bfloat162float(rp[j * p.ldo]);
+              }
+            }
+            if (p.out_f32) {
+              float* op = reinterpret_cast<float*>(outp) + e0;
+  #pragma unroll
               for (int j = 0; j < kGCols; ++j)
-                if (j < nvalid) v[j] += __bfloat162float(rp[j * p.ldo]);
+                if (j < nvalid) op[j * p.ldo] = v[j];
+            } else {
+              __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(outp) + e0;
+  #pragma unroll
+              for (int j = 0; j < kGCols; ++j)
+                if (j < nvalid) op[j * p.ldo] = __float2bfloat16_rn(v[j]);
+            }
+            if (p.out2 != nullptr) {
+              __nv_bfloat16* op = p.out2 + e0;
+  #pragma unroll
+              for (int j = 0; j < kGCols; ++j)
+                if (j < nvalid) op[j * p.ldo] = __float2bfloat16_rn(v[j]);
             }
           }
-          if (p.out_f32) {
-            float* op = reinterpret_cast<float*>(outp) + e0;
-#pragma unroll
-            for (int j = 0; j < kGCols; ++j)
-              if (j < nvalid) op[j * p.ldo] = v[j];
-          } else {
-            __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(outp) + e0;
-#pragma unroll
-            for (int j = 0; j < kGCols; ++j)
-              if (j < nvalid) op[j * p.ldo] = __float2bfloat16_rn(v[j]);
-          }
-          if (p.out2 != nullptr) {
-            __nv_bfloat16* op = p.out2 + e0;
-#pragma unroll
-            for (int j = 0; j < kGCols; ++j)
-              if (j < nvalid) op[j * p.ldo] = __float2bfloat16_rn(v[j]);
-          }
+          __syncwarp();   // reconverge before the next warp-wide TMEM load
         }
-        __syncwarp();   // reconverge before the next warp-wide TMEM load
+        // hand the accumulator buffer back to the MMA issuer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
       }
-      // hand the accumulator buffer back to the MMA issuer
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
   }
 
@@ -355,8 +459,13 @@ cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, 
   p.splits = std::min(a.splits, p.nk);
   p.a_stage = 128 * kGBK * 2;
   p.b_stage = static_cast<uint32_t>(round_up_g(p.NB * kGBK * 2, 1024));
-  // one persistent CTA per SM: a deep stage ring and two accumulator buffers
-  p.nb = std::min(kGMaxStages, static_cast<int>((200 * 1024) / (p.a_stage + p.b_stage)));
+  // TMA-stored output: rows 16-byte aligned, no second output copy
+  const size_t oes = a.out_f32 ? 4 : 2;
+  p.tma_out = a.out2 == nullptr && (reinterpret_cast<uintptr_t>(a.out) % 16) == 0 && (a.ldo * oes) % 16 == 0 &&
+              (a.splits <= 1 || (a.split_stride * oes) % 16 == 0) && a.ldo >= a.M;
+  // one persistent CTA per SM: a deep stage ring, two accumulator buffers, two output staging buffers
+  const int stage_budget = 227 * 1024 - 1024 - 512 - (p.tma_out ? 2 * kGStageO : 0);
+  p.nb = std::min(kGMaxStages, static_cast<int>(stage_budget / (p.a_stage + p.b_stage)));
   p.acc_cols = 32;
   while (p.acc_cols < static_cast<uint32_t>(p.NB)) p.acc_cols <<= 1;
   p.tmem_cols = 2 * p.acc_cols;
@@ -395,7 +504,19 @@ cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, 
       return cudaErrorInvalidValue;
     }
   }
-  const size_t smem = (size_t)p.nb * (p.a_stage + p.b_stage) + 1024;
+  if (p.tma_out) {
+    const cuuint64_t dims[3] = {(cuuint64_t)a.M, (cuuint64_t)a.N, (cuuint64_t)p.splits};
+    const cuuint64_t strides[2] = {(cuuint64_t)(a.ldo * oes),
+                                   (cuuint64_t)(p.splits > 1 ? a.split_stride * oes : a.ldo * oes * a.N)};
+    const cuuint32_t box[3] = {128, 32, 1};
+    if (enc(&p.tmO, a.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.out, dims,
+            strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      *why = "GEMM output tensor map rejected";
+      return cudaErrorInvalidValue;
+    }
+  }
+  const size_t smem = (size_t)p.nb * (p.a_stage + p.b_stage) + (p.tma_out ? 2 * kGStageO : 0) + 1024;
   cudaError_t e = cudaFuncSetAttribute(gemm_cm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long ntiles = (long long)p.n_mtiles * p.n_ntiles * p.splits;

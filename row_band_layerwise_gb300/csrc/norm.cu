@@ -146,11 +146,15 @@ __global__ void __launch_bounds__(kGnThreads) gn_partials_kernel(const T* __rest
   }
 }
 
-// One CTA per (sample, group).  Thread t takes chunks t, t + 256, ... and applies
-// the weighted rule to them in order: N_t = sum n_i, mean_t = sum (n_i/N_t) mean_i,
-// var_t = sum (n_i/N_t)(var_i + (mean_i - mean_t)^2).  The 256 thread results are
-// then combined with the same rule, two parts at a time, along a fixed tree.
-constexpr int kFinThreads = 256;
+// One CTA per (sample, group), in one pass over the chunk moments.  Thread t folds
+// chunks t, t + 512, ... in order into (n, mean, M2) with the two-part form of the
+// weighted rule (for parts a, b: mean = w_a mean_a + w_b mean_b and
+// M2 = M2_a + M2_b + (mean_b - mean_a)^2 n_a n_b / n, which is the rule
+// var = sum w_i (var_i + (mean_i - mean)^2) for two parts times n); the 512
+// thread results are then combined with the same two-part rule along a fixed
+// tree.  Every step is fixed by the chunk geometry, so the result does not
+// depend on how the tensor was produced (band count, tile order).
+constexpr int kFinThreads = 512;
 
 __global__ void __launch_bounds__(kFinThreads) gn_finalize_kernel(const GnPartial* __restrict__ part, int B,
                                                                   int n_chunks, int C, int G,
@@ -158,51 +162,46 @@ __global__ void __launch_bounds__(kFinThreads) gn_finalize_kernel(const GnPartia
                                                                   const float* __restrict__ beta, float eps,
                                                                   float* __restrict__ scale,
                                                                   float* __restrict__ shift) {
-  __shared__ float sn[kFinThreads], sm[kFinThreads], sv[kFinThreads];
+  __shared__ float sn[kFinThreads], sm[kFinThreads], s2[kFinThreads];
   const int b = blockIdx.x / G, g = blockIdx.x % G;
   const int t = threadIdx.x;
   const GnPartial* pp = part + (long long)b * n_chunks * G + g;
-  float nl = 0.f;
-  for (int c = t; c < n_chunks; c += kFinThreads) nl += pp[(long long)c * G].n;
-  float ml = 0.f;
-  for (int c = t; c < n_chunks; c += kFinThreads) {
-    const GnPartial e = pp[(long long)c * G];
-    if (e.n > 0.f) ml += (e.n / nl) * e.mean;
+  float n = 0.f, mean = 0.f, m2 = 0.f;
+  int c = t;
+  // four loads in flight per step, folded in chunk order
+  for (; c + 3 * kFinThreads < n_chunks; c += 4 * kFinThreads) {
+    GnPartial e[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) e[i] = pp[(long long)(c + i * kFinThreads) * G];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) merge_into(n, mean, m2, e[i].n, e[i].mean, e[i].m2);
   }
-  float vl = 0.f;
-  for (int c = t; c < n_chunks; c += kFinThreads) {
+  for (; c < n_chunks; c += kFinThreads) {
     const GnPartial e = pp[(long long)c * G];
-    if (e.n > 0.f) {
-      const float d = e.mean - ml;
-      vl += (e.n / nl) * (e.m2 / e.n + d * d);
-    }
+    merge_into(n, mean, m2, e.n, e.mean, e.m2);
   }
-  sn[t] = nl;
-  sm[t] = ml;
-  sv[t] = vl;
+  sn[t] = n;
+  sm[t] = mean;
+  s2[t] = m2;
   __syncthreads();
   for (int half = kFinThreads / 2; half > 0; half >>= 1) {
     if (t < half) {
-      const float na = sn[t], nb = sn[t + half];
-      if (nb > 0.f) {
-        const float nt = na + nb;
-        const float wa = na / nt, wb = nb / nt;
-        const float m = wa * sm[t] + wb * sm[t + half];
-        const float da = sm[t] - m, db = sm[t + half] - m;
-        sv[t] = wa * (sv[t] + da * da) + wb * (sv[t + half] + db * db);
-        sm[t] = m;
-        sn[t] = nt;
-      }
+      float na = sn[t], ma = sm[t], m2a = s2[t];
+      merge_into(na, ma, m2a, sn[t + half], sm[t + half], s2[t + half]);
+      sn[t] = na;
+      sm[t] = ma;
+      s2[t] = m2a;
     }
     __syncthreads();
   }
-  const float rstd = rsqrtf(sv[0] + eps);
-  const float mean = sm[0];
+  const float var = sn[0] > 0.f ? s2[0] / sn[0] : 0.f;
+  const float rstd = rsqrtf(var + eps);
+  const float gmean = sm[0];
   const int cg = C / G;
-  for (int c = g * cg + t; c < (g + 1) * cg; c += kFinThreads) {
-    const float a = gamma[c] * rstd;
-    scale[(long long)b * C + c] = a;
-    shift[(long long)b * C + c] = beta[c] - mean * a;
+  for (int ch = g * cg + t; ch < (g + 1) * cg; ch += kFinThreads) {
+    const float a = gamma[ch] * rstd;
+    scale[(long long)b * C + ch] = a;
+    shift[(long long)b * C + ch] = beta[ch] - gmean * a;
   }
 }
 
