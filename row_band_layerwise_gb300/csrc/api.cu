@@ -743,7 +743,7 @@ class Walker {
             const size_t qoff = ((size_t)f * Ntok + (size_t)r0 * x.W) * C;
             void* o_band = static_cast<char*>(ptr(hn)) + qoff * oes;   // O overwrites the band's normalised rows
             if (tc) {
-              // S[q, key] = (K Q^T)[key, q] / sqrt(C), keys on the accumulator lanes
+              // S[q, key] = (K Q^T)[key, q] / sqrt(C), keys on the accumulator lanes, stored fp16
               GemmArgs sa;
               sa.A = static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes;
               sa.lda = C;
@@ -754,11 +754,12 @@ class Walker {
               sa.K = C;
               sa.out = h_->attn_s;
               sa.ldo = Ntok;
-              sa.out_f32 = 1;
+              sa.out_f32 = 0;
+              sa.out_f16 = 1;
               sa.scale = scale;
               gemm(sa, "attention scores");
               count();
-              check(launch_softmax_rows(odt_, h_->attn_s, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
+              check(launch_softmax_rows(odt_, h_->attn_s, 1, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
               // O[q, c] = inv_l[q] * (V^T P^T)[c, q], channels on the lanes, keys split
               const int splits = pv_splits(Ntok);
               GemmArgs pa;
@@ -808,7 +809,7 @@ class Walker {
                      static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes, nullptr, nullptr, nullptr,
                      h_->attn_s, nullptr, "attention scores");
               count();
-              check(launch_softmax_rows(odt_, h_->attn_s, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
+              check(launch_softmax_rows(odt_, h_->attn_s, 0, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
               ConvGeom go = gs;
               go.Cin = (int)Ntok;
               go.Cout = C;

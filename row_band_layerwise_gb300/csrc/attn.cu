@@ -5,6 +5,7 @@
 // into the channels-last activation layout.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.h"
 
@@ -52,18 +53,30 @@ __device__ __forceinline__ float store_p<__nv_bfloat16>(__nv_bfloat16* p, float 
   return __bfloat162float(h);
 }
 
-template <typename P>
-__global__ void __launch_bounds__(kSmThreads) softmax_rows_kernel(const float* __restrict__ S, P* __restrict__ Pm,
+__device__ __forceinline__ float load_s(const float* p) { return *p; }
+__device__ __forceinline__ float load_s(const __half* p) { return __half2float(*p); }
+
+// Four consecutive scores (16-byte aligned for fp32, 8-byte for fp16), streamed once.
+__device__ __forceinline__ float4 load_s4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 load_s4(const __half* p) {
+  const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <typename SIn, typename P>
+__global__ void __launch_bounds__(kSmThreads) softmax_rows_kernel(const SIn* __restrict__ S, P* __restrict__ Pm,
                                                                   float* __restrict__ inv_l, int nk) {
   __shared__ float red[32];
   const long long row = blockIdx.x;
-  const float* s = S + row * nk;
+  const SIn* s = S + row * nk;
   P* p = Pm + row * nk;
   float m = -INFINITY;
-  for (int k = threadIdx.x; k < nk; k += blockDim.x) m = fmaxf(m, s[k]);
+  for (int k = threadIdx.x; k < nk; k += blockDim.x) m = fmaxf(m, load_s(s + k));
   m = block_reduce_max(m, red);
   float l = 0.f;
-  for (int k = threadIdx.x; k < nk; k += blockDim.x) l += store_p<P>(p + k, __expf(s[k] - m));
+  for (int k = threadIdx.x; k < nk; k += blockDim.x) l += store_p<P>(p + k, __expf(load_s(s + k) - m));
   l = block_reduce_sum(l, red);
   if (threadIdx.x == 0) inv_l[row] = 1.f / l;
 }
@@ -91,12 +104,12 @@ __device__ __forceinline__ float store_p4<__nv_bfloat16>(__nv_bfloat16* p, float
   return (a.x + a.y) + (b.x + b.y);
 }
 
-template <typename P, int NV>
-__global__ void __launch_bounds__(kSmThreads) softmax_rows_reg_kernel(const float* __restrict__ S, P* __restrict__ Pm,
+template <typename SIn, typename P, int NV>
+__global__ void __launch_bounds__(kSmThreads) softmax_rows_reg_kernel(const SIn* __restrict__ S, P* __restrict__ Pm,
                                                                       float* __restrict__ inv_l, int nk) {
   __shared__ float red[32];
   const long long row = blockIdx.x;
-  const float4* s4 = reinterpret_cast<const float4*>(S + row * nk);
+  const SIn* srow = S + row * nk;
   P* p = Pm + row * nk;
   const int n4 = nk >> 2;
   float4 v[NV];
@@ -105,7 +118,7 @@ __global__ void __launch_bounds__(kSmThreads) softmax_rows_reg_kernel(const floa
   for (int i = 0; i < NV; ++i) {
     const int idx = threadIdx.x + i * kSmThreads;
     if (idx < n4) {
-      v[i] = __ldcs(s4 + idx);
+      v[i] = load_s4(srow + 4 * idx);
       m = fmaxf(m, fmaxf(fmaxf(v[i].x, v[i].y), fmaxf(v[i].z, v[i].w)));
     }
   }
@@ -140,22 +153,19 @@ __global__ void to_channels_last_kernel(const T* __restrict__ x, T* __restrict__
   }
 }
 
-}  // namespace
-
-cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv_l, int rows, int nk,
-                                cudaStream_t stream) {
-  if (rows <= 0) return cudaSuccess;
+template <typename SIn>
+cudaError_t softmax_rows_t(int p_dtype, const SIn* S, void* P, float* inv_l, int rows, int nk, cudaStream_t stream) {
+  const bool bf = p_dtype == kBF16;
   if (nk % 4 == 0 && nk <= 16 * 4 * kSmThreads) {
     const int nv = (nk + 4 * kSmThreads - 1) / (4 * kSmThreads);
-    const bool bf = p_dtype == kBF16;
-#define VD_SOFTMAX_REG(NV)                                                                                       \
-  if (nv <= NV) {                                                                                                \
-    if (bf)                                                                                                      \
-      softmax_rows_reg_kernel<__nv_bfloat16, NV>                                                                 \
-          <<<rows, kSmThreads, 0, stream>>>(S, static_cast<__nv_bfloat16*>(P), inv_l, nk);                       \
-    else                                                                                                         \
-      softmax_rows_reg_kernel<float, NV><<<rows, kSmThreads, 0, stream>>>(S, static_cast<float*>(P), inv_l, nk); \
-    return cudaGetLastError();                                                                                   \
+#define VD_SOFTMAX_REG(NV)                                                                                         \
+  if (nv <= NV) {                                                                                                  \
+    if (bf)                                                                                                        \
+      softmax_rows_reg_kernel<SIn, __nv_bfloat16, NV>                                                              \
+          <<<rows, kSmThreads, 0, stream>>>(S, static_cast<__nv_bfloat16*>(P), inv_l, nk);                         \
+    else                                                                                                           \
+      softmax_rows_reg_kernel<SIn, float, NV><<<rows, kSmThreads, 0, stream>>>(S, static_cast<float*>(P), inv_l, nk); \
+    return cudaGetLastError();                                                                                     \
   }
     VD_SOFTMAX_REG(2)
     VD_SOFTMAX_REG(4)
@@ -163,11 +173,21 @@ cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv
     VD_SOFTMAX_REG(16)
 #undef VD_SOFTMAX_REG
   }
-  if (p_dtype == kBF16)
-    softmax_rows_kernel<__nv_bfloat16><<<rows, kSmThreads, 0, stream>>>(S, static_cast<__nv_bfloat16*>(P), inv_l, nk);
+  if (bf)
+    softmax_rows_kernel<SIn, __nv_bfloat16><<<rows, kSmThreads, 0, stream>>>(S, static_cast<__nv_bfloat16*>(P), inv_l,
+                                                                             nk);
   else
-    softmax_rows_kernel<float><<<rows, kSmThreads, 0, stream>>>(S, static_cast<float*>(P), inv_l, nk);
+    softmax_rows_kernel<SIn, float><<<rows, kSmThreads, 0, stream>>>(S, static_cast<float*>(P), inv_l, nk);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_softmax_rows(int p_dtype, const void* S, int s_f16, void* P, float* inv_l, int rows, int nk,
+                                cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  if (s_f16) return softmax_rows_t(p_dtype, static_cast<const __half*>(S), P, inv_l, rows, nk, stream);
+  return softmax_rows_t(p_dtype, static_cast<const float*>(S), P, inv_l, rows, nk, stream);
 }
 
 cudaError_t launch_to_channels_last(int dtype, const void* x, void* y, int B, int C, long long spatial,

@@ -20,6 +20,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <cstring>
@@ -48,7 +49,7 @@ struct GemmParams {
   uint32_t a_stage, b_stage, acc_cols, tmem_cols;
   void* out;
   long long ldo, split_stride;
-  int out_f32, res_f32;
+  int out_f32, out_f16, res_f32;   // output fp32, fp16, else bf16
   const float* bias_m;
   const float* bias_n;
   const float* scale_n;
@@ -279,6 +280,10 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
             float* sp = reinterpret_cast<float*>(stg) + ml;
 #pragma unroll
             for (int j = 0; j < 32; ++j) sp[j * 128] = v[j];
+          } else if (p.out_f16) {
+            __half* sp = reinterpret_cast<__half*>(stg) + ml;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sp[j * 128] = __float2half_rn(v[j]);
           } else {
             __nv_bfloat16* sp = reinterpret_cast<__nv_bfloat16*>(stg) + ml;
 #pragma unroll
@@ -320,7 +325,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
           tmem_ld_16x_32x32b(lane_addr + static_cast<uint32_t>(c0), rr);
           tmem_ld_wait();
           float v[kGCols];
-  #pragma unroll
+#pragma unroll
           for (int j = 0; j < kGCols; ++j) {
             const int n = d.n0 + c0 + j;
             float sc = p.scale;
@@ -336,30 +341,35 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
             if (p.residual != nullptr) {
               if (p.res_f32) {
                 const float* rp = static_cast<const float*>(p.residual) + e0;
-  #pragma unroll
+#pragma unroll
                 for (int j = 0; j < kGCols; ++j)
                   if (j < nvalid) v[j] += rp[j * p.ldo];
               } else {
                 const __nv_bfloat16* rp = static_cast<const __nv_bfloat16*>(p.residual) + e0;
-  #pragma unroll
+#pragma unroll
                 for (int j = 0; j < kGCols; ++j)
                   if (j < nvalid) v[j] += __bfloat162float(rp[j * p.ldo]);
               }
             }
             if (p.out_f32) {
               float* op = reinterpret_cast<float*>(outp) + e0;
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < kGCols; ++j)
                 if (j < nvalid) op[j * p.ldo] = v[j];
+            } else if (p.out_f16) {
+              __half* op = reinterpret_cast<__half*>(outp) + e0;
+#pragma unroll
+              for (int j = 0; j < kGCols; ++j)
+                if (j < nvalid) op[j * p.ldo] = __float2half_rn(v[j]);
             } else {
               __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(outp) + e0;
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < kGCols; ++j)
                 if (j < nvalid) op[j * p.ldo] = __float2bfloat16_rn(v[j]);
             }
             if (p.out2 != nullptr) {
               __nv_bfloat16* op = p.out2 + e0;
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < kGCols; ++j)
                 if (j < nvalid) op[j * p.ldo] = __float2bfloat16_rn(v[j]);
             }
@@ -473,6 +483,7 @@ cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, 
   p.ldo = a.ldo;
   p.split_stride = a.split_stride;
   p.out_f32 = a.out_f32;
+  p.out_f16 = a.out_f32 ? 0 : a.out_f16;
   p.res_f32 = a.res_f32;
   p.bias_m = a.bias_m;
   p.bias_n = a.bias_n;
@@ -509,7 +520,9 @@ cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, 
     const cuuint64_t strides[2] = {(cuuint64_t)(a.ldo * oes),
                                    (cuuint64_t)(p.splits > 1 ? a.split_stride * oes : a.ldo * oes * a.N)};
     const cuuint32_t box[3] = {128, 32, 1};
-    if (enc(&p.tmO, a.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.out, dims,
+    const CUtensorMapDataType odt = a.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : (a.out_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    if (enc(&p.tmO, odt, 3, a.out, dims,
             strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
       *why = "GEMM output tensor map rejected";

@@ -82,6 +82,7 @@ struct GemmArgs {
   void* out = nullptr;
   long long ldo = 0;
   int out_f32 = 1;
+  int out_f16 = 0;                  // with out_f32 == 0: fp16 output instead of bf16
   int splits = 1;
   long long split_stride = 0;
   const float* bias_m = nullptr;
@@ -99,8 +100,9 @@ cudaError_t launch_splitk_reduce(const float* part, int splits, long long split_
 
 // ---------------------------------------------------------------- attention
 // Row softmax numerators: P[r, k] = exp(S[r, k] - max_k S[r, :]) stored as
-// `p_dtype`, inv_l[r] = 1 / sum_k P[r, k] (sum of the stored values).
-cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv_l, int rows, int nk,
+// `p_dtype`, inv_l[r] = 1 / sum_k P[r, k] (sum of the stored values).  S is fp32,
+// or fp16 when `s_f16`.
+cudaError_t launch_softmax_rows(int p_dtype, const void* S, int s_f16, void* P, float* inv_l, int rows, int nk,
                                 cudaStream_t stream);
 
 // ---------------------------------------------------------------- layout
