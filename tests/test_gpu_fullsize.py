@@ -1,0 +1,84 @@
+"""GPU parity at the full workload sizes, in the launch configuration the bench times.
+
+The float64 oracle needs minutes per full-size decode, so its outputs are
+precomputed by ``tests/golden/make_decode_samples.py`` (which calls only the
+seeded input generators and the oracle) and stored as sampled elements: a few
+thousand uniform positions plus positions on the output rows on each side of
+every band boundary.  Here the CUDA decode of the same workload (same seeds,
+same band count as the bench) must match those samples within the bf16 bars
+(max-abs <= 3e-2, rel-L2 <= 1e-2 over the samples), and the decode must be bit
+for bit the same for one band and for the workload's band count: a property
+that holds at any size, checked on the whole output.
+"""
+import glob
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_helpers import assert_bf16_parity, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+# workloads whose fixtures must be present (their oracle decodes take minutes)
+REQUIRED = ("kl_zimage_512", "kl_zimage_1024")
+
+
+def load_samples(name):
+    path = os.path.join(GOLDEN, f"decode_samples_{name}.txt")
+    shape, idx, val = None, [], []
+    with open(path) as fh:
+        for line in fh:
+            if line.startswith("#"):
+                continue
+            f = line.split()
+            if f[0] == "shape":
+                shape = tuple(int(v) for v in f[1:])
+            elif f[0] in ("l2norm", "samples"):
+                continue
+            else:
+                idx.append(int(f[0]))
+                val.append(float(f[1]))
+    return shape, np.array(idx, np.int64), np.array(val, np.float64)
+
+
+def fixture_names():
+    names = sorted(os.path.basename(p)[len("decode_samples_"):-4]
+                   for p in glob.glob(os.path.join(GOLDEN, "decode_samples_*.txt")))
+    return names
+
+
+def test_required_fixtures_present():
+    names = fixture_names()
+    for r in REQUIRED:
+        assert r in names, f"missing tests/golden/decode_samples_{r}.txt"
+
+
+@pytest.mark.parametrize("name", fixture_names())
+def test_full_size_decode_matches_oracle_samples(name):
+    torch, rbl = require_gpu()
+    w = synth.WORKLOADS[name]
+    shape, idx, ref = load_samples(name)
+    W = synth.make_weights(w.arch, w.dtype)
+    z = synth.make_latent(w.latent_shape, w.dtype)
+    shp = w.latent_shape
+    max_latent = (shp[0], 1, shp[2], shp[3]) if len(shp) == 4 else (shp[0], shp[2], shp[3], shp[4])
+    dec = rbl.Decoder(w.arch, W, w.dtype, max_latent)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    zd = torch.from_numpy(z).to("cuda").to(tdt).contiguous()
+    out = dec.decode(zd, w.n_bands)
+    torch.cuda.synchronize()
+    dec.sync()
+    assert tuple(out.shape) == shape
+    got_all = out.float().cpu().numpy()
+    got = got_all.reshape(-1)[idx].astype(np.float64)
+    assert np.isfinite(got_all).all()
+    # band-count invariance over the whole output
+    one = dec.decode(zd, 1)
+    torch.cuda.synchronize()
+    dec.sync()
+    assert bool((one == out).all()), "1-band decode differs from the banded decode"
+    dec.close()
+    assert_bf16_parity(got, ref)
