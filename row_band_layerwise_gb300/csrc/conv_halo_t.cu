@@ -12,10 +12,13 @@
 // output channel, so each epilogue store instruction writes 32 consecutive
 // channels of one pixel: fully coalesced, with residual reads batched 32 deep.
 //
-// Roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
-// warps 2..9 epilogue (two warps per TMEM lane quarter, splitting the rows).  A weight stage holds the three taps of one kernel row,
-// so each stage wait is followed by ~1500 cycles of MMA work.  Waits are
-// bounded (ptx.cuh).
+// Roles (352 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warp 2 waiter,
+// warps 3..10 epilogue (two warps per TMEM lane quarter).  The waiter polls the stage and
+// accumulator barriers in the MMA warp's order and releases the MMA warp through a named barrier,
+// so the MMA-issuing thread never polls shared memory while the tensor pipe saturates it (a poll
+// then costs about a thousand cycles, more than a one-row weight stage's 768 cycles of MMAs).  A
+// weight stage holds the three taps of one kernel row.  Every wait is bounded (ptx.cuh); the waiter
+// and the MMA warp pass the named barrier the same number of times on every path.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -33,7 +36,7 @@ namespace vd {
 
 namespace {
 
-constexpr int kThreadsT = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue (two per TMEM lane quarter)
+constexpr int kThreadsT = 352;   // warp 0 TMA, warp 1 MMA, warp 2 waiter, warps 3..10 epilogue (two per TMEM lane quarter)
 constexpr int kEpiWarpsT = 8;
 constexpr int kMaxWStages = 4;
 constexpr int kPipeBytesT = 212 * 1024;
@@ -104,6 +107,9 @@ __device__ __forceinline__ TileT decode_tile(const HaloTParams& p, int t) {
   d.m0 = d.mtile * 128;
   return d;
 }
+
+// Named barrier 1, shared by the waiter warp and the MMA warp (64 threads).
+__device__ __forceinline__ void stage_handoff() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
 template <int BK>
 __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_constant__ HaloTParams p) {
@@ -201,71 +207,94 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
       }
     }
     __syncwarp();
+  } else if (warp == 2) {
+    // ---- waiter: polls the barriers the MMA warp consumes, in the MMA warp's order, and hands
+    // each completed one over through the named barrier (one hand-off per wait, also after an abort)
+    int acg = 0, kbg = 0, it = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
+      const int buf = it % p.nbuf;
+      if (it >= p.nbuf) {
+        if (lane == 0 && !abort_flag)
+          mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it / p.nbuf) & 1u) ^ 1u, p.status, kErrTimeoutEmpty,
+                    &abort_flag);
+        __syncwarp();
+        stage_handoff();
+      }
+      for (int ac = 0; ac < nac; ++ac, ++acg) {
+        if (lane == 0 && !abort_flag)
+          mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag);
+        __syncwarp();
+        stage_handoff();
+        for (int gi = 0; gi < ngrp; ++gi, ++kbg) {
+          if (lane == 0 && !abort_flag)
+            mbar_wait(&w_full[kbg % p.nw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
+                      &abort_flag);
+          __syncwarp();
+          stage_handoff();
+        }
+      }
+    }
   } else if (warp == 1) {
-    // ---- MMA issuer: tile i accumulates into TMEM buffer i % nbuf
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, p.npx);
-      const uint32_t x_base0 = smem_u32(smX), w_base0 = smem_u32(smW);
-      int acg = 0, kbg = 0, it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x, ++it) {
-        const int phase = decode_tile(p, t).phase;
-        const int buf = it % p.nbuf;
-        if (it >= p.nbuf && !mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it / p.nbuf) & 1u) ^ 1u, p.status,
-                                       kErrTimeoutEmpty, &abort_flag))
-          break;
+    // ---- MMA issuer: tile i accumulates into TMEM buffer i % nbuf.  It never polls shared memory:
+    // the waiter warp releases it through the named barrier once a stage (or buffer) is ready.
+    const uint32_t idesc = idesc_bf16_f32(128, p.npx);
+    const uint32_t x_base0 = smem_u32(smX), w_base0 = smem_u32(smW);
+    int acg = 0, kbg = 0, it = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
+      const int phase = decode_tile(p, t).phase;
+      const int buf = it % p.nbuf;
+      if (it >= p.nbuf) stage_handoff();
+      tc_fence_after();
+      const uint32_t dbase = tmem + static_cast<uint32_t>(buf * p.acc_cols);
+      for (int ac = 0; ac < nac; ++ac, ++acg) {
+        const int dti = ac / p.n_kchunks;
+        const int sx = acg & 1;
+        stage_handoff();
         tc_fence_after();
-        const uint32_t dbase = tmem + static_cast<uint32_t>(buf * p.acc_cols);
-        for (int ac = 0; ac < nac && ok; ++ac) {
-          const int dti = ac / p.n_kchunks;
-          const int sx = acg & 1;
-          if (!mbar_wait(&x_full[sx], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag)) {
-            ok = false;
-            break;
-          }
+        const uint32_t xb = x_base0 + sx * p.x_stage_bytes;
+        for (int gi = 0; gi < ngrp; ++gi, ++kbg) {
+          const int sw = kbg % p.nw;
+          stage_handoff();
           tc_fence_after();
-          const uint32_t xb = x_base0 + sx * p.x_stage_bytes;
-          for (int gi = 0; gi < ngrp; ++gi, ++kbg) {
-            const int sw = kbg % p.nw;
-            if (!mbar_wait(&w_full[sw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
-                           &abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t wb = w_base0 + sw * p.w_stage_bytes;
-            for (int tp = 0; tp < 3; ++tp) {
-              const ConvTap tap = g.taps[phase][dti * nsp + gi * 3 + tp];
-              const uint32_t wa = wb + tp * p.w_tap_bytes;
-              for (int r = 0; r < p.R; ++r) {
-                const uint32_t xa =
-                    xb + (r + tap.dy + 1) * p.row_bytes + static_cast<uint32_t>((tap.dx + 1) * BK * 2);
+          if (lane == 0) {
+            if (!abort_flag) {
+              const uint32_t wb = w_base0 + sw * p.w_stage_bytes;
+              for (int tp = 0; tp < 3; ++tp) {
+                const ConvTap tap = g.taps[phase][dti * nsp + gi * 3 + tp];
+                const uint32_t wa = wb + tp * p.w_tap_bytes;
+                for (int r = 0; r < p.R; ++r) {
+                  const uint32_t xa =
+                      xb + (r + tap.dy + 1) * p.row_bytes + static_cast<uint32_t>((tap.dx + 1) * BK * 2);
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                  const uint64_t da = smem_desc_kmajor(wa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
-                  const uint64_t db = smem_desc_kmajor(xa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
-                  tc_mma_bf16(dbase + static_cast<uint32_t>(r * p.npx), da, db, idesc,
-                              (ac | gi | tp | k) != 0 ? 1u : 0u);
+                  for (int k = 0; k < BK / 16; ++k) {
+                    const uint64_t da = smem_desc_kmajor(wa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
+                    const uint64_t db = smem_desc_kmajor(xa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
+                    tc_mma_bf16(dbase + static_cast<uint32_t>(r * p.npx), da, db, idesc,
+                                (ac | gi | tp | k) != 0 ? 1u : 0u);
+                  }
                 }
               }
             }
             tc_commit(&w_empty[sw]);
           }
-          if (!ok) break;
-          tc_commit(&x_empty[sx]);
-          ++acg;
+          __syncwarp();
         }
-        if (ok) tc_commit(&acc_full[buf]);
+        if (lane == 0) tc_commit(&x_empty[sx]);
+        __syncwarp();
       }
-      // every MMA issued has completed before the CTA releases TMEM (also after a timeout)
+      if (lane == 0) tc_commit(&acc_full[buf]);
+      __syncwarp();
+    }
+    // every MMA issued has completed before the CTA releases TMEM (also after a timeout)
+    if (lane == 0) {
       tc_commit(&mma_done);
       mbar_drain(&mma_done, 0);
     }
     __syncwarp();
   } else {
-    // ---- epilogue (warps 2..9): TMEM lane = output channel; columns = pixels of a tile row
+    // ---- epilogue (warps 3..10): TMEM lane = output channel; columns = pixels of a tile row
     const int q = warp & 3;
-    const int sub = (warp - 2) >> 2;   // csplit 1: rows r with r % 2 == sub; csplit 2: half `sub` of the row
+    const int sub = (warp - 3) >> 2;   // csplit 1: rows r with r % 2 == sub; csplit 2: half `sub` of the row
     const int hc = p.csplit == 2 ? (((p.npx + 1) / 2 + 31) & ~31) : p.npx;
     const int r_begin = p.csplit == 2 ? 0 : sub, r_step = p.csplit == 2 ? 1 : 2;
     const int c_begin = p.csplit == 2 ? sub * hc : 0, c_end = p.csplit == 2 ? min(p.npx, (sub + 1) * hc) : p.npx;
@@ -286,7 +315,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
             ((static_cast<long long>(d.bb) * g.oT + d.tt) * g.oH + yo) * static_cast<long long>(g.oW);
         return (row_pix + static_cast<long long>(d.x0) * g.osx + (g.nphase > 1 ? px : 0)) * g.oC;
       };
-      if (p.residual != nullptr && warp == 2 && lane == 0) {
+      if (p.residual != nullptr && warp == 3 && lane == 0) {
         // pull this tile's residual rows into L2 while its MMAs run (whole pixels, all channels: contiguous)
         const int nv = min(p.npx, g.W - d.x0);
         for (int r = 0; r < p.R && d.y0 + r < g.H; ++r) {
