@@ -236,41 +236,51 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
     }
   } else if (warp == 1) {
     // ---- MMA issuer: tile i accumulates into TMEM buffer i % nbuf.  It never polls shared memory:
-    // the waiter warp releases it through the named barrier once a stage (or buffer) is ready.
+    // the waiter warp releases it through the named barrier once a stage (or buffer) is ready.  The
+    // issue loop only adds precomputed offsets to two base descriptors (the start-address field is
+    // in 16-byte units), so one thread issues faster than the tensor pipe executes.
     const uint32_t idesc = idesc_bf16_f32(128, p.npx);
-    const uint32_t x_base0 = smem_u32(smX), w_base0 = smem_u32(smW);
-    int acg = 0, kbg = 0, it = 0;
+    const uint64_t dA0 = smem_desc_kmajor(smem_u32(smW), SwzT<BK>::kSbo, SwzT<BK>::kMode);
+    const uint64_t dB0 = smem_desc_kmajor(smem_u32(smX), SwzT<BK>::kSbo, SwzT<BK>::kMode);
+    const uint32_t w_stage16 = p.w_stage_bytes >> 4, w_tap16 = p.w_tap_bytes >> 4;
+    const uint32_t x_stage16 = p.x_stage_bytes >> 4, row16 = p.row_bytes >> 4;
+    int it = 0, sw = 0;
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
       const int phase = decode_tile(p, t).phase;
+      // per spatial tap (the same for every causal frame): offset of its shifted rows
+      uint32_t xoff[9];
+#pragma unroll
+      for (int i = 0; i < 9; ++i) {
+        const ConvTap tap = g.taps[phase][i];
+        xoff[i] = static_cast<uint32_t>(((tap.dy + 1) * static_cast<int>(p.row_bytes) + (tap.dx + 1) * BK * 2) >> 4);
+      }
       const int buf = it % p.nbuf;
       if (it >= p.nbuf) stage_handoff();
       tc_fence_after();
-      const uint32_t dbase = tmem + static_cast<uint32_t>(buf * p.acc_cols);
-      for (int ac = 0; ac < nac; ++ac, ++acg) {
-        const int dti = ac / p.n_kchunks;
-        const int sx = acg & 1;
+      const uint32_t dcol = tmem + static_cast<uint32_t>(buf * p.acc_cols);
+      for (int ac = 0; ac < nac; ++ac) {
+        const int sx = (it * nac + ac) & 1;
         stage_handoff();
         tc_fence_after();
-        const uint32_t xb = x_base0 + sx * p.x_stage_bytes;
-        for (int gi = 0; gi < ngrp; ++gi, ++kbg) {
-          const int sw = kbg % p.nw;
+        const uint64_t dBs = dB0 + static_cast<uint64_t>(sx * x_stage16);
+#pragma unroll
+        for (int gi = 0; gi < 3; ++gi) {
           stage_handoff();
           tc_fence_after();
           if (lane == 0) {
             if (!abort_flag) {
-              const uint32_t wb = w_base0 + sw * p.w_stage_bytes;
-              for (int tp = 0; tp < 3; ++tp) {
-                const ConvTap tap = g.taps[phase][dti * nsp + gi * 3 + tp];
-                const uint32_t wa = wb + tp * p.w_tap_bytes;
-                for (int r = 0; r < p.R; ++r) {
-                  const uint32_t xa =
-                      xb + (r + tap.dy + 1) * p.row_bytes + static_cast<uint32_t>((tap.dx + 1) * BK * 2);
+              const uint64_t dAs = dA0 + static_cast<uint64_t>(sw * w_stage16);
 #pragma unroll
-                  for (int k = 0; k < BK / 16; ++k) {
-                    const uint64_t da = smem_desc_kmajor(wa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
-                    const uint64_t db = smem_desc_kmajor(xa + k * 32, SwzT<BK>::kSbo, SwzT<BK>::kMode);
-                    tc_mma_bf16(dbase + static_cast<uint32_t>(r * p.npx), da, db, idesc,
-                                (ac | gi | tp | k) != 0 ? 1u : 0u);
+              for (int tp = 0; tp < 3; ++tp) {
+                const uint64_t dAt = dAs + tp * w_tap16;
+                const uint64_t dBt = dBs + xoff[gi * 3 + tp];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                  if (r < p.R) {
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                      tc_mma_bf16(dcol + static_cast<uint32_t>(r * p.npx), dAt + 2 * k, dBt + r * row16 + 2 * k, idesc,
+                                  (ac | gi | tp | k) != 0 ? 1u : 0u);
                   }
                 }
               }
@@ -278,6 +288,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
             tc_commit(&w_empty[sw]);
           }
           __syncwarp();
+          sw = (sw + 1 == p.nw) ? 0 : sw + 1;
         }
         if (lane == 0) tc_commit(&x_empty[sx]);
         __syncwarp();

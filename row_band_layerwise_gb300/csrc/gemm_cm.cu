@@ -176,8 +176,11 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
   } else if (warp == 1) {
     // ---- MMA issuer: tile i accumulates into TMEM buffer i & 1; same stage sequence as the waiter
     const uint32_t idesc = idesc_bf16_f32(128, p.NB);
-    const uint32_t a0 = smem_u32(smA), b0 = smem_u32(smB);
-    int g = 0, it = 0;
+    // base descriptors; a stage / K step only adds to the start-address field (16-byte units)
+    const uint64_t dA0 = smem_desc_kmajor(smem_u32(smA), 1024, 2);
+    const uint64_t dB0 = smem_desc_kmajor(smem_u32(smB), 1024, 2);
+    const uint32_t a_stage16 = p.a_stage >> 4, b_stage16 = p.b_stage >> 4;
+    int g = 0, it = 0, s = 0;
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
       const int nks = gemm_tile(p, t).nks;
       const int buf = it & 1;
@@ -188,21 +191,19 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
       tc_fence_after();
       const uint32_t dbase = tmem + static_cast<uint32_t>(buf) * p.acc_cols;
       for (int i = 0; i < nks; ++i, ++g) {
-        const int s = g % p.nb;
         stage_handoff();
         tc_fence_after();
         if (lane == 0) {
           if (!abort_flag) {
+            const uint64_t da = dA0 + static_cast<uint64_t>(s * a_stage16);
+            const uint64_t db = dB0 + static_cast<uint64_t>(s * b_stage16);
 #pragma unroll
-            for (int k = 0; k < kGBK / 16; ++k) {
-              const uint64_t da = smem_desc_kmajor(a0 + s * p.a_stage + k * 32, 1024, 2);
-              const uint64_t db = smem_desc_kmajor(b0 + s * p.b_stage + k * 32, 1024, 2);
-              tc_mma_bf16(dbase, da, db, idesc, (i | k) != 0 ? 1u : 0u);
-            }
+            for (int k = 0; k < kGBK / 16; ++k) tc_mma_bf16(dbase, da + 2 * k, db + 2 * k, idesc, (i | k) != 0 ? 1u : 0u);
           }
           tc_commit(&empty_bar[s]);
         }
         __syncwarp();
+        s = (s + 1 == p.nb) ? 0 : s + 1;
       }
       if (lane == 0) tc_commit(&acc_full[buf]);
       __syncwarp();
