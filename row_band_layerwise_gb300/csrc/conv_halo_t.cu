@@ -208,27 +208,24 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
     }
     __syncwarp();
   } else if (warp == 2) {
-    // ---- waiter: polls the barriers the MMA warp consumes, in the MMA warp's order, and hands
-    // each completed one over through the named barrier (one hand-off per wait, also after an abort)
+    // ---- waiter: polls the barriers the MMA warp consumes, in the MMA warp's order, and hands each
+    // weight stage over through the named barrier (one hand-off per stage, also after an abort)
     int acg = 0, kbg = 0, it = 0;
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
       const int buf = it % p.nbuf;
-      if (it >= p.nbuf) {
-        if (lane == 0 && !abort_flag)
-          mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it / p.nbuf) & 1u) ^ 1u, p.status, kErrTimeoutEmpty,
-                    &abort_flag);
-        __syncwarp();
-        stage_handoff();
-      }
       for (int ac = 0; ac < nac; ++ac, ++acg) {
-        if (lane == 0 && !abort_flag)
-          mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag);
-        __syncwarp();
-        stage_handoff();
         for (int gi = 0; gi < ngrp; ++gi, ++kbg) {
-          if (lane == 0 && !abort_flag)
+          if (lane == 0 && !abort_flag) {
+            // the first hand-off of a tile also covers its accumulator buffer, the first of a chunk its rows
+            if (ac == 0 && gi == 0 && it >= p.nbuf)
+              mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it / p.nbuf) & 1u) ^ 1u, p.status, kErrTimeoutEmpty,
+                        &abort_flag);
+            if (gi == 0)
+              mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull,
+                        &abort_flag);
             mbar_wait(&w_full[kbg % p.nw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
                       &abort_flag);
+          }
           __syncwarp();
           stage_handoff();
         }
@@ -255,13 +252,9 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
         xoff[i] = static_cast<uint32_t>(((tap.dy + 1) * static_cast<int>(p.row_bytes) + (tap.dx + 1) * BK * 2) >> 4);
       }
       const int buf = it % p.nbuf;
-      if (it >= p.nbuf) stage_handoff();
-      tc_fence_after();
       const uint32_t dcol = tmem + static_cast<uint32_t>(buf * p.acc_cols);
       for (int ac = 0; ac < nac; ++ac) {
         const int sx = (it * nac + ac) & 1;
-        stage_handoff();
-        tc_fence_after();
         const uint64_t dBs = dB0 + static_cast<uint64_t>(sx * x_stage16);
 #pragma unroll
         for (int gi = 0; gi < 3; ++gi) {
