@@ -32,6 +32,13 @@ struct Vec8<float> {
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
   }
+  // streaming load: the data is read once, keep it from displacing reused lines in L2
+  __device__ static void load_stream(const float* p, float (&v)[8]) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
   __device__ static void store(float* p, const float (&v)[8]) {
     reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
     reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
@@ -41,6 +48,16 @@ template <>
 struct Vec8<__nv_bfloat16> {
   __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
     const uint4 a = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&a);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      v[2 * j] = f.x;
+      v[2 * j + 1] = f.y;
+    }
+  }
+  __device__ static void load_stream(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p));
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&a);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -219,87 +236,119 @@ __device__ __forceinline__ void load8f(const float* p, float (&o)[8]) {
 
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(256) gn_apply_kernel(const Tin* __restrict__ x, Tout* __restrict__ y,
-                                                       Tout* __restrict__ y_raw, long long nvec,
-                                                       long long vec_per_sample, int C,
+                                                       Tout* __restrict__ y_raw, uint32_t nvec,
+                                                       uint32_t vec_per_sample, int C, int vpp_log2,
                                                        const float* __restrict__ scale,
                                                        const float* __restrict__ shift, int silu) {
-  const int vpp = C / 8;
-  const long long step = (long long)gridDim.x * blockDim.x;
+  // 32-bit vector indices (the launcher guarantees nvec < 2^31); the channel of a vector is a
+  // mask when C / 8 is a power of two (every GroupNorm width here), else a 32-bit remainder
+  const uint32_t vpp = static_cast<uint32_t>(C / 8);
+  const uint32_t step = gridDim.x * blockDim.x;
   // two 8-element vectors per thread and iteration: more loads in flight
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nvec; i += 2 * step) {
-    const long long i2 = i + step;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += 2 * step) {
+    const uint32_t i2 = i + step;
     const bool has2 = i2 < nvec;
     float v[8], w[8];
-    Vec8<Tin>::load(x + i * 8, v);
-    if (has2) Vec8<Tin>::load(x + i2 * 8, w);
-    {
-      if (y_raw != nullptr) Vec8<Tout>::store(y_raw + i * 8, v);
-      const int b = static_cast<int>(i / vec_per_sample);
-      const int c0 = static_cast<int>(i % vpp) * 8;
+    Vec8<Tin>::load_stream(x + static_cast<size_t>(i) * 8, v);
+    if (has2) Vec8<Tin>::load_stream(x + static_cast<size_t>(i2) * 8, w);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (h == 1 && !has2) break;
+      const uint32_t iv = h == 0 ? i : i2;
+      float (&u)[8] = h == 0 ? v : w;
+      if (y_raw != nullptr) Vec8<Tout>::store(y_raw + static_cast<size_t>(iv) * 8, u);
+      const uint32_t bs = vec_per_sample == nvec ? 0u : iv / vec_per_sample;
+      const uint32_t c0 = (vpp_log2 >= 0 ? (iv & (vpp - 1)) : iv % vpp) * 8;
       float a[8], sh[8], o[8];
-      load8f(scale + (long long)b * C + c0, a);
-      load8f(shift + (long long)b * C + c0, sh);
+      load8f(scale + static_cast<size_t>(bs) * C + c0, a);
+      load8f(shift + static_cast<size_t>(bs) * C + c0, sh);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float t = fmaf(v[j], a[j], sh[j]);
+        const float t = fmaf(u[j], a[j], sh[j]);
         o[j] = silu ? silu_f(t) : t;
       }
-      Vec8<Tout>::store(y + i * 8, o);
-    }
-    if (has2) {
-      if (y_raw != nullptr) Vec8<Tout>::store(y_raw + i2 * 8, w);
-      const int b = static_cast<int>(i2 / vec_per_sample);
-      const int c0 = static_cast<int>(i2 % vpp) * 8;
-      float a[8], sh[8], o[8];
-      load8f(scale + (long long)b * C + c0, a);
-      load8f(shift + (long long)b * C + c0, sh);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float t = fmaf(w[j], a[j], sh[j]);
-        o[j] = silu ? silu_f(t) : t;
-      }
-      Vec8<Tout>::store(y + i2 * 8, o);
+      Vec8<Tout>::store(y + static_cast<size_t>(iv) * 8, o);
     }
   }
 }
 
-// One warp per pixel.
-template <typename Tin, typename Tout>
-__global__ void rms_norm_kernel(const Tin* __restrict__ x, Tout* __restrict__ y, Tout* __restrict__ y_raw,
-                                long long pixels, int C, const float* __restrict__ gamma, int silu) {
-  const long long wid = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+// Four consecutive channels.
+template <typename T>
+struct Vec4;
+template <>
+struct Vec4<float> {
+  __device__ static float4 load(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+  __device__ static void store(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+};
+template <>
+struct Vec4<__nv_bfloat16> {
+  __device__ static float4 load(const __nv_bfloat16* p) {
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  __device__ static void store(__nv_bfloat16* p, float4 v) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+};
+
+// A group of GS lanes per pixel (GS a power of two dividing 32), each lane holding V four-channel
+// vectors (C = 4 * GS * V), so a warp covers 32 / GS consecutive pixels with every lane busy and
+// each warp-wide access touches 512 contiguous bytes.  Sum of squares: per lane in a fixed order,
+// then a shuffle tree inside the group.
+template <typename Tin, typename Tout, int V>
+__global__ void __launch_bounds__(256) rms_norm_kernel(const Tin* __restrict__ x, Tout* __restrict__ y,
+                                                       Tout* __restrict__ y_raw, long long pixels, int C, int gs,
+                                                       const float* __restrict__ gamma, int silu) {
   const int lane = threadIdx.x & 31;
-  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-  const int nv = C / 8;
+  const int j = lane & (gs - 1);          // position in the group
+  const int ppw = 32 / gs;                // pixels per warp step
+  const long long warp_id = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const float sc = sqrtf(static_cast<float>(C));
-  for (long long pix = wid; pix < pixels; pix += nw) {
-    const Tin* xp = x + pix * C;
-    float v[2][8];
+  float4 gm[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const float* gp = gamma + 4 * (j + gs * i);
+    gm[i] = make_float4(__ldg(gp), __ldg(gp + 1), __ldg(gp + 2), __ldg(gp + 3));
+  }
+  for (long long p0 = warp_id * ppw; p0 < pixels; p0 += nwarps * ppw) {
+    const long long pix = p0 + lane / gs;
+    const bool ok = pix < pixels;
+    float4 v[V];
     float ss = 0.f;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int vi = lane + 32 * k;
-      if (vi < nv) {
-        Vec8<Tin>::load(xp + vi * 8, v[k]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ss = fmaf(v[k][j], v[k][j], ss);
-      }
+    for (int i = 0; i < V; ++i) {
+      v[i] = ok ? Vec4<Tin>::load(x + pix * C + 4 * (j + gs * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      ss = fmaf(v[i].x, v[i].x, ss);
+      ss = fmaf(v[i].y, v[i].y, ss);
+      ss = fmaf(v[i].z, v[i].z, ss);
+      ss = fmaf(v[i].w, v[i].w, ss);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    for (int off = 1; off < gs; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float inv = sc / fmaxf(sqrtf(ss), 1e-12f);
+    if (ok) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int vi = lane + 32 * k;
-      if (vi < nv) {
-        if (y_raw != nullptr) Vec8<Tout>::store(y_raw + pix * C + vi * 8, v[k]);
-        float o[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float t = v[k][j] * inv * __ldg(gamma + vi * 8 + j);
-          o[j] = silu ? silu_f(t) : t;
+      for (int i = 0; i < V; ++i) {
+        const long long e = pix * C + 4 * (j + gs * i);
+        if (y_raw != nullptr) Vec4<Tout>::store(y_raw + e, v[i]);
+        float4 o;
+        o.x = v[i].x * inv * gm[i].x;
+        o.y = v[i].y * inv * gm[i].y;
+        o.z = v[i].z * inv * gm[i].z;
+        o.w = v[i].w * inv * gm[i].w;
+        if (silu) {
+          o.x = silu_f(o.x);
+          o.y = silu_f(o.y);
+          o.z = silu_f(o.z);
+          o.w = silu_f(o.w);
         }
-        Vec8<Tout>::store(y + pix * C + vi * 8, o);
+        Vec4<Tout>::store(y + e, o);
       }
     }
   }
@@ -337,9 +386,11 @@ template <typename Tin, typename Tout>
 void gn_apply_t(const void* x, void* y, void* y_raw, long long nvec, long long vps, int C, const float* scale,
                 const float* shift, int silu, cudaStream_t stream) {
   const int threads = 256;
+  const int vpp = C / 8;
+  const int vpp_log2 = (vpp & (vpp - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(vpp)) : -1;
   gn_apply_kernel<Tin, Tout><<<grid_for(nvec, threads), threads, 0, stream>>>(
-      static_cast<const Tin*>(x), static_cast<Tout*>(y), static_cast<Tout*>(y_raw), nvec, vps, C, scale, shift,
-      silu);
+      static_cast<const Tin*>(x), static_cast<Tout*>(y), static_cast<Tout*>(y_raw), static_cast<uint32_t>(nvec),
+      static_cast<uint32_t>(vps), C, vpp_log2, scale, shift, silu);
 }
 
 cudaError_t launch_gn_apply(int in_dtype, int out_dtype, const void* x, void* y, void* y_raw,
@@ -347,6 +398,7 @@ cudaError_t launch_gn_apply(int in_dtype, int out_dtype, const void* x, void* y,
                             int silu, cudaStream_t stream) {
   if (C % 8 != 0) return cudaErrorInvalidValue;
   const long long vps = pixels_per_sample * (C / 8);
+  if ((long long)B * vps >= (1LL << 31)) return cudaErrorInvalidValue;   // 32-bit vector indices
   const long long nvec = vps * B;
   if (nvec <= 0) return cudaSuccess;
   if (in_dtype == kF32 && out_dtype == kBF16)
@@ -364,13 +416,31 @@ template <typename Tin, typename Tout>
 void rms_t(const void* x, void* y, void* y_raw, long long pixels, int C, const float* gamma, int silu,
            cudaStream_t stream) {
   const int threads = 256;
-  rms_norm_kernel<Tin, Tout><<<grid_for(pixels * 32, threads), threads, 0, stream>>>(
-      static_cast<const Tin*>(x), static_cast<Tout*>(y), static_cast<Tout*>(y_raw), pixels, C, gamma, silu);
+  // lanes per pixel: the largest power of two <= 32 dividing C / 4, leaving at most 8 vectors per lane
+  const int nv4 = C / 4;
+  int gs = 32;
+  while (nv4 % gs != 0) gs >>= 1;
+  const int v = nv4 / gs;
+  const long long warps = (pixels + (32 / gs) - 1) / (32 / gs);
+  const int grid = grid_for(warps * 32, threads);
+  const Tin* xi = static_cast<const Tin*>(x);
+  Tout* yo = static_cast<Tout*>(y);
+  Tout* yr = static_cast<Tout*>(y_raw);
+  switch (v) {
+    case 1: rms_norm_kernel<Tin, Tout, 1><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
+    case 2: rms_norm_kernel<Tin, Tout, 2><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
+    case 3: rms_norm_kernel<Tin, Tout, 3><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
+    case 4: rms_norm_kernel<Tin, Tout, 4><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
+    case 5: rms_norm_kernel<Tin, Tout, 5><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
+    case 6: rms_norm_kernel<Tin, Tout, 6><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
+    case 7: rms_norm_kernel<Tin, Tout, 7><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
+    default: rms_norm_kernel<Tin, Tout, 8><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
+  }
 }
 
 cudaError_t launch_rms_norm(int in_dtype, int out_dtype, const void* x, void* y, void* y_raw, long long pixels,
                             int C, const float* gamma, int silu, cudaStream_t stream) {
-  if (C % 8 != 0 || C > 512) return cudaErrorInvalidValue;
+  if (C % 8 != 0 || C > 512) return cudaErrorInvalidValue;   // C / 4 = (lanes per pixel) x (vectors <= 8)
   if (pixels <= 0) return cudaSuccess;
   if (in_dtype == kF32 && out_dtype == kBF16)
     rms_t<float, __nv_bfloat16>(x, y, y_raw, pixels, C, gamma, silu, stream);
