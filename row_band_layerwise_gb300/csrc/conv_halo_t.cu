@@ -430,15 +430,16 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
             const int yo = (d.y0 + r) * g.osy + (g.nphase > 1 ? py : 0);
             const int npxp = g.nphase > 1 ? 2 : 1;
             const long long orow = static_cast<long long>(d.tt) * g.oH + yo;
-            const long long chunk = (((static_cast<long long>(d.bb) * g.oT * g.oH + orow) * npxp +
-                                      (g.nphase > 1 ? px : 0)) * p.tiles_x + d.tx) * p.csplit +
+            const long long chunk = ((orow * npxp + (g.nphase > 1 ? px : 0)) * p.tiles_x + d.tx) * p.csplit +
                                     (p.csplit == 2 ? sub : 0);
+            const long long n_chunks = static_cast<long long>(g.oT) * g.oH * npxp * p.tiles_x * p.csplit;
             GnPartial o;
             o.n = sn;
             o.mean = smean;
             o.m2 = sm2;
             o.pad = 0.f;
-            p.gn_part[chunk * g.gn_groups + co / p.gn_cg] = o;
+            // [sample][group][chunk]: a group's chunks are contiguous for the merge
+            p.gn_part[(static_cast<long long>(d.bb) * g.gn_groups + co / p.gn_cg) * n_chunks + chunk] = o;
           }
         }
       }

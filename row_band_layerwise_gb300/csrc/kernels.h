@@ -49,7 +49,8 @@ struct GnPartial {
 };
 
 // Phase 1: per (sample, row chunk, group) central moments of a channels-last
-// [B][rows][W][C] tensor (rows = T*H for video; chunk = `chunk_rows` rows).
+// [B][rows][W][C] tensor (rows = T*H for video; chunk = `chunk_rows` rows), stored
+// [sample][group][chunk] (the conv epilogue writes the same layout).
 cudaError_t launch_gn_partials(int dtype, const void* x, int B, int rows, int W, int C, int G, int chunk_rows,
                                GnPartial* part, cudaStream_t stream);
 // Phase 2: merge the chunks of each (sample, group) with the weighted rule and

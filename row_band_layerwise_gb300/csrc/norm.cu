@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kGnThreads) gn_partials_kernel(const T* __rest
     o.mean = mean;
     o.m2 = m2;
     o.pad = 0.f;
-    part[((long long)b * n_chunks + chunk) * G + g] = o;
+    part[((long long)b * G + g) * n_chunks + chunk] = o;
   }
 }
 
@@ -182,19 +182,19 @@ __global__ void __launch_bounds__(kFinThreads) gn_finalize_kernel(const GnPartia
   __shared__ float sn[kFinThreads], sm[kFinThreads], s2[kFinThreads];
   const int b = blockIdx.x / G, g = blockIdx.x % G;
   const int t = threadIdx.x;
-  const GnPartial* pp = part + (long long)b * n_chunks * G + g;
+  const GnPartial* pp = part + ((long long)b * G + g) * n_chunks;   // [sample][group][chunk]
   float n = 0.f, mean = 0.f, m2 = 0.f;
   int c = t;
   // four loads in flight per step, folded in chunk order
   for (; c + 3 * kFinThreads < n_chunks; c += 4 * kFinThreads) {
     GnPartial e[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) e[i] = pp[(long long)(c + i * kFinThreads) * G];
+    for (int i = 0; i < 4; ++i) e[i] = pp[c + i * kFinThreads];
 #pragma unroll
     for (int i = 0; i < 4; ++i) merge_into(n, mean, m2, e[i].n, e[i].mean, e[i].m2);
   }
   for (; c < n_chunks; c += kFinThreads) {
-    const GnPartial e = pp[(long long)c * G];
+    const GnPartial e = pp[c];
     merge_into(n, mean, m2, e.n, e.mean, e.m2);
   }
   sn[t] = n;
