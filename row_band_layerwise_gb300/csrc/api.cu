@@ -46,6 +46,7 @@ constexpr int kNumAct = 5;
 
 struct DevConv {
   void* w = nullptr;     // [rows][ntaps][cin] model dtype
+  void* wn = nullptr;    // bf16 3x3(x kt) convs with 3 outputs: [16][kt * 3][cin], row = kernel_row * 3 + co
   float* b = nullptr;    // [cout]
   int rows = 0, ntaps = 0, cin = 0, cout = 0;
   int kt = 1, kh = 1, kw = 1;
@@ -334,9 +335,10 @@ class Walker {
   }
 
   // Name of the kernel `launch` will run for a conv op (recorded in the op description).
-  const char* conv_kernel(const ConvGeom& g, bool residual, bool out2) const {
+  const char* conv_kernel(const ConvGeom& g, bool residual, bool out2, bool narrow_w) const {
     if (h_->dtype != kBF16) return "conv_simple_f32";
     if (gemm_conv(g, false, residual, out2)) return "gemm_cm";
+    if (narrow_w && !residual && !out2 && g.gn_part == nullptr && conv_narrow_applicable(g)) return "conv_narrow";
     if (conv_halo_t_applicable(g)) return "conv_halo_t";
     if (conv_halo_applicable(g)) return "conv_halo";
     return "conv_tc";
@@ -386,6 +388,13 @@ class Walker {
           gemm(af, what, f > 0);
         }
       }
+      return 0;
+    }
+    if (h_->dtype == kBF16 && w.wn != nullptr && wptr == w.w && residual == nullptr && rowscale == nullptr &&
+        out2 == nullptr && g.gn_part == nullptr && conv_narrow_applicable(g)) {
+      const char* why = nullptr;
+      cudaError_t e = launch_conv_narrow(g, in, w.wn, bias, out, h_->status, st_, &why);
+      if (e != cudaSuccess) set_err(VAEDEC_ERR_CUDA, std::string(what) + ": " + (why ? why : cudaGetErrorString(e)));
       return 0;
     }
     if (h_->dtype == kBF16) {
@@ -511,7 +520,7 @@ class Walker {
     d << "kind=conv name=" << name << " conv="
       << (kind == K3 ? "k3" : kind == K1 ? "k1" : kind == C3 ? "causal3" : kind == UP ? "up2x_k3" : "time")
       << io(x, res, y) << " res=" << (res ? 1 : 0) << " final=" << (final_out ? 1 : 0) << " taps=" << w->ntaps
-      << " flops=" << conv_flops(x, y, *w, kind) << " kernel=" << conv_kernel(g, res != nullptr, copy != nullptr);
+      << " flops=" << conv_flops(x, y, *w, kind) << " kernel=" << conv_kernel(g, res != nullptr, copy != nullptr, w->wn != nullptr);
     if (begin(d.str())) {
       const char* in = static_cast<const char*>(ptr(x));
       void* out2 = copy ? ptr(yc) : nullptr;
@@ -1147,6 +1156,24 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
         if (s != VAEDEC_OK) return bail(s);
         cudaError_t e = cudaMemcpy(dc.w, buf.data(), n * 2, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return bail(cuda_fail(e, "weight upload"));
+        if (nd.cout == 3 && nd.kh == 3 && nd.kw == 3 && !nd.linear) {
+          // narrow-output layout: the three kernel rows x three outputs share one 16-wide MMA N
+          const size_t nn = (size_t)16 * kt * 3 * nd.cin;
+          std::vector<uint16_t> wn(nn, 0);
+          for (int co = 0; co < 3; ++co)
+            for (int ci = 0; ci < nd.cin; ++ci)
+              for (int dt = 0; dt < kt; ++dt)
+                for (int i = 0; i < 3; ++i)
+                  for (int j = 0; j < 3; ++j) {
+                    const int t = (dt * 3 + i) * 3 + j;
+                    wn[((size_t)(i * 3 + co) * (kt * 3) + dt * 3 + j) * nd.cin + ci] =
+                        f32_to_bf16(to_f32(*w, ((size_t)co * nd.cin + ci) * ntaps + t));
+                  }
+          s = h->dalloc(&dc.wn, nn * 2, nd.name.c_str());
+          if (s != VAEDEC_OK) return bail(s);
+          e = cudaMemcpy(dc.wn, wn.data(), nn * 2, cudaMemcpyHostToDevice);
+          if (e != cudaSuccess) return bail(cuda_fail(e, "weight upload"));
+        }
       } else {
         std::vector<float> buf(n, 0.f);
         for (int co = 0; co < nd.cout; ++co)

@@ -35,6 +35,13 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
                                const float* bias, const void* residual, void* out, void* out2, int* status,
                                cudaStream_t stream, const char** why, int* gn_chunks);
 
+// Narrow-output 3x3 / causal 3x3x3 conv (C_out = 3): the three kernel rows share the
+// MMA's N dimension.  `w_narrow` is [16][kt * 3 (frame, kernel column)][Cin] bf16 with row
+// n = kernel_row * C_out + co (rows beyond 3 * C_out zero).
+bool conv_narrow_applicable(const ConvGeom& g);
+cudaError_t launch_conv_narrow(const ConvGeom& g, const void* in, const void* w_narrow, const float* bias,
+                               void* out, int* status, cudaStream_t stream, const char** why);
+
 // CUDA-core fp32 direct convolution over the same ConvGeom (the fp32 path).
 // `wts` is [w_rows][ntaps_w][Cin] fp32.
 cudaError_t launch_conv_simple_f32(const ConvGeom& g, const float* in, const float* wts, int ntaps_w,
