@@ -47,6 +47,7 @@ constexpr int kNumAct = 5;
 struct DevConv {
   void* w = nullptr;     // [rows][ntaps][cin] model dtype
   void* wn = nullptr;    // bf16 3x3(x kt) convs with 3 outputs: [16][kt * 3][cin], row = kernel_row * 3 + co
+  float* b_sc = nullptr; // a resnet conv2: its bias plus the block's shortcut bias (fused shortcut)
   float* b = nullptr;    // [cout]
   int rows = 0, ntaps = 0, cin = 0, cout = 0;
   int kt = 1, kh = 1, kw = 1;
@@ -239,7 +240,7 @@ class Walker {
 
   static std::string io(const Act& x, const Act* aux, const Act& y) {
     std::string s = " in=" + shp(x) + " in_dt=" + dts(x.dt) + " out=" + shp(y) + " out_dt=" + dts(y.dt);
-    if (aux) s += std::string(" aux_dt=") + dts(aux->dt);
+    if (aux) s += std::string(" aux=") + shp(*aux) + " aux_dt=" + dts(aux->dt);
     return s;
   }
 
@@ -346,11 +347,12 @@ class Walker {
 
   // Launch one GEMM/conv described by `g`.
   int launch(const ConvGeom& g, const void* in, const DevConv& w, const void* wptr, const float* bias,
-             const void* residual, const float* rowscale, void* out, void* out2, const char* what) {
+             const void* residual, const float* rowscale, void* out, void* out2, const char* what,
+             const ConvShortcut* sc = nullptr) {
     count();
     if (g.gn_part != nullptr) ++stats_epoch_;   // the moments buffer is about to be rewritten
     int gn_chunks = 0;
-    if (gemm_conv(g, rowscale != nullptr, residual != nullptr, out2 != nullptr)) {
+    if (sc == nullptr && gemm_conv(g, rowscale != nullptr, residual != nullptr, out2 != nullptr)) {
       // 1x1 convolution = channel-major GEMM: out[pixel][co] = W[co][:] . in[pixel][:]
       const long long S = (long long)g.H * g.W;
       GemmArgs a;
@@ -390,8 +392,8 @@ class Walker {
       }
       return 0;
     }
-    if (h_->dtype == kBF16 && w.wn != nullptr && wptr == w.w && residual == nullptr && rowscale == nullptr &&
-        out2 == nullptr && g.gn_part == nullptr && conv_narrow_applicable(g)) {
+    if (sc == nullptr && h_->dtype == kBF16 && w.wn != nullptr && wptr == w.w && residual == nullptr &&
+        rowscale == nullptr && out2 == nullptr && g.gn_part == nullptr && conv_narrow_applicable(g)) {
       const char* why = nullptr;
       cudaError_t e = launch_conv_narrow(g, in, w.wn, bias, out, h_->status, st_, &why);
       if (e != cudaSuccess) set_err(VAEDEC_ERR_CUDA, std::string(what) + ": " + (why ? why : cudaGetErrorString(e)));
@@ -400,7 +402,7 @@ class Walker {
     if (h_->dtype == kBF16) {
       const char* why = nullptr;
       cudaError_t e = launch_conv_tc(g, in, wptr, w.ntaps, w.rows, bias, residual, rowscale, out, out2, h_->status,
-                                     st_, &why, &gn_chunks);
+                                     st_, &why, &gn_chunks, sc);
       if (e != cudaSuccess) set_err(VAEDEC_ERR_CUDA, std::string(what) + ": " + (why ? why : cudaGetErrorString(e)));
     } else {
       check(launch_conv_simple_f32(g, static_cast<const float*>(in), static_cast<const float*>(wptr), w.ntaps, bias,
@@ -463,7 +465,8 @@ class Walker {
   // conv op: x (operand dtype) -> y (`out_dt`, channels-last buffer `out_buf`, or the
   // final channels-first output).  `copy` (optional) receives a bf16 copy of y.
   Act conv(const Act& x, const std::string& name, ConvKind kind, const Act* res, int out_buf, int out_dt,
-           void* final_out = nullptr, Act* copy = nullptr, int copy_buf = -1, bool want_stats = false) {
+           void* final_out = nullptr, Act* copy = nullptr, int copy_buf = -1, bool want_stats = false,
+           const Act* sc_x = nullptr, const std::string& sc_name = std::string()) {
     Act y = x;
     y.stats_chunks = 0;
     y.stats_epoch = -1;
@@ -516,11 +519,18 @@ class Walker {
       g.res_f32 = (res && res->dt == kF32) ? 1 : 0;
       g.scale = 1.f;
     }
+    // a fused 1x1 shortcut (sc_x, weights sc_name) adds its flops and uses the combined bias
+    const DevConv* scw = sc_x ? W(sc_name) : nullptr;
+    if (sc_x && (!scw || !w->b_sc)) return y;
+    double flops = conv_flops(x, y, *w, kind);
+    if (scw) flops += 2.0 * (double)y.pixels() * scw->cout * scw->cin;
     std::ostringstream d;
     d << "kind=conv name=" << name << " conv="
       << (kind == K3 ? "k3" : kind == K1 ? "k1" : kind == C3 ? "causal3" : kind == UP ? "up2x_k3" : "time")
-      << io(x, res, y) << " res=" << (res ? 1 : 0) << " final=" << (final_out ? 1 : 0) << " taps=" << w->ntaps
-      << " flops=" << conv_flops(x, y, *w, kind) << " kernel=" << conv_kernel(g, res != nullptr, copy != nullptr, w->wn != nullptr);
+      << io(x, sc_x ? sc_x : res, y) << " res=" << (res ? 1 : 0) << " final=" << (final_out ? 1 : 0)
+      << " taps=" << w->ntaps << " flops=" << flops
+      << " kernel=" << (scw ? "conv_halo_t" : conv_kernel(g, res != nullptr, copy != nullptr, w->wn != nullptr));
+    if (scw) d << " shortcut=" << sc_name;
     if (begin(d.str())) {
       const char* in = static_cast<const char*>(ptr(x));
       void* out2 = copy ? ptr(yc) : nullptr;
@@ -547,15 +557,22 @@ class Walker {
           g.gn_part = h_->gn_part;
           g.gn_groups = h_->cfg.norm_groups;
         }
-        const int chunks = launch(g, in, *w, w->w, w->b, res ? ptr(*res) : nullptr, nullptr, ptr(y), out2,
-                                  name.c_str());
+        ConvShortcut csc;
+        if (scw) {
+          csc.in = ptr(*sc_x);
+          csc.w = scw->w;
+          csc.cin = scw->cin;
+          csc.w_rows = scw->rows;
+        }
+        const int chunks = launch(g, in, *w, w->w, scw ? w->b_sc : w->b, res ? ptr(*res) : nullptr, nullptr, ptr(y),
+                                  out2, name.c_str(), scw ? &csc : nullptr);
         if (chunks > 0) {
           y.stats_chunks = chunks;
           y.stats_epoch = ++stats_epoch_;
         }
       }
     }
-    end(&x, res, y);
+    end(&x, sc_x ? sc_x : res, y);
     return y;
   }
 
@@ -846,6 +863,31 @@ class Walker {
   // ---------------------------------------------------------------- blocks
   // Residual block on the fp32 stream x.  When `copy` is given, the block output
   // is also stored as a bf16 operand copy (for a following upsample conv).
+  // Whether block `p`'s 1x1 shortcut can be fused into its conv2 (bf16 2D path, channel-major
+  // halo kernel geometry).
+  bool fuse_shortcut(const Act& t2, const std::string& p) const {
+    if (h_->dtype != kBF16 || h_->cfg.family != VAEDEC_FAMILY_KL2D) return false;
+    auto c2 = h_->conv.find(p + ".conv2");
+    auto sc = h_->conv.find(p + ".conv_shortcut");
+    if (c2 == h_->conv.end() || sc == h_->conv.end() || c2->second.b_sc == nullptr) return false;
+    if (sc->second.ntaps != 1) return false;
+    ConvGeom g;
+    std::memset(&g, 0, sizeof(g));
+    g.B = t2.B;
+    g.T = t2.T;
+    g.H = t2.H;
+    g.W = t2.W;
+    g.Cin = t2.C;
+    g.Cout = c2->second.cout;
+    fill_taps(g, K3, c2->second);
+    g.oT = t2.T;
+    g.oH = t2.H;
+    g.oW = t2.W;
+    g.oC = g.Cout;
+    g.osy = g.osx = 1;
+    return conv_halo_t_applicable(g) && conv_halo_t_shortcut_ok(g, sc->second.cin);
+  }
+
   Act resnet(const Act& x, const std::string& p, bool wan, Act* copy) {
     const bool sc = h_->conv.count(p + ".conv_shortcut") > 0;
     const int tb = pick({x.buf});
@@ -857,6 +899,15 @@ class Walker {
     const int hb = pick({x.buf, tb, rb});
     Act hh = conv(t, p + ".conv1", wan ? C3 : K3, nullptr, hb, sdt_, nullptr, nullptr, -1, !wan);
     Act t2 = wan ? rms_norm(hh, p + ".norm2", true, tb) : group_norm(hh, p + ".norm2", true, tb);
+    if (sc && need_raw && fuse_shortcut(t2, p)) {
+      // the 1x1 shortcut runs inside conv2 (extra K over the raw operand copy of x)
+      if (copy && mixed())
+        return conv(t2, p + ".conv2", K3, nullptr, hb, sdt_, nullptr, copy, pick({tb, hb, rb}), true, &xb,
+                    p + ".conv_shortcut");
+      Act y = conv(t2, p + ".conv2", K3, nullptr, hb, sdt_, nullptr, nullptr, -1, true, &xb, p + ".conv_shortcut");
+      if (copy) *copy = y;
+      return y;
+    }
     Act res = x;
     int scb = -1;
     if (sc) {
@@ -1190,6 +1241,21 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
       s = upload_f32(h, bias, &dc.b, nd.name.c_str());
       if (s != VAEDEC_OK) return bail(s);
       h->conv[nd.name] = dc;
+      static const std::string kShortcut = ".conv_shortcut";
+      if (h->dtype == kBF16 && nd.name.size() > kShortcut.size() &&
+          nd.name.compare(nd.name.size() - kShortcut.size(), kShortcut.size(), kShortcut) == 0) {
+        // conv2 of the same block gets its bias plus this one (for the fused shortcut)
+        auto c2 = h->conv.find(nd.name.substr(0, nd.name.size() - kShortcut.size()) + ".conv2");
+        if (c2 != h->conv.end() && c2->second.cout == nd.cout) {
+          std::vector<float> b2(nd.cout), bs(nd.cout);
+          cudaError_t e = cudaMemcpy(b2.data(), c2->second.b, nd.cout * sizeof(float), cudaMemcpyDeviceToHost);
+          if (e == cudaSuccess) e = cudaMemcpy(bs.data(), dc.b, nd.cout * sizeof(float), cudaMemcpyDeviceToHost);
+          if (e != cudaSuccess) return bail(cuda_fail(e, "bias download"));
+          for (int i = 0; i < nd.cout; ++i) b2[i] += bs[i];
+          s = upload_f32(h, b2, &c2->second.b_sc, nd.name.c_str());
+          if (s != VAEDEC_OK) return bail(s);
+        }
+      }
     } else {
       DevNorm dn;
       dn.c = nd.cout;

@@ -60,6 +60,12 @@ struct HaloTParams {
   int* status;
   GnPartial* gn_part;            // GroupNorm chunk moments of the output, or null
   int gn_cg;                     // channels per group (divides 32)
+  // fused 1x1 shortcut (R == 1 only): its input's centre row staged in up to three channel chunks
+  // per stage, beside the matching weight chunks in the three tap slots of a weight stage
+  CUtensorMap tmX2;              // shortcut input 5D (sc_cin, W, H, T, B), box (BK, half, 1, 1, 1)
+  CUtensorMap tmW2;              // shortcut weights 3D (sc_cin, 1, rows), box (BK, 1, 128)
+  int sc_chunks;                 // shortcut channel chunks (sc_cin / BK), 0 = no shortcut
+  int n_sc;                      // shortcut stages per tile: ceil(sc_chunks / 3)
 };
 
 template <int BK>
@@ -147,6 +153,10 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmX);
     tma_prefetch_desc(&p.tmW);
+    if (p.n_sc > 0) {
+      tma_prefetch_desc(&p.tmX2);
+      tma_prefetch_desc(&p.tmW2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, p.tmem_cols);
@@ -197,6 +207,31 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
             ++kbg;
           }
         }
+        for (int sc = 0; sc < p.n_sc && !abort_flag; ++sc) {
+          // fused shortcut: centre row (y0, R == 1) of up to three channel chunks, and their weights
+          const int cnt = min(3, p.sc_chunks - 3 * sc);
+          const int sx = acg & 1;
+          if (acg >= 2 && !mbar_wait(&x_empty[sx], (static_cast<uint32_t>(acg >> 1) & 1u) ^ 1u, p.status,
+                                     kErrTimeoutEmpty, &abort_flag))
+            break;
+          mbar_arrive_expect_tx(&x_full[sx], static_cast<uint32_t>(cnt * 2 * p.half * BK * 2));
+          uint8_t* xs = smX + sx * p.x_stage_bytes;
+          for (int sl = 0; sl < cnt; ++sl) {
+            const int kc = 3 * sc + sl;
+            tma_load_5d(xs + sl * p.row_bytes, &p.tmX2, &x_full[sx], kc * BK, d.x0 - 1, d.y0, d.tt, d.bb);
+            tma_load_5d(xs + sl * p.row_bytes + p.half * BK * 2, &p.tmX2, &x_full[sx], kc * BK, d.x0 - 1 + p.half,
+                        d.y0, d.tt, d.bb);
+          }
+          ++acg;
+          const int sw = kbg % p.nw;
+          if (kbg >= p.nw && !mbar_wait(&w_empty[sw], (static_cast<uint32_t>(kbg / p.nw) & 1u) ^ 1u, p.status,
+                                        kErrTimeoutEmpty, &abort_flag))
+            break;
+          mbar_arrive_expect_tx(&w_full[sw], static_cast<uint32_t>(cnt) * p.w_tap_bytes);
+          uint8_t* ws = smW + sw * p.w_stage_bytes;
+          for (int sl = 0; sl < cnt; ++sl) tma_load_3d(ws + sl * p.w_tap_bytes, &p.tmW2, &w_full[sw], (3 * sc + sl) * BK, 0, d.m0);
+          ++kbg;
+        }
       }
       if (abort_flag) {
         // let the copies already issued land before the CTA exits
@@ -230,6 +265,15 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
           stage_handoff();
         }
       }
+      for (int sc = 0; sc < p.n_sc; ++sc, ++acg, ++kbg) {
+        if (lane == 0 && !abort_flag) {
+          mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag);
+          mbar_wait(&w_full[kbg % p.nw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
+                    &abort_flag);
+        }
+        __syncwarp();
+        stage_handoff();
+      }
     }
   } else if (warp == 1) {
     // ---- MMA issuer: tile i accumulates into TMEM buffer i % nbuf.  It never polls shared memory:
@@ -241,7 +285,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
     const uint64_t dB0 = smem_desc_kmajor(smem_u32(smX), SwzT<BK>::kSbo, SwzT<BK>::kMode);
     const uint32_t w_stage16 = p.w_stage_bytes >> 4, w_tap16 = p.w_tap_bytes >> 4;
     const uint32_t x_stage16 = p.x_stage_bytes >> 4, row16 = p.row_bytes >> 4;
-    int it = 0, sw = 0;
+    int it = 0, sw = 0, acg = 0;
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
       const int phase = decode_tile(p, t).phase;
       // per spatial tap (the same for every causal frame): offset of its shifted rows
@@ -253,8 +297,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
       }
       const int buf = it % p.nbuf;
       const uint32_t dcol = tmem + static_cast<uint32_t>(buf * p.acc_cols);
-      for (int ac = 0; ac < nac; ++ac) {
-        const int sx = (it * nac + ac) & 1;
+      for (int ac = 0; ac < nac; ++ac, ++acg) {
+        const int sx = acg & 1;
         const uint64_t dBs = dB0 + static_cast<uint64_t>(sx * x_stage16);
 #pragma unroll
         for (int gi = 0; gi < 3; ++gi) {
@@ -285,6 +329,30 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
         }
         if (lane == 0) tc_commit(&x_empty[sx]);
         __syncwarp();
+      }
+      for (int sc = 0; sc < p.n_sc; ++sc, ++acg) {
+        // fused shortcut: slot i holds channel chunk 3 sc + i of the centre row and its weights
+        const int cnt = min(3, p.sc_chunks - 3 * sc);
+        const int sx = acg & 1;
+        const uint64_t dBs = dB0 + static_cast<uint64_t>(sx * x_stage16) + (BK * 2 / 16);   // centre pixel
+        stage_handoff();
+        tc_fence_after();
+        if (lane == 0) {
+          if (!abort_flag) {
+            const uint64_t dAs = dA0 + static_cast<uint64_t>(sw * w_stage16);
+#pragma unroll
+            for (int sl = 0; sl < 3; ++sl)
+              if (sl < cnt) {
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                  tc_mma_bf16(dcol, dAs + sl * w_tap16 + 2 * k, dBs + sl * row16 + 2 * k, idesc, 1u);
+              }
+          }
+          tc_commit(&w_empty[sw]);
+          tc_commit(&x_empty[sx]);
+        }
+        __syncwarp();
+        sw = (sw + 1 == p.nw) ? 0 : sw + 1;
       }
       if (lane == 0) tc_commit(&acc_full[buf]);
       __syncwarp();
@@ -480,9 +548,14 @@ bool conv_halo_t_applicable(const ConvGeom& g) {
   return true;
 }
 
+bool conv_halo_t_shortcut_ok(const ConvGeom& g, int sc_cin) {
+  // 2D 3x3 convs only (the shortcut stages the tile's centre row); channel chunks of any BK
+  return g.ntaps == 9 && g.nphase == 1 && g.T >= 1 && sc_cin > 0 && sc_cin % 64 == 0;
+}
+
 cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
                                const float* bias, const void* residual, void* out, void* out2, int* status,
-                               cudaStream_t stream, const char** why, int* gn_chunks) {
+                               cudaStream_t stream, const char** why, int* gn_chunks, const ConvShortcut* sc) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) {
     *why = "cuTensorMapEncodeTiled unavailable";
@@ -502,7 +575,7 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
   p.tiles_x = (g.W + p.npx - 1) / p.npx;
   p.half = round_up_t(p.npx + 2, 16) / 2;          // two boxes per staged row, multiple of 8 pixels each
   const bool heavy_epilogue = g.Cin <= 128 || (g.Cin <= 256 && residual != nullptr);
-  if (p.npx >= 192 && heavy_epilogue) {
+  if ((p.npx >= 192 && heavy_epilogue) || sc != nullptr) {   // a fused shortcut needs one-row tiles
     p.nbuf = 2;
     p.R = 1;
   } else {
@@ -573,6 +646,39 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
       *why = "channel-major halo weight tensor map rejected";
       return cudaErrorInvalidValue;
+    }
+  }
+  if (sc != nullptr) {
+    if (p.R != 1 || sc->cin % bk != 0 || (reinterpret_cast<uintptr_t>(sc->in) & 15) ||
+        (reinterpret_cast<uintptr_t>(sc->w) & 15)) {
+      *why = "shortcut fusion needs one-row tiles and 16-byte aligned operands";
+      return cudaErrorInvalidValue;
+    }
+    p.sc_chunks = sc->cin / bk;
+    p.n_sc = (p.sc_chunks + 2) / 3;
+    {
+      const cuuint64_t dims[5] = {(cuuint64_t)sc->cin, (cuuint64_t)g.W, (cuuint64_t)g.H, (cuuint64_t)g.T,
+                                  (cuuint64_t)g.B};
+      const cuuint64_t strides[4] = {dims[0] * 2, dims[0] * dims[1] * 2, dims[0] * dims[1] * dims[2] * 2,
+                                     dims[0] * dims[1] * dims[2] * dims[3] * 2};
+      const cuuint32_t box[5] = {(cuuint32_t)bk, (cuuint32_t)p.half, 1, 1, 1};
+      if (enc(&p.tmX2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(sc->in), dims, strides, box, ones,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+        *why = "shortcut input tensor map rejected";
+        return cudaErrorInvalidValue;
+      }
+    }
+    {
+      const cuuint64_t dims[3] = {(cuuint64_t)sc->cin, 1, (cuuint64_t)sc->w_rows};
+      const cuuint64_t strides[2] = {dims[0] * 2, dims[0] * 2};
+      const cuuint32_t box[3] = {(cuuint32_t)bk, 1, 128};
+      if (enc(&p.tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(sc->w), dims, strides, box, ones,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+        *why = "shortcut weight tensor map rejected";
+        return cudaErrorInvalidValue;
+      }
     }
   }
   const long long ntiles = (long long)g.B * g.T * p.tiles_y * p.tiles_x * g.nphase * p.n_mtiles;

@@ -252,9 +252,19 @@ const char* conv_tc_plan(const ConvGeom& g, int* bk_out) {
 
 cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
                            const float* bias, const void* residual, const float* rowscale, void* out, void* out2,
-                           int* status, cudaStream_t stream, const char** why, int* gn_chunks) {
+                           int* status, cudaStream_t stream, const char** why, int* gn_chunks,
+                           const ConvShortcut* sc) {
   *why = nullptr;
   if (gn_chunks != nullptr) *gn_chunks = 0;
+  if (sc != nullptr) {
+    // a fused shortcut exists only in the channel-major halo kernel
+    if (rowscale != nullptr || !conv_halo_t_applicable(g) || !conv_halo_t_shortcut_ok(g, sc->cin)) {
+      *why = "shortcut fusion not supported for this conv";
+      return cudaErrorInvalidValue;
+    }
+    return launch_conv_halo_t(g, in, wts, ntaps_w, w_rows, bias, residual, out, out2, status, stream, why,
+                              gn_chunks, sc);
+  }
   int bk = 64;
   if (const char* e = conv_tc_plan(g, &bk)) {
     *why = e;

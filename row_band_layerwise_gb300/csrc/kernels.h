@@ -15,12 +15,23 @@ enum DType : int { kF32 = 1, kBF16 = 2 };
 // `wts` is [w_rows][ntaps_w][Cin] bf16 (K-major per output channel).  `out2`
 // (optional) receives a bf16 copy of a channels-last output.
 const char* conv_tc_plan(const ConvGeom& g, int* bk_out);
+
+// A 1x1 convolution summed into a 3x3 conv's accumulators (a resnet's shortcut fused
+// into its conv2): `in` channels-last bf16 [B][T][H][W][cin] on the conv's grid,
+// `w` [w_rows][1][cin] bf16.  The caller folds the shortcut bias into the conv bias.
+struct ConvShortcut {
+  const void* in = nullptr;
+  const void* w = nullptr;
+  int cin = 0;
+  int w_rows = 0;
+};
 // When g.gn_part is set and the chosen kernel can, the epilogue also writes the
 // GroupNorm central moments of its output in fixed chunks and *gn_chunks receives
 // the number of chunks per sample (0 when no moments were written).
 cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
                            const float* bias, const void* residual, const float* rowscale, void* out, void* out2,
-                           int* status, cudaStream_t stream, const char** why, int* gn_chunks = nullptr);
+                           int* status, cudaStream_t stream, const char** why, int* gn_chunks = nullptr,
+                           const ConvShortcut* sc = nullptr);
 
 // Halo-tile variant (R output rows per CTA, activations staged once per channel
 // chunk for all 3x3 taps); launch_conv_tc dispatches to it when applicable.
@@ -31,9 +42,12 @@ cudaError_t launch_conv_halo(const ConvGeom& g, const void* in, const void* wts,
 
 // Channel-major halo variant (output channels on M, up to 256 pixels on N).
 bool conv_halo_t_applicable(const ConvGeom& g);
+// Whether a shortcut of `sc_cin` input channels can be fused into this conv.
+bool conv_halo_t_shortcut_ok(const ConvGeom& g, int sc_cin);
 cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wts, int ntaps_w, int w_rows,
                                const float* bias, const void* residual, void* out, void* out2, int* status,
-                               cudaStream_t stream, const char** why, int* gn_chunks);
+                               cudaStream_t stream, const char** why, int* gn_chunks,
+                               const ConvShortcut* sc = nullptr);
 
 // Narrow-output 3x3 / causal 3x3x3 conv (C_out = 3): the three kernel rows share the
 // MMA's N dimension.  `w_narrow` is [16][kt * 3 (frame, kernel column)][Cin] bf16 with row

@@ -103,7 +103,15 @@ def oracle_op(d: Dict[str, str], W, arch, x_cl: np.ndarray, aux_cl):
             y = odec.temporal_upsample(x, w, b)
         else:
             raise ValueError(conv)
-        if d.get("res") == "1":
+        if d.get("shortcut"):
+            # 1x1 shortcut of the block fused into this conv: aux is its input
+            sw, sb = W[d["shortcut"] + ".weight"], W[d["shortcut"] + ".bias"]
+            a = cl_to_cf(aux_cl)
+            n, c, t, h, wd = a.shape
+            af = a.transpose(0, 2, 1, 3, 4).reshape(n * t, c, h, wd)
+            s = ops.conv2d_same(af, sw.reshape(sw.shape[0], sw.shape[1], 1, 1), sb)
+            y = y + s.reshape(n, t, s.shape[1], h, wd).transpose(0, 2, 1, 3, 4)
+        elif d.get("res") == "1":
             y = y + cl_to_cf(aux_cl)
         if d.get("final") == "1":
             return y[:, :, 0] if two_d else y
@@ -157,11 +165,12 @@ class Case:
         out_shape = parse_shape(d["out"])
         t_in = torch.empty(int(np.prod(in_shape)), dtype=tdt[d["in_dt"]], device="cuda")
         t_out = torch.empty(int(np.prod(out_shape)), dtype=tdt[d["out_dt"]], device="cuda")
-        t_aux = (torch.empty(int(np.prod(out_shape)), dtype=tdt[d["aux_dt"]], device="cuda")
-                 if d.get("res") == "1" else None)
+        aux_shape = parse_shape(d["aux"]) if "aux" in d else None
+        t_aux = (torch.empty(int(np.prod(aux_shape)), dtype=tdt[d["aux_dt"]], device="cuda")
+                 if aux_shape is not None else None)
         self.dec.run_until(self.z_dev, n_bands, op, t_in, t_aux, t_out)
         torch.cuda.synchronize()
         x = to_numpy(t_in)
         y = to_numpy(t_out)
-        aux = to_numpy(t_aux).reshape(out_shape) if t_aux is not None else None
+        aux = to_numpy(t_aux).reshape(aux_shape) if t_aux is not None else None
         return d, x, aux, y
