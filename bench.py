@@ -93,6 +93,24 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback (no MEASURED_PEAKS.json)"
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks of the default process group (itself when there is
+    none).  Works on any backend: the tensor lives on `device` (CUDA for NCCL, CPU for gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world_size: int, steps: int, pixels_per_step: int, seconds: float) -> float:
+    """Whole-job Mpixel/s of `world_size` replicas that each decoded `steps` steps, timed by the
+    slowest rank (weak scaling: every rank decodes the full workload)."""
+    return world_size * steps * pixels_per_step / seconds / 1e6
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -275,13 +293,9 @@ def run_ours(args, w: synth.Workload):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     per_op = dec.profile_read()             # last timed step
     dec.profile(False)
-    total_ms = sum(step_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     px = out_pixels(w)
-    value = ws * args.steps * px / (total_ms / 1e3) / 1e6
+    value = replica_throughput(ws, args.steps, px, total_ms / 1e3)
 
     # roofline of the dominant kernel: its conv ops' algorithmic flops over their event-timed durations
     conv_ms = sum(ms for d, ms in zip(ops, per_op) if d["kind"] == "conv")
@@ -305,12 +319,8 @@ def run_ours(args, w: synth.Workload):
     t0 = time.perf_counter()
     for _ in range(args.steps):
         dec.decode_host(zh, oh, nb)
-    e2e_s = time.perf_counter() - t0
-    if ws > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = ws * args.steps * px / e2e_s / 1e6
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+    e2e_value = replica_throughput(ws, args.steps, px, e2e_s)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
