@@ -197,6 +197,28 @@ vaedec_status vaedec_debug_run_until(vaedec_t* h, const void* latent, const int6
                                      int n_bands, int op, void* dst_in, size_t in_bytes, void* dst_aux,
                                      size_t aux_bytes, void* dst_out, size_t out_bytes, void* stream);
 
+/* ---- failure injection (no counterpart on the pages; they test exception cleanup and
+ * buffer release on failure: "Static Layer-Wise VAE Decode", Tests).  Process-wide, for tests.
+ *
+ * vaedec_debug_inject_fault: kind 0 = off; 1 = the nth device allocation made by any
+ * vaedec_create from now on fails (create returns VAEDEC_ERR_OOM after releasing everything it
+ * allocated); 2 = at the nth kernel launch of any decode from now on the decode records a
+ * failure, enqueues nothing after that kernel and returns VAEDEC_ERR_CUDA (kernels already
+ * enqueued complete).  nth >= 1.
+ * The fault fires once, then injection switches itself off.  INVALID_ARG for other kinds.
+ *
+ * vaedec_debug_set_wait_limit: the limit of every bounded wait inside the library's kernels,
+ * in nanoseconds (0 restores the default of 2 s).  With a tiny limit the waits run out: the
+ * kernels record a status bit, let their issued copies land, free their TMEM and return, and the
+ * decode returns VAEDEC_ERR_TIMEOUT; the handle stays usable.  Applies to the current device. */
+vaedec_status vaedec_debug_inject_fault(int kind, int nth);
+vaedec_status vaedec_debug_set_wait_limit(uint64_t ns);
+/* Enqueues on `stream` (NULL: the legacy default stream) one kernel that waits, through the
+ * same bounded wait as the decode kernels, on a barrier nothing ever completes: after the wait
+ * limit it records a timeout in the handle's status word and returns, so the next vaedec_sync
+ * returns VAEDEC_ERR_TIMEOUT and the handle stays usable. */
+vaedec_status vaedec_debug_wait_probe(vaedec_t* h, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,8 @@ import numpy as np
 
 from .build import lib_path
 
-__all__ = ["Decoder", "VaedecError", "load_library", "EXPORTED_SYMBOLS", "STATUS_NAMES"]
+__all__ = ["Decoder", "VaedecError", "load_library", "EXPORTED_SYMBOLS", "STATUS_NAMES", "inject_fault",
+           "set_wait_limit"]
 
 FAMILY = {"kl2d": 1, "wan3d": 2}
 DTYPE = {"fp32": 1, "bf16": 2}
@@ -28,7 +29,8 @@ EXPORTED_SYMBOLS = (
     "vaedec_decode", "vaedec_decode_host", "vaedec_sync", "vaedec_last_error",
     "vaedec_launch_count", "vaedec_profile_enable", "vaedec_profile_read",
     "vaedec_debug_num_ops", "vaedec_debug_op_desc", "vaedec_debug_run_until",
-    "vaedec_groupnorm_noalloc",
+    "vaedec_groupnorm_noalloc", "vaedec_debug_inject_fault", "vaedec_debug_set_wait_limit",
+    "vaedec_debug_wait_probe",
 )
 
 
@@ -87,6 +89,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.vaedec_debug_run_until.argtypes = [vp, vp, i64p, i, i, i, vp, ctypes.c_size_t, vp, ctypes.c_size_t,
                                            vp, ctypes.c_size_t, vp]
     lib.vaedec_groupnorm_noalloc.argtypes = [i, i, vp, vp, i, i, i, i, i, vp, vp, ctypes.c_float, i, vp]
+    lib.vaedec_debug_inject_fault.argtypes = [i, i]
+    lib.vaedec_debug_set_wait_limit.argtypes = [ctypes.c_uint64]
+    lib.vaedec_debug_wait_probe.argtypes = [vp, vp]
     for name in EXPORTED_SYMBOLS:
         if name not in ("vaedec_destroy", "vaedec_last_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -131,6 +136,22 @@ def make_config(arch, dtype: str, max_latent: Sequence[int]) -> _Config:
     for k in range(4):
         c.max_latent[k] = int(max_latent[k])
     return c
+
+
+FAULT_KINDS = {"off": 0, "alloc": 1, "launch": 2}
+
+
+def inject_fault(kind: str, nth: int = 1) -> None:
+    """Make the nth device allocation of a create fail ("alloc"), or stop a decode at its nth
+    kernel launch ("launch"), once; "off" clears a pending fault.  Process-wide, for tests."""
+    lib = load_library()
+    _check(lib, lib.vaedec_debug_inject_fault(FAULT_KINDS[kind], int(nth)))
+
+
+def set_wait_limit(ns: int) -> None:
+    """Set the limit of the kernels' bounded waits in nanoseconds (0 restores the default)."""
+    lib = load_library()
+    _check(lib, lib.vaedec_debug_set_wait_limit(int(ns)))
 
 
 def groupnorm_noalloc(x, y, groups: int, gamma, beta, eps: float, silu: bool, stream=None) -> None:
@@ -247,6 +268,10 @@ class Decoder:
 
     def sync(self, stream=None) -> None:
         _check(self.lib, self.lib.vaedec_sync(self._h, self._stream_ptr(stream)))
+
+    def wait_probe(self, stream=None) -> None:
+        """Enqueue a kernel whose bounded wait runs out (see vaedec_debug_wait_probe)."""
+        _check(self.lib, self.lib.vaedec_debug_wait_probe(self._h, self._stream_ptr(stream)))
 
     def launch_count(self) -> int:
         n = ctypes.c_uint64()

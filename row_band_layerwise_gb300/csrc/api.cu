@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -43,6 +44,20 @@ vaedec_status cuda_fail(cudaError_t e, const std::string& where) {
 }
 
 constexpr int kNumAct = 5;
+
+// Process-wide failure injection (vaedec_debug_inject_fault).
+std::atomic<int> g_fault_kind{0};
+std::atomic<int> g_fault_left{0};
+
+// True when the injected fault of `kind` fires now (it fires once, then switches off).
+bool fault_now(int kind) {
+  if (g_fault_kind.load() != kind) return false;
+  if (g_fault_left.fetch_sub(1) == 1) {
+    g_fault_kind.store(0);
+    return true;
+  }
+  return false;
+}
 
 struct DevConv {
   void* w = nullptr;     // [rows][ntaps][cin] model dtype
@@ -125,6 +140,7 @@ struct vaedec {
   vaedec_status dalloc(void** p, size_t bytes, const char* what) {
     *p = nullptr;
     if (bytes == 0) return VAEDEC_OK;
+    if (fault_now(1)) return fail(VAEDEC_ERR_OOM, std::string("injected allocation failure for ") + what);
     cudaError_t e = cudaMalloc(p, bytes);
     if (e != cudaSuccess) {
       cudaGetLastError();
@@ -266,7 +282,10 @@ class Walker {
   }
 
   void count(int n = 1) {
-    if (!dry_) h_->launches += (unsigned long long)n;
+    if (dry_) return;
+    for (int i = 0; i < n; ++i)
+      if (fault_now(2)) set_err(VAEDEC_ERR_CUDA, "injected launch failure");
+    h_->launches += (unsigned long long)n;
   }
 
   // End a traced op: at the stop op, copy its activations out and stop.
@@ -1417,6 +1436,31 @@ vaedec_status vaedec_decode_host(vaedec_t* h, const void* latent_host, const int
   e = cudaMemcpyAsync(out_host, h->io_out, out_b, cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e, "output download");
   return vaedec_sync(h, stream);
+}
+
+vaedec_status vaedec_debug_inject_fault(int kind, int nth) {
+  if (kind < 0 || kind > 2 || (kind != 0 && nth < 1)) return fail(VAEDEC_ERR_INVALID_ARG, "bad fault kind or count");
+  g_fault_kind.store(0);
+  g_fault_left.store(nth);
+  g_fault_kind.store(kind);
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_debug_set_wait_limit(uint64_t ns) {
+  cudaError_t e = set_wait_limit_conv_tc(ns);
+  if (e == cudaSuccess) e = set_wait_limit_conv_halo(ns);
+  if (e == cudaSuccess) e = set_wait_limit_conv_halo_t(ns);
+  if (e == cudaSuccess) e = set_wait_limit_conv_narrow(ns);
+  if (e == cudaSuccess) e = set_wait_limit_gemm_cm(ns);
+  if (e != cudaSuccess) return fail(VAEDEC_ERR_CUDA, std::string("setting the wait limit: ") + cudaGetErrorString(e));
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_debug_wait_probe(vaedec_t* h, void* stream) {
+  if (h == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL handle");
+  cudaError_t e = launch_wait_probe(h->status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(VAEDEC_ERR_CUDA, std::string("wait probe: ") + cudaGetErrorString(e));
+  return VAEDEC_OK;
 }
 
 vaedec_status vaedec_launch_count(const vaedec_t* h, uint64_t* n) {

@@ -210,6 +210,9 @@ __global__ void __launch_bounds__(kHaloThreads, 1) conv_halo_kernel(const __grid
         tc_commit(&a_empty[sa]);
       }
       tc_commit(&accum_bar);
+      // every MMA issued has completed before the CTA releases TMEM (also after a timeout,
+      // when the epilogue stops waiting for the accumulator)
+      mbar_drain(&accum_bar, 0);
     }
     __syncwarp();
   } else {
@@ -392,5 +395,7 @@ cudaError_t launch_conv_halo(const ConvGeom& g, const void* in, const void* wts,
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
+
+VD_WAIT_LIMIT_SETTER(set_wait_limit_conv_halo)
 
 }  // namespace vd

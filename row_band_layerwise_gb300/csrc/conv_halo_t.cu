@@ -714,4 +714,6 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
   return cudaGetLastError();
 }
 
+VD_WAIT_LIMIT_SETTER(set_wait_limit_conv_halo_t)
+
 }  // namespace vd

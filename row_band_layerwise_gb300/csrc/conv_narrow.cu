@@ -376,4 +376,6 @@ cudaError_t launch_conv_narrow(const ConvGeom& g, const void* in, const void* w_
   return cudaGetLastError();
 }
 
+VD_WAIT_LIMIT_SETTER(set_wait_limit_conv_narrow)
+
 }  // namespace vd

@@ -165,6 +165,9 @@ __global__ void __launch_bounds__(kThreads) conv_tc_kernel(const __grid_constant
         tc_commit(&empty_bar[s]);
       }
       tc_commit(&accum_bar);
+      // every MMA issued has completed before the CTA releases TMEM (also after a timeout,
+      // when the epilogue stops waiting for the accumulator)
+      mbar_drain(&accum_bar, 0);
     }
     __syncwarp();
   } else {
@@ -390,5 +393,29 @@ cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, i
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
+
+namespace {
+
+// Waits, with the library's bounded wait, on a barrier that nothing ever completes: the wait
+// runs out after the current limit, records kErrTimeoutFull in *status and the kernel returns.
+__global__ void wait_probe_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    mbar_wait(&bar, 0, status, kErrTimeoutFull, &abort_flag);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_probe(int* status, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(status);
+  return cudaGetLastError();
+}
+
+VD_WAIT_LIMIT_SETTER(set_wait_limit_conv_tc)
 
 }  // namespace vd

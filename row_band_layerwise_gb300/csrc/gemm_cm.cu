@@ -548,4 +548,6 @@ cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, 
   return cudaGetLastError();
 }
 
+VD_WAIT_LIMIT_SETTER(set_wait_limit_gemm_cm)
+
 }  // namespace vd

@@ -132,6 +132,16 @@ cudaError_t launch_softmax_rows(int p_dtype, const void* S, int s_f16, void* P, 
 cudaError_t launch_to_channels_last(int dtype, const void* x, void* y, int B, int C, long long spatial,
                                     cudaStream_t stream);
 
+// Lower (ns > 0) or restore (ns == 0) the bounded-wait limit of each source's kernels.
+cudaError_t set_wait_limit_conv_tc(unsigned long long ns);
+cudaError_t set_wait_limit_conv_halo(unsigned long long ns);
+cudaError_t set_wait_limit_conv_halo_t(unsigned long long ns);
+cudaError_t set_wait_limit_conv_narrow(unsigned long long ns);
+cudaError_t set_wait_limit_gemm_cm(unsigned long long ns);
+
+// One thread waits (bounded) on a barrier nothing completes; records kErrTimeoutFull in *status.
+cudaError_t launch_wait_probe(int* status, cudaStream_t stream);
+
 // Message returned by vaedec_last_error() on the calling thread.
 void record_last_error(const std::string& message);
 

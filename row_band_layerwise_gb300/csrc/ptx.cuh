@@ -21,6 +21,16 @@ enum : int {
 // 2 s: far above any legitimate wait (a stage lands in microseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Limit of the bounded waits in this translation unit (kWaitLimitNs unless a test lowers it to
+// make the waits run out); shutdown drains always use kWaitLimitNs.  Each source that waits
+// defines a host setter for its copy with VD_WAIT_LIMIT_SETTER.
+static __device__ unsigned long long vd_wait_limit_ns = kWaitLimitNs;
+#define VD_WAIT_LIMIT_SETTER(name)                                                     \
+  cudaError_t name(unsigned long long ns) {                                            \
+    const unsigned long long v = ns == 0 ? kWaitLimitNs : ns;                          \
+    return cudaMemcpyToSymbol(vd_wait_limit_ns, &v, sizeof(v));                        \
+  }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -75,7 +85,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 255u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > vd_wait_limit_ns) {
         atomicOr(status, err_bit);
         *abort = 1;
         return false;

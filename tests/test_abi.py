@@ -62,3 +62,9 @@ def test_null_arguments_rejected(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         rbl.load_library(str(tmp_path / "nope.so"))
+
+
+def test_fault_injection_arguments_checked_without_cuda(lib):
+    assert lib.vaedec_debug_inject_fault(7, 1) == 1
+    assert lib.vaedec_debug_inject_fault(1, 0) == 1
+    assert lib.vaedec_debug_inject_fault(0, 0) == 0

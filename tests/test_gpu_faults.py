@@ -1,0 +1,80 @@
+"""Failure handling on the GPU, with no GPU fault, trap or hang.
+
+* Allocation failures injected on the host make vaedec_create return OOM after
+  releasing everything it had allocated (device free memory is unchanged), and a
+  following create works.
+* A refused kernel launch makes the decode return an error; the next decode on
+  the same handle is bit-identical to a clean one.
+* A kernel whose bounded wait is on a barrier nothing completes (the same wait
+  the decode kernels use, its limit lowered to 1 ms) records a timeout in the
+  handle's status word and returns; vaedec_sync reports TIMEOUT once and the
+  same handle then decodes bit-identically again.
+"""
+import numpy as np
+import pytest
+
+import synth
+from gpu_helpers import Case, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+SHAPE = (1, 16, 8, 16)   # widths where the channel-major conv, the GEMM and the narrow conv all run
+
+
+@pytest.fixture(scope="module")
+def case():
+    return Case(synth.KL_ZIMAGE, "bf16", SHAPE)
+
+
+@pytest.fixture(scope="module")
+def clean(case):
+    return case.decode(2).cpu()
+
+
+def _free_bytes(torch):
+    torch.cuda.synchronize()
+    return torch.cuda.mem_get_info()[0]
+
+
+def test_injected_allocation_failure_releases_everything(case):
+    torch, rbl = require_gpu()
+    W = case.W
+    before = _free_bytes(torch)
+    for nth in (1, 5, 17):
+        rbl.inject_fault("alloc", nth)
+        with pytest.raises(rbl.VaedecError) as ei:
+            rbl.Decoder(synth.KL_ZIMAGE, W, "bf16", (1, 1, SHAPE[2], SHAPE[3]))
+        assert ei.value.status == 3   # OOM
+        assert abs(_free_bytes(torch) - before) <= 2 << 20
+    rbl.inject_fault("off")
+    dec = rbl.Decoder(synth.KL_ZIMAGE, W, "bf16", (1, 1, SHAPE[2], SHAPE[3]))
+    out = dec.decode(case.z_dev, 2)
+    torch.cuda.synchronize()
+    dec.sync()
+    assert bool((out.cpu() == case.decode(2).cpu()).all())
+    dec.close()
+
+
+def test_refused_launch_then_clean_decode(case, clean):
+    torch, rbl = require_gpu()
+    rbl.inject_fault("launch", 7)
+    with pytest.raises(rbl.VaedecError) as ei:
+        case.decode(2)
+    assert ei.value.status == 4   # CUDA
+    rbl.inject_fault("off")
+    assert bool((case.decode(2).cpu() == clean).all())
+
+
+def test_bounded_wait_runs_out_and_the_handle_recovers(case, clean):
+    torch, rbl = require_gpu()
+    rbl.set_wait_limit(1_000_000)   # 1 ms
+    try:
+        case.dec.wait_probe()
+        torch.cuda.synchronize()
+        with pytest.raises(rbl.VaedecError) as ei:
+            case.dec.sync()
+        assert ei.value.status == 5   # TIMEOUT
+        case.dec.sync()               # the status word was cleared when it was reported
+    finally:
+        rbl.set_wait_limit(0)
+    assert bool((case.decode(2).cpu() == clean).all())
