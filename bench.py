@@ -334,7 +334,8 @@ def run_ours(args, w: synth.Workload):
     if rank == 0:
         line = {
             "impl": "ours", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "median_ms_per_step": statistics.median(step_ms), "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": value / PAGES_DENSE_MPIXS if w.name == "kl_zimage_1024" else None,
             "dtype": "bf16" if w.dtype == "bf16" else "f32",
@@ -344,6 +345,7 @@ def run_ours(args, w: synth.Workload):
                        "l2": f"{L2_FLUSH_BYTES >> 20} MiB buffer written between steps, outside the step events",
                        "parallelism": "replicas" if ws > 1 else "single GPU",
                        "per_op_times": "CUDA events per op on the decode stream, last timed step",
+                       "workspace_bytes": dec.workspace_bytes(),
                        "vs_baseline_ref": "pages' dense single-GPU Z-Image BF16 1024x1024 decode, 105.97 ms on "
                                           "RTX PRO 6000 Blackwell (context only)"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
