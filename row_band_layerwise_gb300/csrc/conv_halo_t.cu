@@ -114,8 +114,9 @@ __device__ __forceinline__ TileT decode_tile(const HaloTParams& p, int t) {
   return d;
 }
 
-// Named barrier 1, shared by the waiter warp and the MMA warp (64 threads).
-__device__ __forceinline__ void stage_handoff() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+// Named barrier 1, shared by the waiter warp and the MMA warp (64 threads); returns true when the
+// waiter saw the abort flag raised.
+__device__ __forceinline__ bool stage_handoff(bool aborted) { return bar_sync_or(1, 64, aborted); }
 
 template <int BK>
 __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_constant__ HaloTParams p) {
@@ -250,34 +251,44 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
       const int buf = it % p.nbuf;
       for (int ac = 0; ac < nac; ++ac, ++acg) {
         for (int gi = 0; gi < ngrp; ++gi, ++kbg) {
-          if (lane == 0 && !abort_flag) {
-            // the first hand-off of a tile also covers its accumulator buffer, the first of a chunk its rows
-            if (ac == 0 && gi == 0 && it >= p.nbuf)
-              mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it / p.nbuf) & 1u) ^ 1u, p.status, kErrTimeoutEmpty,
+          bool ab = false;
+          if (lane == 0) {
+            if (!abort_flag) {
+              // the first hand-off of a tile also covers its accumulator buffer, the first of a chunk its rows
+              if (ac == 0 && gi == 0 && it >= p.nbuf)
+                mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it / p.nbuf) & 1u) ^ 1u, p.status,
+                          kErrTimeoutEmpty, &abort_flag);
+              if (gi == 0)
+                mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull,
+                          &abort_flag);
+              mbar_wait(&w_full[kbg % p.nw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
                         &abort_flag);
-            if (gi == 0)
-              mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull,
-                        &abort_flag);
-            mbar_wait(&w_full[kbg % p.nw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
-                      &abort_flag);
+            }
+            ab = abort_flag != 0;
           }
           __syncwarp();
-          stage_handoff();
+          stage_handoff(ab);
         }
       }
       for (int sc = 0; sc < p.n_sc; ++sc, ++acg, ++kbg) {
-        if (lane == 0 && !abort_flag) {
-          mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag);
-          mbar_wait(&w_full[kbg % p.nw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
-                    &abort_flag);
+        bool ab = false;
+        if (lane == 0) {
+          if (!abort_flag) {
+            mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull,
+                      &abort_flag);
+            mbar_wait(&w_full[kbg % p.nw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
+                      &abort_flag);
+          }
+          ab = abort_flag != 0;
         }
         __syncwarp();
-        stage_handoff();
+        stage_handoff(ab);
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer: tile i accumulates into TMEM buffer i % nbuf.  It never polls shared memory:
-    // the waiter warp releases it through the named barrier once a stage (or buffer) is ready.  The
+    // ---- MMA issuer: tile i accumulates into TMEM buffer i % nbuf.  It never reads shared memory:
+    // the waiter warp releases it through the named barrier once a stage (or buffer) is ready, and
+    // hands over the abort state in the same barrier.  The
     // issue loop only adds precomputed offsets to two base descriptors (the start-address field is
     // in 16-byte units), so one thread issues faster than the tensor pipe executes.
     const uint32_t idesc = idesc_bf16_f32(128, p.npx);
@@ -302,10 +313,10 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
         const uint64_t dBs = dB0 + static_cast<uint64_t>(sx * x_stage16);
 #pragma unroll
         for (int gi = 0; gi < 3; ++gi) {
-          stage_handoff();
+          const bool aborted = stage_handoff(false);
           tc_fence_after();
           if (lane == 0) {
-            if (!abort_flag) {
+            if (!aborted) {
               const uint64_t dAs = dA0 + static_cast<uint64_t>(sw * w_stage16);
 #pragma unroll
               for (int tp = 0; tp < 3; ++tp) {
@@ -335,10 +346,10 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
         const int cnt = min(3, p.sc_chunks - 3 * sc);
         const int sx = acg & 1;
         const uint64_t dBs = dB0 + static_cast<uint64_t>(sx * x_stage16) + (BK * 2 / 16);   // centre pixel
-        stage_handoff();
+        const bool aborted = stage_handoff(false);
         tc_fence_after();
         if (lane == 0) {
-          if (!abort_flag) {
+          if (!aborted) {
             const uint64_t dAs = dA0 + static_cast<uint64_t>(sw * w_stage16);
 #pragma unroll
             for (int sl = 0; sl < 3; ++sl)

@@ -60,7 +60,7 @@ struct SwzN {
   static constexpr uint32_t kMode = BK == 64 ? 2u : (BK == 32 ? 4u : 6u);
 };
 
-__device__ __forceinline__ void handoff_n() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+__device__ __forceinline__ bool handoff_n(bool aborted) { return bar_sync_or(1, 64, aborted); }
 
 template <int BK>
 __global__ void __launch_bounds__(kThreadsN, 1) conv_narrow_kernel(const __grid_constant__ NarrowParams p) {
@@ -151,14 +151,19 @@ __global__ void __launch_bounds__(kThreadsN, 1) conv_narrow_kernel(const __grid_
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
       const int buf = it & 1;
       for (int c = 0; c < nchunk; ++c, ++gs) {
-        if (lane == 0 && !abort_flag) {
-          if (c == 0 && it >= 2)
-            mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, p.status, kErrTimeoutEmpty,
+        bool ab = false;
+        if (lane == 0) {
+          if (!abort_flag) {
+            if (c == 0 && it >= 2)
+              mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, p.status, kErrTimeoutEmpty,
+                        &abort_flag);
+            mbar_wait(&full_bar[gs & 1], static_cast<uint32_t>(gs >> 1) & 1u, p.status, kErrTimeoutFull,
                       &abort_flag);
-          mbar_wait(&full_bar[gs & 1], static_cast<uint32_t>(gs >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag);
+          }
+          ab = abort_flag != 0;
         }
         __syncwarp();
-        handoff_n();
+        handoff_n(ab);
       }
     }
   } else if (warp == 1) {
@@ -174,10 +179,10 @@ __global__ void __launch_bounds__(kThreadsN, 1) conv_narrow_kernel(const __grid_
       const uint32_t dcol = tmem + static_cast<uint32_t>(buf * kAcc);
       for (int c = 0; c < nchunk; ++c, ++gs) {
         const int s = gs & 1;
-        handoff_n();
+        const bool aborted = handoff_n(false);
         tc_fence_after();
         if (lane == 0) {
-          if (!abort_flag) {
+          if (!aborted) {
             const uint64_t dXs = dX0 + static_cast<uint64_t>(s * stage16);
             const uint64_t dWs = dW0 + static_cast<uint64_t>(s * stage16);
 #pragma unroll

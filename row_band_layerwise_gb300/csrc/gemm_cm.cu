@@ -77,8 +77,9 @@ __device__ __forceinline__ GTile gemm_tile(const GemmParams& p, int t) {
   return d;
 }
 
-// Named barrier 1, shared by the waiter warp and the MMA warp (64 threads).
-__device__ __forceinline__ void stage_handoff() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+// Named barrier 1, shared by the waiter warp and the MMA warp (64 threads); returns true when the
+// waiter saw the abort flag raised.
+__device__ __forceinline__ bool stage_handoff(bool aborted) { return bar_sync_or(1, 64, aborted); }
 
 // Named barrier `id` over the 128 threads of one epilogue half (four warps).
 __device__ __forceinline__ void half_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
@@ -161,16 +162,26 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
     }
     __syncwarp();
   } else if (warp == 2) {
-    // ---- waiter: one hand-off per stage of every tile, always (also after an abort)
-    int g = 0;
-    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+    // ---- waiter: one hand-off per stage of every tile, always (also after an abort); the first of a
+    // tile also covers the tile's accumulator buffer
+    int g = 0, it = 0;
+    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
       const int nks = gemm_tile(p, t).nks;
+      const int buf = it & 1;
       for (int i = 0; i < nks; ++i, ++g) {
-        if (lane == 0 && !abort_flag)
-          mbar_wait(&full_bar[g % p.nb], static_cast<uint32_t>(g / p.nb) & 1u, p.status, kErrTimeoutFull,
-                    &abort_flag);
+        bool ab = false;
+        if (lane == 0) {
+          if (!abort_flag) {
+            if (i == 0 && it >= 2)
+              mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, p.status, kErrTimeoutEmpty,
+                        &abort_flag);
+            mbar_wait(&full_bar[g % p.nb], static_cast<uint32_t>(g / p.nb) & 1u, p.status, kErrTimeoutFull,
+                      &abort_flag);
+          }
+          ab = abort_flag != 0;
+        }
         __syncwarp();
-        stage_handoff();
+        stage_handoff(ab);
       }
     }
   } else if (warp == 1) {
@@ -184,17 +195,12 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
       const int nks = gemm_tile(p, t).nks;
       const int buf = it & 1;
-      if (lane == 0 && it >= 2 && !abort_flag)
-        mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it >> 1) & 1u) ^ 1u, p.status, kErrTimeoutEmpty,
-                  &abort_flag);
-      __syncwarp();
-      tc_fence_after();
       const uint32_t dbase = tmem + static_cast<uint32_t>(buf) * p.acc_cols;
       for (int i = 0; i < nks; ++i, ++g) {
-        stage_handoff();
+        const bool aborted = stage_handoff(false);
         tc_fence_after();
         if (lane == 0) {
-          if (!abort_flag) {
+          if (!aborted) {
             const uint64_t da = dA0 + static_cast<uint64_t>(s * a_stage16);
             const uint64_t db = dB0 + static_cast<uint64_t>(s * b_stage16);
 #pragma unroll

@@ -354,9 +354,31 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(const Tin* __restrict__ x
   }
 }
 
-int grid_for(long long work, int threads) {
+int sm_count() {
+  static const int n = [] {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      sms = 1;
+    return sms;
+  }();
+  return n;
+}
+
+// Blocks of `threads` that are resident on one SM at once for `kernel` (its registers decide).
+template <typename KernelT>
+int blocks_per_sm(KernelT kernel, int threads) {
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0) != cudaSuccess || occ < 1) occ = 1;
+  return occ;
+}
+
+// Grid for a grid-stride loop over `work` items: no more blocks than are resident at once, so
+// every block loops over an equal share and no partial second wave runs at low occupancy.
+int grid_for(long long work, int threads, int resident_per_sm) {
   const long long b = (work + threads - 1) / threads;
-  return static_cast<int>(b < 152LL * 8 ? (b < 1 ? 1 : b) : 152LL * 8);
+  const long long cap = static_cast<long long>(sm_count()) * resident_per_sm;
+  return static_cast<int>(b < cap ? (b < 1 ? 1 : b) : cap);
 }
 
 }  // namespace
@@ -388,7 +410,8 @@ void gn_apply_t(const void* x, void* y, void* y_raw, long long nvec, long long v
   const int threads = 256;
   const int vpp = C / 8;
   const int vpp_log2 = (vpp & (vpp - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(vpp)) : -1;
-  gn_apply_kernel<Tin, Tout><<<grid_for(nvec, threads), threads, 0, stream>>>(
+  static const int occ = blocks_per_sm(gn_apply_kernel<Tin, Tout>, threads);
+  gn_apply_kernel<Tin, Tout><<<grid_for(nvec, threads, occ), threads, 0, stream>>>(
       static_cast<const Tin*>(x), static_cast<Tout*>(y), static_cast<Tout*>(y_raw), static_cast<uint32_t>(nvec),
       static_cast<uint32_t>(vps), C, vpp_log2, scale, shift, silu);
 }
@@ -412,29 +435,36 @@ cudaError_t launch_gn_apply(int in_dtype, int out_dtype, const void* x, void* y,
   return cudaGetLastError();
 }
 
+template <typename Tin, typename Tout, int V>
+void rms_launch(const Tin* x, Tout* y, Tout* y_raw, long long warps, long long pixels, int C, int gs,
+                const float* gamma, int silu, cudaStream_t stream) {
+  const int threads = 256;
+  static const int occ = blocks_per_sm(rms_norm_kernel<Tin, Tout, V>, threads);
+  rms_norm_kernel<Tin, Tout, V><<<grid_for(warps * 32, threads, occ), threads, 0, stream>>>(x, y, y_raw, pixels, C, gs,
+                                                                                            gamma, silu);
+}
+
 template <typename Tin, typename Tout>
 void rms_t(const void* x, void* y, void* y_raw, long long pixels, int C, const float* gamma, int silu,
            cudaStream_t stream) {
-  const int threads = 256;
   // lanes per pixel: the largest power of two <= 32 dividing C / 4, leaving at most 8 vectors per lane
   const int nv4 = C / 4;
   int gs = 32;
   while (nv4 % gs != 0) gs >>= 1;
   const int v = nv4 / gs;
   const long long warps = (pixels + (32 / gs) - 1) / (32 / gs);
-  const int grid = grid_for(warps * 32, threads);
   const Tin* xi = static_cast<const Tin*>(x);
   Tout* yo = static_cast<Tout*>(y);
   Tout* yr = static_cast<Tout*>(y_raw);
   switch (v) {
-    case 1: rms_norm_kernel<Tin, Tout, 1><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
-    case 2: rms_norm_kernel<Tin, Tout, 2><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
-    case 3: rms_norm_kernel<Tin, Tout, 3><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
-    case 4: rms_norm_kernel<Tin, Tout, 4><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
-    case 5: rms_norm_kernel<Tin, Tout, 5><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
-    case 6: rms_norm_kernel<Tin, Tout, 6><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
-    case 7: rms_norm_kernel<Tin, Tout, 7><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
-    default: rms_norm_kernel<Tin, Tout, 8><<<grid, threads, 0, stream>>>(xi, yo, yr, pixels, C, gs, gamma, silu); break;
+    case 1: rms_launch<Tin, Tout, 1>(xi, yo, yr, warps, pixels, C, gs, gamma, silu, stream); break;
+    case 2: rms_launch<Tin, Tout, 2>(xi, yo, yr, warps, pixels, C, gs, gamma, silu, stream); break;
+    case 3: rms_launch<Tin, Tout, 3>(xi, yo, yr, warps, pixels, C, gs, gamma, silu, stream); break;
+    case 4: rms_launch<Tin, Tout, 4>(xi, yo, yr, warps, pixels, C, gs, gamma, silu, stream); break;
+    case 5: rms_launch<Tin, Tout, 5>(xi, yo, yr, warps, pixels, C, gs, gamma, silu, stream); break;
+    case 6: rms_launch<Tin, Tout, 6>(xi, yo, yr, warps, pixels, C, gs, gamma, silu, stream); break;
+    case 7: rms_launch<Tin, Tout, 7>(xi, yo, yr, warps, pixels, C, gs, gamma, silu, stream); break;
+    default: rms_launch<Tin, Tout, 8>(xi, yo, yr, warps, pixels, C, gs, gamma, silu, stream); break;
   }
 }
 

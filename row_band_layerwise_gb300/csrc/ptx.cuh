@@ -105,6 +105,21 @@ __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Named barrier `id` over `count` threads (a multiple of 32) that also returns the OR of `v` over
+// them.  A waiter warp hands the abort state to an MMA-issuing warp this way, so the issuing thread
+// never loads it from shared memory (a load costs about a thousand cycles while the tensor pipe
+// saturates shared memory).
+__device__ __forceinline__ bool bar_sync_or(int id, int count, bool v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred pv, pr;\n\tsetp.ne.s32 pv, %1, 0;\n\tbar.red.or.pred pr, %2, %3, pv;\n\t"
+      "selp.s32 %0, 1, 0, pr;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<int>(v)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
