@@ -176,6 +176,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
       const uint32_t x_tx = static_cast<uint32_t>((p.R + 2) * 2 * p.half * BK * 2);
       const uint32_t w_tx = static_cast<uint32_t>(3 * 128 * BK * 2);
       int acg = 0, kbg = 0;   // chunks / weight stages issued so far (all tiles)
+      int sw = 0;             // weight slot of stage kbg (kbg % nw, kept as a running count)
+      uint32_t wpar = 1u;     // parity of the empty phase that frees slot sw for stage kbg
       for (int t = blockIdx.x; t < p.ntiles && !abort_flag; t += gridDim.x) {
         const TileT d = decode_tile(p, t);
         for (int ac = 0; ac < nac && !abort_flag; ++ac) {
@@ -196,16 +198,17 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
           }
           ++acg;
           for (int gi = 0; gi < ngrp; ++gi) {
-            const int sw = kbg % p.nw;
-            if (kbg >= p.nw && !mbar_wait(&w_empty[sw], (static_cast<uint32_t>(kbg / p.nw) & 1u) ^ 1u, p.status,
-                                          kErrTimeoutEmpty, &abort_flag))
-              break;
+            if (kbg >= p.nw && !mbar_wait(&w_empty[sw], wpar, p.status, kErrTimeoutEmpty, &abort_flag)) break;
             mbar_arrive_expect_tx(&w_full[sw], w_tx);
             uint8_t* ws = smW + sw * p.w_stage_bytes;
             for (int tp = 0; tp < 3; ++tp)
               tma_load_3d(ws + tp * p.w_tap_bytes, &p.tmW, &w_full[sw], kc * BK,
                           g.taps[d.phase][dti * nsp + gi * 3 + tp].wtap, d.m0);
             ++kbg;
+            if (++sw == p.nw) {
+              sw = 0;
+              wpar ^= 1u;
+            }
           }
         }
         for (int sc = 0; sc < p.n_sc && !abort_flag; ++sc) {
@@ -224,14 +227,15 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
                         d.y0, d.tt, d.bb);
           }
           ++acg;
-          const int sw = kbg % p.nw;
-          if (kbg >= p.nw && !mbar_wait(&w_empty[sw], (static_cast<uint32_t>(kbg / p.nw) & 1u) ^ 1u, p.status,
-                                        kErrTimeoutEmpty, &abort_flag))
-            break;
+          if (kbg >= p.nw && !mbar_wait(&w_empty[sw], wpar, p.status, kErrTimeoutEmpty, &abort_flag)) break;
           mbar_arrive_expect_tx(&w_full[sw], static_cast<uint32_t>(cnt) * p.w_tap_bytes);
           uint8_t* ws = smW + sw * p.w_stage_bytes;
           for (int sl = 0; sl < cnt; ++sl) tma_load_3d(ws + sl * p.w_tap_bytes, &p.tmW2, &w_full[sw], (3 * sc + sl) * BK, 0, d.m0);
           ++kbg;
+          if (++sw == p.nw) {
+            sw = 0;
+            wpar ^= 1u;
+          }
         }
       }
       if (abort_flag) {
@@ -246,43 +250,47 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
   } else if (warp == 2) {
     // ---- waiter: polls the barriers the MMA warp consumes, in the MMA warp's order, and hands each
     // weight stage over through the named barrier (one hand-off per stage, also after an abort)
-    int acg = 0, kbg = 0, it = 0;
+    // (slot, parity) of every ring advance as running counts: no divisions in the loop
+    int acg = 0, it = 0, buf = 0, sw = 0;
+    uint32_t wpar = 0u, apar = 1u;   // full parity of slot sw; empty parity of accumulator buf
+    bool ab = false;                 // abort seen (lane 0)
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
-      const int buf = it % p.nbuf;
       for (int ac = 0; ac < nac; ++ac, ++acg) {
-        for (int gi = 0; gi < ngrp; ++gi, ++kbg) {
-          bool ab = false;
-          if (lane == 0) {
-            if (!abort_flag) {
-              // the first hand-off of a tile also covers its accumulator buffer, the first of a chunk its rows
-              if (ac == 0 && gi == 0 && it >= p.nbuf)
-                mbar_wait(&acc_empty[buf], (static_cast<uint32_t>(it / p.nbuf) & 1u) ^ 1u, p.status,
-                          kErrTimeoutEmpty, &abort_flag);
-              if (gi == 0)
-                mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull,
-                          &abort_flag);
-              mbar_wait(&w_full[kbg % p.nw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
+        for (int gi = 0; gi < ngrp; ++gi) {
+          if (lane == 0 && !ab) {
+            // the first hand-off of a tile also covers its accumulator buffer, the first of a chunk its rows
+            if (ac == 0 && gi == 0 && it >= p.nbuf)
+              mbar_wait(&acc_empty[buf], apar, p.status, kErrTimeoutEmpty, &abort_flag);
+            if (gi == 0)
+              mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull,
                         &abort_flag);
-            }
+            mbar_wait(&w_full[sw], wpar, p.status, kErrTimeoutFull, &abort_flag);
             ab = abort_flag != 0;
           }
           __syncwarp();
           stage_handoff(ab);
+          if (++sw == p.nw) {
+            sw = 0;
+            wpar ^= 1u;
+          }
         }
       }
-      for (int sc = 0; sc < p.n_sc; ++sc, ++acg, ++kbg) {
-        bool ab = false;
-        if (lane == 0) {
-          if (!abort_flag) {
-            mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull,
-                      &abort_flag);
-            mbar_wait(&w_full[kbg % p.nw], static_cast<uint32_t>(kbg / p.nw) & 1u, p.status, kErrTimeoutFull,
-                      &abort_flag);
-          }
+      for (int sc = 0; sc < p.n_sc; ++sc, ++acg) {
+        if (lane == 0 && !ab) {
+          mbar_wait(&x_full[acg & 1], static_cast<uint32_t>(acg >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag);
+          mbar_wait(&w_full[sw], wpar, p.status, kErrTimeoutFull, &abort_flag);
           ab = abort_flag != 0;
         }
         __syncwarp();
         stage_handoff(ab);
+        if (++sw == p.nw) {
+          sw = 0;
+          wpar ^= 1u;
+        }
+      }
+      if (++buf == p.nbuf) {
+        buf = 0;
+        apar ^= 1u;
       }
     }
   } else if (warp == 1) {
