@@ -40,6 +40,8 @@ constexpr int kThreadsT = 352;   // warp 0 TMA, warp 1 MMA, warp 2 waiter, warps
 constexpr int kEpiWarpsT = 8;
 constexpr int kMaxWStages = 4;
 constexpr int kPipeBytesT = 212 * 1024;
+constexpr int kStageOutBytes = 16 * 32 * 4;   // one epilogue warp's [16 px][32 ch] fp32 staging
+constexpr int kMaxDynSmemT = 227 * 1024;
 
 struct HaloTParams {
   CUtensorMap tmX;               // activations 5D (Cin, W, H, T, B), box (BK, half, 1, 1, 1)
@@ -66,6 +68,11 @@ struct HaloTParams {
   CUtensorMap tmW2;              // shortcut weights 3D (sc_cin, 1, rows), box (BK, 1, 128)
   int sc_chunks;                 // shortcut channel chunks (sc_cin / BK), 0 = no shortcut
   int n_sc;                      // shortcut stages per tile: ceil(sc_chunks / 3)
+  // fp32 output through shared memory and TMA tensor stores (each epilogue warp stages 16 pixels x
+  // its 32 channels, then one thread stores them), instead of one 4-byte store per value
+  CUtensorMap tmO;               // output 3D (oC, oW, B * oT * oH), box (32, 16, 1)
+  int tma_out;
+  uint32_t stage_out_off;        // byte offset of the eight 2 KB staging buffers in the pipeline
 };
 
 template <int BK>
@@ -114,11 +121,52 @@ __device__ __forceinline__ TileT decode_tile(const HaloTParams& p, int t) {
   return d;
 }
 
+// GroupNorm chunk moments of output channel `co` over tile row r, from sums shifted by kshift, merged
+// over the group's gn_cg consecutive lanes and stored by the group's first lane.
+__device__ __forceinline__ void gn_store(const HaloTParams& p, const TileT& d, int r, int co, bool cvalid, int lane,
+                                         int sub, float kshift, float s1, float s2, float cnt) {
+  const ConvGeom& g = p.g;
+  const int py = d.phase >> 1, px = d.phase & 1;
+  // this channel's (count, mean, centred sum of squares) over the row
+  float sn = cnt, smean = 0.f, sm2 = 0.f;
+  if (cnt > 0.f) {
+    const float d1 = s1 / cnt;
+    smean = kshift + d1;
+    sm2 = fmaxf(s2 - s1 * d1, 0.f);
+  }
+  // merge the group's channels (gn_cg consecutive lanes), lower lane first
+  for (int off = 1; off < p.gn_cg; off <<= 1) {
+    const float on = __shfl_xor_sync(0xffffffffu, sn, off);
+    const float om = __shfl_xor_sync(0xffffffffu, smean, off);
+    const float o2 = __shfl_xor_sync(0xffffffffu, sm2, off);
+    if (lane & off)
+      moments_merge(on, om, o2, sn, smean, sm2, sn, smean, sm2);
+    else
+      moments_merge(sn, smean, sm2, on, om, o2, sn, smean, sm2);
+  }
+  if (cvalid && (lane % p.gn_cg) == 0) {
+    // chunk = (output row, phase column, pixel tile, column half), fixed by the geometry alone
+    const int yo = (d.y0 + r) * g.osy + (g.nphase > 1 ? py : 0);
+    const int npxp = g.nphase > 1 ? 2 : 1;
+    const long long orow = static_cast<long long>(d.tt) * g.oH + yo;
+    const long long chunk = ((orow * npxp + (g.nphase > 1 ? px : 0)) * p.tiles_x + d.tx) * p.csplit +
+                            (p.csplit == 2 ? sub : 0);
+    const long long n_chunks = static_cast<long long>(g.oT) * g.oH * npxp * p.tiles_x * p.csplit;
+    GnPartial o;
+    o.n = sn;
+    o.mean = smean;
+    o.m2 = sm2;
+    o.pad = 0.f;
+    // [sample][group][chunk]: a group's chunks are contiguous for the merge
+    p.gn_part[(static_cast<long long>(d.bb) * g.gn_groups + co / p.gn_cg) * n_chunks + chunk] = o;
+  }
+}
+
 // Named barrier 1, shared by the waiter warp and the MMA warp (64 threads); returns true when the
 // waiter saw the abort flag raised.
 __device__ __forceinline__ bool stage_handoff(bool aborted) { return bar_sync_or(1, 64, aborted); }
 
-template <int BK>
+template <int BK, bool kTmaOut>
 __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_constant__ HaloTParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t x_full[2], x_empty[2];
@@ -425,6 +473,67 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
       for (int r = r_begin; r < p.R; r += r_step) {
         if (d.y0 + r >= g.H) break;   // uniform across the warp
         const long long erow = row_first(r) + co;
+        if constexpr (kTmaOut) {
+          // 16-pixel sub-chunks: TMEM -> registers -> this warp's staging rows -> TMA tensor store
+          uint8_t* stg = smem + p.stage_out_off + (warp - 3) * kStageOutBytes;
+          const uint32_t stg_lane = smem_u32(stg) + 4u * lane;
+          const int orow = (d.bb * g.oT + d.tt) * g.oH + (d.y0 + r);
+          float rv[16], rn[16];
+          auto load_res16 = [&](int c0, float (&dst)[16]) {
+            const int nvalid = min(16, min(c_end - c0, g.W - (d.x0 + c0)));
+            const float* rp = static_cast<const float*>(p.residual) + erow + static_cast<long long>(c0) * stride;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dst[j] = (j < nvalid) ? rp[j * stride] : 0.f;
+          };
+          if (has_res && c_begin < c_end && d.x0 + c_begin < g.W) load_res16(c_begin, rv);
+          float kshift = 0.f, s1 = 0.f, s2 = 0.f, cnt = 0.f;
+          for (int c0 = c_begin; c0 < c_end; c0 += 16) {
+            const int nvalid = min(16, min(c_end - c0, g.W - (d.x0 + c0)));
+            if (nvalid <= 0) break;   // uniform across the warp
+            uint32_t rr[16];
+            tmem_ld_16x_32x32b(lane_addr + static_cast<uint32_t>(r * p.npx + c0), rr);
+            if (has_res && c0 + 16 < c_end && d.x0 + c0 + 16 < g.W) load_res16(c0 + 16, rn);
+            tmem_ld_wait();
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(rr[j]) * g.scale + bias;
+            if (has_res) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += rv[j];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) rv[j] = rn[j];
+            }
+            if (p.gn_part != nullptr) {
+              if (c0 == c_begin) kshift = v[0];
+              float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float dv = (j < nvalid) ? v[j] - kshift : 0.f;
+                a1[j & 3] += dv;
+                a2[j & 3] = fmaf(dv, dv, a2[j & 3]);
+              }
+              s1 += (a1[0] + a1[1]) + (a1[2] + a1[3]);
+              s2 += (a2[0] + a2[1]) + (a2[2] + a2[3]);
+              cnt += static_cast<float>(nvalid);
+            }
+            // the previous store from this buffer has finished reading it
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg_lane + 128u * j), "f"(v[j]) : "memory");
+            fence_proxy_async_smem();
+            __syncwarp();
+            // pixels beyond the image width are clipped by the store
+            if (lane == 0) {
+              tma_store_3d(&p.tmO, stg, d.m0 + q * 32, d.x0 + c0, orow);
+              bulk_commit_group();
+            }
+            __syncwarp();   // reconverge before the next warp-wide TMEM load
+          }
+          if (p.gn_part != nullptr) gn_store(p, d, r, co, cvalid, lane, sub, kshift, s1, s2, cnt);
+          continue;
+        }
         // residual of chunk c0 in rv; the next chunk's loads are issued before this one is used
         float rv[32], rn[32];
         auto load_res = [&](int c0, float (&dst)[32]) {
@@ -494,56 +603,23 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
           }
           __syncwarp();   // reconverge before the next warp-wide TMEM load
         }
-        if (p.gn_part != nullptr) {
-          // this channel's (count, mean, centred sum of squares) over the row
-          float sn = cnt, smean = 0.f, sm2 = 0.f;
-          if (cnt > 0.f) {
-            const float d1 = s1 / cnt;
-            smean = kshift + d1;
-            sm2 = fmaxf(s2 - s1 * d1, 0.f);
-          }
-          // merge the group's channels (gn_cg consecutive lanes), lower lane first
-          for (int off = 1; off < p.gn_cg; off <<= 1) {
-            const float on = __shfl_xor_sync(0xffffffffu, sn, off);
-            const float om = __shfl_xor_sync(0xffffffffu, smean, off);
-            const float o2 = __shfl_xor_sync(0xffffffffu, sm2, off);
-            if (lane & off)
-              moments_merge(on, om, o2, sn, smean, sm2, sn, smean, sm2);
-            else
-              moments_merge(sn, smean, sm2, on, om, o2, sn, smean, sm2);
-          }
-          if (cvalid && (lane % p.gn_cg) == 0) {
-            // chunk = (output row, phase column, pixel tile, column half), fixed by the geometry alone
-            const int yo = (d.y0 + r) * g.osy + (g.nphase > 1 ? py : 0);
-            const int npxp = g.nphase > 1 ? 2 : 1;
-            const long long orow = static_cast<long long>(d.tt) * g.oH + yo;
-            const long long chunk = ((orow * npxp + (g.nphase > 1 ? px : 0)) * p.tiles_x + d.tx) * p.csplit +
-                                    (p.csplit == 2 ? sub : 0);
-            const long long n_chunks = static_cast<long long>(g.oT) * g.oH * npxp * p.tiles_x * p.csplit;
-            GnPartial o;
-            o.n = sn;
-            o.mean = smean;
-            o.m2 = sm2;
-            o.pad = 0.f;
-            // [sample][group][chunk]: a group's chunks are contiguous for the merge
-            p.gn_part[(static_cast<long long>(d.bb) * g.gn_groups + co / p.gn_cg) * n_chunks + chunk] = o;
-          }
-        }
+        if (p.gn_part != nullptr) gn_store(p, d, r, co, cvalid, lane, sub, kshift, s1, s2, cnt);
       }
       // hand the accumulator buffer back to the MMA issuer
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
+    // every staged store has completed before the CTA exits
+    if (kTmaOut && lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
-
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, p.tmem_cols);
   }
 }
-
 int round_up_t(int a, int b) { return (a + b - 1) / b * b; }
 
 }  // namespace
@@ -700,6 +776,25 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
       }
     }
   }
+  // fp32 channels-last output with whole 32-channel quarters: store through shared memory with TMA
+  size_t smem = 2 * (size_t)p.x_stage_bytes + (size_t)p.nw * p.w_stage_bytes + 1024;
+  // (not where a residual is read in a serial epilogue: there the 32-pixel chunks' deeper residual
+  // loads of the direct stores win)
+  if (g.out_f32 && out2 == nullptr && g.nphase == 1 && g.osx == 1 && g.osy == 1 && g.Cout % 32 == 0 &&
+      (p.nbuf == 2 || residual == nullptr) &&
+      g.oC == g.Cout && (residual == nullptr || g.res_f32) && (reinterpret_cast<uintptr_t>(out) & 15) == 0 &&
+      smem + kEpiWarpsT * kStageOutBytes <= (size_t)kMaxDynSmemT) {
+    const cuuint64_t dims[3] = {(cuuint64_t)g.oC, (cuuint64_t)g.oW, (cuuint64_t)g.B * g.oT * g.oH};
+    const cuuint64_t strides[2] = {dims[0] * 4, dims[0] * dims[1] * 4};
+    const cuuint32_t box[3] = {32, 16, 1};
+    if (enc(&p.tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+      p.tma_out = 1;
+      p.stage_out_off = 2 * p.x_stage_bytes + static_cast<uint32_t>(p.nw) * p.w_stage_bytes;
+      smem += kEpiWarpsT * kStageOutBytes;
+    }
+  }
   const long long ntiles = (long long)g.B * g.T * p.tiles_y * p.tiles_x * g.nphase * p.n_mtiles;
   if (ntiles <= 0) return cudaSuccess;
   if (ntiles > 0x7fffffffLL) {
@@ -713,20 +808,21 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
   if (ea == cudaSuccess) ea = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (ea != cudaSuccess) return ea;
   const long long nblocks = std::min<long long>(ntiles, std::max(1, sms));
-  const size_t smem = 2 * (size_t)p.x_stage_bytes + (size_t)p.nw * p.w_stage_bytes + 1024;
   cudaError_t e;
+  auto go = [&](auto kern) {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (r == cudaSuccess) kern<<<(unsigned)nblocks, kThreadsT, smem, stream>>>(p);
+    return r;
+  };
   switch (bk) {
     case 64:
-      e = cudaFuncSetAttribute(conv_halo_t_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_halo_t_kernel<64><<<(unsigned)nblocks, kThreadsT, smem, stream>>>(p);
+      e = p.tma_out ? go(conv_halo_t_kernel<64, true>) : go(conv_halo_t_kernel<64, false>);
       break;
     case 32:
-      e = cudaFuncSetAttribute(conv_halo_t_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_halo_t_kernel<32><<<(unsigned)nblocks, kThreadsT, smem, stream>>>(p);
+      e = p.tma_out ? go(conv_halo_t_kernel<32, true>) : go(conv_halo_t_kernel<32, false>);
       break;
     default:
-      e = cudaFuncSetAttribute(conv_halo_t_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_halo_t_kernel<16><<<(unsigned)nblocks, kThreadsT, smem, stream>>>(p);
+      e = p.tma_out ? go(conv_halo_t_kernel<16, true>) : go(conv_halo_t_kernel<16, false>);
       break;
   }
   if (e != cudaSuccess) return e;
