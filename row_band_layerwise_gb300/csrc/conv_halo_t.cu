@@ -41,6 +41,7 @@ constexpr int kEpiWarpsT = 8;
 constexpr int kMaxWStages = 4;
 constexpr int kPipeBytesT = 212 * 1024;
 constexpr int kStageOutBytes = 16 * 32 * 4;   // one epilogue warp's [16 px][32 ch] fp32 staging
+constexpr int kResBufs = 3;                    // staging buffers per warp when the residual comes by TMA
 constexpr int kMaxDynSmemT = 227 * 1024;
 
 struct HaloTParams {
@@ -71,8 +72,9 @@ struct HaloTParams {
   // fp32 output through shared memory and TMA tensor stores (each epilogue warp stages 16 pixels x
   // its 32 channels, then one thread stores them), instead of one 4-byte store per value
   CUtensorMap tmO;               // output 3D (oC, oW, B * oT * oH), box (32, 16, 1)
-  int tma_out;
-  uint32_t stage_out_off;        // byte offset of the eight 2 KB staging buffers in the pipeline
+  CUtensorMap tmR;               // fp32 residual, same geometry as tmO (loaded with TMA when tma_out == 2)
+  int tma_out;                   // 0: direct stores; 1: TMA stores; 2: also TMA residual loads (one-row tiles)
+  uint32_t stage_out_off;        // byte offset of the epilogue staging buffers (2 KB each) in the pipeline
 };
 
 template <int BK>
@@ -166,12 +168,13 @@ __device__ __forceinline__ void gn_store(const HaloTParams& p, const TileT& d, i
 // waiter saw the abort flag raised.
 __device__ __forceinline__ bool stage_handoff(bool aborted) { return bar_sync_or(1, 64, aborted); }
 
-template <int BK, bool kTmaOut>
+template <int BK, int kOut>
 __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_constant__ HaloTParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t x_full[2], x_empty[2];
   __shared__ __align__(8) uint64_t w_full[kMaxWStages], w_empty[kMaxWStages];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
+  __shared__ __align__(8) uint64_t res_full[kEpiWarpsT * kResBufs];   // residual TMA loads (tma_out == 2)
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -195,6 +198,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
       mbar_init(&w_empty[i], 1);
     }
     mbar_init(&mma_done, 1);
+    for (int i = 0; i < kEpiWarpsT * kResBufs; ++i) mbar_init(&res_full[i], 1);
     abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -202,6 +206,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmX);
     tma_prefetch_desc(&p.tmW);
+    if (p.tma_out != 0) tma_prefetch_desc(&p.tmO);
+    if (p.tma_out == 2) tma_prefetch_desc(&p.tmR);
     if (p.n_sc > 0) {
       tma_prefetch_desc(&p.tmX2);
       tma_prefetch_desc(&p.tmW2);
@@ -440,10 +446,32 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
     const long long stride = static_cast<long long>(g.osx) * g.oC;   // elements between neighbouring pixels
     const bool res_f32 = g.res_f32 != 0;
     const int rsize = res_f32 ? 4 : 2;
+    // tma_out == 2: this warp's ring of kResBufs staging buffers; the residual of a 16-pixel sub-chunk is
+    // loaded into a buffer two sub-chunks ahead, the output overwrites it in place and is stored from it
+    uint8_t* rbuf0 = smem + p.stage_out_off + (warp - 3) * kResBufs * kStageOutBytes;
+    uint64_t* rbar = res_full + (warp - 3) * kResBufs;
+    int ld_slot = 0, use_slot = 0, pending = 0;   // next slot to load / to consume; loads not yet consumed
+    uint32_t use_par = 0u;
     int it = 0;
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
       const TileT d = decode_tile(p, t);
       const int buf = it % p.nbuf;
+      // tma_out == 2 (one-row tiles): this warp's residual sub-chunks, the first two loaded before the
+      // accumulator is ready
+      const int orow0 = (d.bb * g.oT + d.tt) * g.oH + d.y0;
+      const int c_lim = min(c_end, g.W - d.x0);
+      const int nsc = (kOut == 2 && d.y0 < g.H && c_lim > c_begin) ? (c_lim - c_begin + 15) / 16 : 0;
+      auto issue_res = [&](int i) {   // lane 0: residual of sub-chunk i into the next slot
+        bulk_wait_group_read1();      // the store that last used the slot (all but the newest) has read it
+        mbar_arrive_expect_tx(&rbar[ld_slot], kStageOutBytes);
+        tma_load_3d(rbuf0 + ld_slot * kStageOutBytes, &p.tmR, &rbar[ld_slot], d.m0 + q * 32, d.x0 + c_begin + 16 * i,
+                    orow0);
+        ld_slot = ld_slot + 1 == kResBufs ? 0 : ld_slot + 1;
+        ++pending;
+      };
+      if (kOut == 2 && lane == 0) {
+        for (int i = 0; i < 2 && i < nsc; ++i) issue_res(i);
+      }
       const int co = d.m0 + q * 32 + lane;
       const bool cvalid = co < g.Cout;
       const float bias = (p.bias != nullptr && cvalid) ? p.bias[co] : 0.f;
@@ -473,7 +501,60 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
       for (int r = r_begin; r < p.R; r += r_step) {
         if (d.y0 + r >= g.H) break;   // uniform across the warp
         const long long erow = row_first(r) + co;
-        if constexpr (kTmaOut) {
+        if constexpr (kOut == 2) {
+          // one-row tiles: residual and output both pass through this warp's staging ring
+          float kshift = 0.f, s1 = 0.f, s2 = 0.f, cnt = 0.f;
+          const uint32_t lane4 = 4u * lane;
+          for (int i = 0; i < nsc; ++i) {
+            const int c0 = c_begin + 16 * i;
+            const int nvalid = min(16, c_lim - c0);
+            uint32_t rr[16];
+            tmem_ld_16x_32x32b(lane_addr + static_cast<uint32_t>(c0), rr);
+            uint8_t* sb = rbuf0 + use_slot * kStageOutBytes;
+            const uint32_t sa = smem_u32(sb) + lane4;
+            const bool okr = mbar_wait(&rbar[use_slot], use_par, p.status, kErrTimeoutAccum, &abort_flag);
+            tmem_ld_wait();
+            if (!__all_sync(0xffffffffu, okr)) break;
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float rj;
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(rj) : "r"(sa + 128u * j) : "memory");
+              v[j] = __uint_as_float(rr[j]) * g.scale + bias + (cvalid ? rj : 0.f);
+            }
+            if (p.gn_part != nullptr) {
+              if (i == 0) kshift = v[0];
+              float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float dv = (j < nvalid) ? v[j] - kshift : 0.f;
+                a1[j & 3] += dv;
+                a2[j & 3] = fmaf(dv, dv, a2[j & 3]);
+              }
+              s1 += (a1[0] + a1[1]) + (a1[2] + a1[3]);
+              s2 += (a2[0] + a2[1]) + (a2[2] + a2[3]);
+              cnt += static_cast<float>(nvalid);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              asm volatile("st.shared.f32 [%0], %1;" ::"r"(sa + 128u * j), "f"(v[j]) : "memory");
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              // pixels beyond the image width are clipped by the store
+              tma_store_3d(&p.tmO, sb, d.m0 + q * 32, d.x0 + c0, orow0);
+              bulk_commit_group();
+              if (i + 2 < nsc) issue_res(i + 2);
+            }
+            --pending;
+            use_slot = use_slot + 1 == kResBufs ? 0 : use_slot + 1;
+            if (use_slot == 0) use_par ^= 1u;
+            __syncwarp();   // reconverge before the next warp-wide TMEM load
+          }
+          if (p.gn_part != nullptr) gn_store(p, d, r, co, cvalid, lane, sub, kshift, s1, s2, cnt);
+          continue;
+        }
+        if constexpr (kOut == 1) {
           // 16-pixel sub-chunks: TMEM -> registers -> this warp's staging rows -> TMA tensor store
           uint8_t* stg = smem + p.stage_out_off + (warp - 3) * kStageOutBytes;
           const uint32_t stg_lane = smem_u32(stg) + 4u * lane;
@@ -611,7 +692,15 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
     // every staged store has completed before the CTA exits
-    if (kTmaOut && lane == 0) bulk_wait_group0();
+    if (kOut == 2 && lane == 0) {
+      // residual loads issued but not consumed (a stopped decode) land before the CTA exits
+      for (; pending > 0; --pending) {
+        mbar_drain(&rbar[use_slot], use_par);
+        use_slot = use_slot + 1 == kResBufs ? 0 : use_slot + 1;
+        if (use_slot == 0) use_par ^= 1u;
+      }
+    }
+    if (kOut != 0 && lane == 0) bulk_wait_group0();
     __syncwarp();
   }
   __syncthreads();
@@ -791,8 +880,23 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
       p.tma_out = 1;
+      // one-row tiles with an fp32 residual: the residual also comes by TMA, through a ring of three
+      // staging buffers per warp (room taken from the fourth weight stage)
+      const int nw3 = std::min(p.nw, 3);
+      const size_t smem3 = 2 * (size_t)p.x_stage_bytes + (size_t)nw3 * p.w_stage_bytes + 1024 +
+                           (size_t)kEpiWarpsT * kResBufs * kStageOutBytes;
+      if (residual != nullptr && p.nbuf == 2 && p.R == 1 && p.csplit == 2 && nw3 >= 3 &&
+          (reinterpret_cast<uintptr_t>(residual) & 15) == 0 && smem3 <= (size_t)kMaxDynSmemT &&
+          enc(&p.tmR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(residual), dims, strides, box, ones,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+        p.tma_out = 2;
+        p.nw = nw3;
+        smem = smem3;
+      } else {
+        smem += kEpiWarpsT * kStageOutBytes;
+      }
       p.stage_out_off = 2 * p.x_stage_bytes + static_cast<uint32_t>(p.nw) * p.w_stage_bytes;
-      smem += kEpiWarpsT * kStageOutBytes;
     }
   }
   const long long ntiles = (long long)g.B * g.T * p.tiles_y * p.tiles_x * g.nphase * p.n_mtiles;
@@ -814,16 +918,16 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
     if (r == cudaSuccess) kern<<<(unsigned)nblocks, kThreadsT, smem, stream>>>(p);
     return r;
   };
-  switch (bk) {
-    case 64:
-      e = p.tma_out ? go(conv_halo_t_kernel<64, true>) : go(conv_halo_t_kernel<64, false>);
-      break;
-    case 32:
-      e = p.tma_out ? go(conv_halo_t_kernel<32, true>) : go(conv_halo_t_kernel<32, false>);
-      break;
-    default:
-      e = p.tma_out ? go(conv_halo_t_kernel<16, true>) : go(conv_halo_t_kernel<16, false>);
-      break;
+  switch (bk * 4 + p.tma_out) {
+    case 64 * 4 + 0: e = go(conv_halo_t_kernel<64, 0>); break;
+    case 64 * 4 + 1: e = go(conv_halo_t_kernel<64, 1>); break;
+    case 64 * 4 + 2: e = go(conv_halo_t_kernel<64, 2>); break;
+    case 32 * 4 + 0: e = go(conv_halo_t_kernel<32, 0>); break;
+    case 32 * 4 + 1: e = go(conv_halo_t_kernel<32, 1>); break;
+    case 32 * 4 + 2: e = go(conv_halo_t_kernel<32, 2>); break;
+    case 16 * 4 + 0: e = go(conv_halo_t_kernel<16, 0>); break;
+    case 16 * 4 + 1: e = go(conv_halo_t_kernel<16, 1>); break;
+    default: e = go(conv_halo_t_kernel<16, 2>); break;
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
