@@ -42,6 +42,7 @@ constexpr int kMaxWStages = 4;
 constexpr int kPipeBytesT = 212 * 1024;
 constexpr int kStageOutBytes = 16 * 32 * 4;   // one epilogue warp's [16 px][32 ch] fp32 staging
 constexpr int kResBufs = 3;                    // staging buffers per warp when the residual comes by TMA
+constexpr int kStageOut2Bytes = 16 * 32 * 2;   // one epilogue warp's [16 px][32 ch] bf16 copy staging
 constexpr int kMaxDynSmemT = 227 * 1024;
 
 struct HaloTParams {
@@ -73,6 +74,7 @@ struct HaloTParams {
   // its 32 channels, then one thread stores them), instead of one 4-byte store per value
   CUtensorMap tmO;               // output 3D (oC, oW, B * oT * oH), box (32, 16, 1)
   CUtensorMap tmR;               // fp32 residual, same geometry as tmO (loaded with TMA when tma_out == 2)
+  CUtensorMap tmO2;              // bf16 copy of the output, same geometry (tma_out == 1 with out2)
   int tma_out;                   // 0: direct stores; 1: TMA stores; 2: also TMA residual loads (one-row tiles)
   uint32_t stage_out_off;        // byte offset of the epilogue staging buffers (2 KB each) in the pipeline
 };
@@ -558,6 +560,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
           // 16-pixel sub-chunks: TMEM -> registers -> this warp's staging rows -> TMA tensor store
           uint8_t* stg = smem + p.stage_out_off + (warp - 3) * kStageOutBytes;
           const uint32_t stg_lane = smem_u32(stg) + 4u * lane;
+          uint8_t* stg2 = smem + p.stage_out_off + kEpiWarpsT * kStageOutBytes + (warp - 3) * kStageOut2Bytes;
+          const uint32_t stg2_lane = smem_u32(stg2) + 2u * lane;
           const int orow = (d.bb * g.oT + d.tt) * g.oH + (d.y0 + r);
           float rv[16], rn[16];
           auto load_res16 = [&](int c0, float (&dst)[16]) {
@@ -603,11 +607,19 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg_lane + 128u * j), "f"(v[j]) : "memory");
+            if (p.out2 != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                asm volatile("st.shared.b16 [%0], %1;" ::"r"(stg2_lane + 64u * j),
+                             "h"(__bfloat16_as_ushort(__float2bfloat16_rn(v[j])))
+                             : "memory");
+            }
             fence_proxy_async_smem();
             __syncwarp();
             // pixels beyond the image width are clipped by the store
             if (lane == 0) {
               tma_store_3d(&p.tmO, stg, d.m0 + q * 32, d.x0 + c0, orow);
+              if (p.out2 != nullptr) tma_store_3d(&p.tmO2, stg2, d.m0 + q * 32, d.x0 + c0, orow);
               bulk_commit_group();
             }
             __syncwarp();   // reconverge before the next warp-wide TMEM load
@@ -869,10 +881,11 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
   size_t smem = 2 * (size_t)p.x_stage_bytes + (size_t)p.nw * p.w_stage_bytes + 1024;
   // (not where a residual is read in a serial epilogue: there the 32-pixel chunks' deeper residual
   // loads of the direct stores win)
-  if (g.out_f32 && out2 == nullptr && g.nphase == 1 && g.osx == 1 && g.osy == 1 && g.Cout % 32 == 0 &&
+  const size_t stage1 = (size_t)kEpiWarpsT * (kStageOutBytes + (out2 != nullptr ? kStageOut2Bytes : 0));
+  if (g.out_f32 && g.nphase == 1 && g.osx == 1 && g.osy == 1 && g.Cout % 32 == 0 &&
       (p.nbuf == 2 || residual == nullptr) &&
       g.oC == g.Cout && (residual == nullptr || g.res_f32) && (reinterpret_cast<uintptr_t>(out) & 15) == 0 &&
-      smem + kEpiWarpsT * kStageOutBytes <= (size_t)kMaxDynSmemT) {
+      (reinterpret_cast<uintptr_t>(out2) & 15) == 0 && smem + stage1 <= (size_t)kMaxDynSmemT) {
     const cuuint64_t dims[3] = {(cuuint64_t)g.oC, (cuuint64_t)g.oW, (cuuint64_t)g.B * g.oT * g.oH};
     const cuuint64_t strides[2] = {dims[0] * 4, dims[0] * dims[1] * 4};
     const cuuint32_t box[3] = {32, 16, 1};
@@ -885,7 +898,15 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
       const int nw3 = std::min(p.nw, 3);
       const size_t smem3 = 2 * (size_t)p.x_stage_bytes + (size_t)nw3 * p.w_stage_bytes + 1024 +
                            (size_t)kEpiWarpsT * kResBufs * kStageOutBytes;
-      if (residual != nullptr && p.nbuf == 2 && p.R == 1 && p.csplit == 2 && nw3 >= 3 &&
+      if (out2 != nullptr) {
+        const cuuint64_t strides2[2] = {dims[0] * 2, dims[0] * dims[1] * 2};
+        if (enc(&p.tmO2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out2, dims, strides2, box, ones,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          p.tma_out = 0;
+      }
+      if (p.tma_out == 1 && out2 == nullptr && residual != nullptr && p.nbuf == 2 && p.R == 1 && p.csplit == 2 &&
+          nw3 >= 3 &&
           (reinterpret_cast<uintptr_t>(residual) & 15) == 0 && smem3 <= (size_t)kMaxDynSmemT &&
           enc(&p.tmR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(residual), dims, strides, box, ones,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -893,8 +914,8 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
         p.tma_out = 2;
         p.nw = nw3;
         smem = smem3;
-      } else {
-        smem += kEpiWarpsT * kStageOutBytes;
+      } else if (p.tma_out == 1) {
+        smem += stage1;
       }
       p.stage_out_off = 2 * p.x_stage_bytes + static_cast<uint32_t>(p.nw) * p.w_stage_bytes;
     }
