@@ -760,18 +760,19 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
   HaloTParams p;
   std::memset(&p, 0, sizeof(p));
   p.g = g;
-  // pixel tile: split the row into equal tiles of at most 256 pixels (multiple of 16).  Where the
-  // epilogue is heavy next to the MMA work (128 input channels, or up to 256 with a residual to
-  // read) and tiles have at least 192 pixels, a tile is one row in one of two 256-column
-  // accumulator buffers, so its epilogue overlaps the next tile's MMAs.  Otherwise R rows share
-  // one buffer of up to 512 columns: twice the pixels per weight fetch, which wins when the MMA
-  // work dominates (and keeps the MMAs wide: narrower ones are shared-memory bound).
+  // pixel tile: split the row into equal tiles of at most 256 pixels (multiple of 16).  Where tiles
+  // have at least 192 pixels and the layer is not an upsample, a tile is one row in one of two
+  // 256-column accumulator buffers, so its epilogue overlaps the next tile's MMAs; measured on the
+  // decoders' layers this wins everywhere except for wide rows (> 256 px) read with more than 256
+  // input channels and no residual, where R rows sharing one buffer of up to 512 columns (twice
+  // the pixels per weight fetch, fewer re-read halo rows) keep the loads below the TMA rate.
+  // Narrower tiles also take R rows (narrower MMAs are shared-memory bound).
   const int ntx = (g.W + 255) / 256;
   p.npx = round_up_t((g.W + ntx - 1) / ntx, 16);
   p.tiles_x = (g.W + p.npx - 1) / p.npx;
   p.half = round_up_t(p.npx + 2, 16) / 2;          // two boxes per staged row, multiple of 8 pixels each
-  const bool heavy_epilogue = g.Cin <= 128 || (g.Cin <= 256 && residual != nullptr);
-  if ((p.npx >= 192 && heavy_epilogue) || sc != nullptr) {   // a fused shortcut needs one-row tiles
+  const bool one_row = g.nphase == 1 && (g.Cin <= 256 || residual != nullptr || g.W <= 256);
+  if ((p.npx >= 192 && one_row) || sc != nullptr) {   // a fused shortcut needs one-row tiles
     p.nbuf = 2;
     p.R = 1;
   } else {

@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 # workloads whose fixtures must be present (their oracle decodes take minutes)
-REQUIRED = ("kl_zimage_512", "kl_zimage_1024", "kl_zimage_b2_800x1088")
+REQUIRED = ("kl_zimage_512", "kl_zimage_1024", "kl_zimage_b2_800x1088", "wan_17x480x832")
 
 
 def load_samples(name):
