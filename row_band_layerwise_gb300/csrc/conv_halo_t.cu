@@ -125,6 +125,41 @@ __device__ __forceinline__ TileT decode_tile(const HaloTParams& p, int t) {
   return d;
 }
 
+// Shifted GroupNorm sums of v[0..15] (the first nvalid values): four interleaved partial sums per
+// moment, the pairs of each group of four added as packed f32x2 (the same roundings, in the same
+// order, as four scalar accumulators), then folded in a fixed tree.
+__device__ __forceinline__ void gn_sums16(const float (&v)[16], int nvalid, float kshift, float& s1, float& s2,
+                                          float& cnt) {
+  float2 a1l = make_float2(0.f, 0.f), a1h = a1l, a2l = a1l, a2h = a1l;
+  if (nvalid == 16) {
+    const float2 nk = make_float2(-kshift, -kshift);
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+      const float2 dl = __fadd2_rn(make_float2(v[j], v[j + 1]), nk);
+      const float2 dh = __fadd2_rn(make_float2(v[j + 2], v[j + 3]), nk);
+      a1l = __fadd2_rn(a1l, dl);
+      a1h = __fadd2_rn(a1h, dh);
+      a2l = __ffma2_rn(dl, dl, a2l);
+      a2h = __ffma2_rn(dh, dh, a2h);
+    }
+  } else {
+    float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float dv = (j < nvalid) ? v[j] - kshift : 0.f;
+      a1[j & 3] += dv;
+      a2[j & 3] = fmaf(dv, dv, a2[j & 3]);
+    }
+    a1l = make_float2(a1[0], a1[1]);
+    a1h = make_float2(a1[2], a1[3]);
+    a2l = make_float2(a2[0], a2[1]);
+    a2h = make_float2(a2[2], a2[3]);
+  }
+  s1 += (a1l.x + a1l.y) + (a1h.x + a1h.y);
+  s2 += (a2l.x + a2l.y) + (a2h.x + a2h.y);
+  cnt += static_cast<float>(nvalid);
+}
+
 // GroupNorm chunk moments of output channel `co` over tile row r, from sums shifted by kshift, merged
 // over the group's gn_cg consecutive lanes and stored by the group's first lane.
 __device__ __forceinline__ void gn_store(const HaloTParams& p, const TileT& d, int r, int co, bool cvalid, int lane,
@@ -518,24 +553,20 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
             tmem_ld_wait();
             if (!__all_sync(0xffffffffu, okr)) break;
             float v[16];
+            const float2 sc2 = make_float2(g.scale, g.scale), b2 = make_float2(bias, bias);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float rj;
-              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(rj) : "r"(sa + 128u * j) : "memory");
-              v[j] = __uint_as_float(rr[j]) * g.scale + bias + (cvalid ? rj : 0.f);
+            for (int j = 0; j < 16; j += 2) {
+              float r0, r1;
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r0) : "r"(sa + 128u * j) : "memory");
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r1) : "r"(sa + 128u * (j + 1)) : "memory");
+              float2 t = __ffma2_rn(make_float2(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1])), sc2, b2);
+              t = __fadd2_rn(t, cvalid ? make_float2(r0, r1) : make_float2(0.f, 0.f));
+              v[j] = t.x;
+              v[j + 1] = t.y;
             }
             if (p.gn_part != nullptr) {
               if (i == 0) kshift = v[0];
-              float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float dv = (j < nvalid) ? v[j] - kshift : 0.f;
-                a1[j & 3] += dv;
-                a2[j & 3] = fmaf(dv, dv, a2[j & 3]);
-              }
-              s1 += (a1[0] + a1[1]) + (a1[2] + a1[3]);
-              s2 += (a2[0] + a2[1]) + (a2[2] + a2[3]);
-              cnt += static_cast<float>(nvalid);
+              gn_sums16(v, nvalid, kshift, s1, s2, cnt);
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -580,26 +611,21 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
             if (has_res && c0 + 16 < c_end && d.x0 + c0 + 16 < g.W) load_res16(c0 + 16, rn);
             tmem_ld_wait();
             float v[16];
+            const float2 sc2 = make_float2(g.scale, g.scale), b2 = make_float2(bias, bias);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(rr[j]) * g.scale + bias;
+            for (int j = 0; j < 16; j += 2) {
+              float2 t = __ffma2_rn(make_float2(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1])), sc2, b2);
+              if (has_res) t = __fadd2_rn(t, make_float2(rv[j], rv[j + 1]));
+              v[j] = t.x;
+              v[j + 1] = t.y;
+            }
             if (has_res) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += rv[j];
 #pragma unroll
               for (int j = 0; j < 16; ++j) rv[j] = rn[j];
             }
             if (p.gn_part != nullptr) {
               if (c0 == c_begin) kshift = v[0];
-              float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float dv = (j < nvalid) ? v[j] - kshift : 0.f;
-                a1[j & 3] += dv;
-                a2[j & 3] = fmaf(dv, dv, a2[j & 3]);
-              }
-              s1 += (a1[0] + a1[1]) + (a1[2] + a1[3]);
-              s2 += (a2[0] + a2[1]) + (a2[2] + a2[3]);
-              cnt += static_cast<float>(nvalid);
+              gn_sums16(v, nvalid, kshift, s1, s2, cnt);
             }
             // the previous store from this buffer has finished reading it
             if (lane == 0) bulk_wait_group_read0();
