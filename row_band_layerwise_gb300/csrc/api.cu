@@ -121,6 +121,10 @@ struct vaedec {
   void* attn_p = nullptr;
   float* attn_l = nullptr;
   size_t s_elems = 0, l_elems = 0;
+  // attention pipeline: each band's softmax runs on `side` while the next band's score GEMM runs on
+  // the decode stream; scores, probabilities and row sums have two slots (events order them)
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_s[2] = {}, ev_p[2] = {};
   GnPartial* gn_part = nullptr;
   size_t part_elems = 0;
   float* gn_scale = nullptr;
@@ -153,6 +157,9 @@ struct vaedec {
   }
   ~vaedec() {
     for (cudaEvent_t e : prof_ev) cudaEventDestroy(e);
+    for (cudaEvent_t e : {ev_fork, ev_join, ev_s[0], ev_s[1], ev_p[0], ev_p[1]})
+      if (e != nullptr) cudaEventDestroy(e);
+    if (side != nullptr) cudaStreamDestroy(side);
     for (void* p : allocs) cudaFree(p);
   }
 };
@@ -700,8 +707,9 @@ class Walker {
       int maxrows = 0;
       for (int r : band_rows(x.H, n_bands_)) maxrows = std::max(maxrows, r);
       plan->s = std::max(plan->s, (size_t)maxrows * (size_t)x.W * (size_t)Ntok);
-      if (pv_splits(Ntok) > 1)   // fp32 partials of the split probabilities x values product
-        plan->s = std::max(plan->s, (size_t)pv_splits(Ntok) * (size_t)maxrows * (size_t)x.W * (size_t)C);
+      if (pv_splits(Ntok) > 1)   // fp32 partials of the split probabilities x values product, in one
+                                 // fp16 score slot (half of the scores buffer)
+        plan->s = std::max(plan->s, 2 * (size_t)pv_splits(Ntok) * (size_t)maxrows * (size_t)x.W * (size_t)C);
       plan->l = std::max(plan->l, (size_t)maxrows * x.W);
     }
     note_act(y);
@@ -781,6 +789,56 @@ class Walker {
         vview.cout = C;
         const float scale = 1.f / std::sqrt((float)C);
         const bool tc = h_->dtype == kBF16;
+        // tensor-core path, pipelined over bands: S(b) on the decode stream, softmax(b) on the side
+        // stream (slot b % 2) while S(b + 1) runs, then P(b) x V on the decode stream
+        const bool overlap = tc && h_->side != nullptr;
+        cudaStream_t sm_st = overlap ? h_->side : st_;
+        struct Band {
+          int f, nr, slot;
+          size_t qoff;
+          void* o_band;
+        };
+        bool have_pend = false;
+        Band pend{};
+        auto s_slot = [&](int slot) { return static_cast<void*>(reinterpret_cast<char*>(h_->attn_s) + slot * h_->s_elems * 2); };
+        auto p_slot = [&](int slot) { return static_cast<void*>(static_cast<char*>(h_->attn_p) + slot * h_->s_elems * oes); };
+        auto l_slot = [&](int slot) { return h_->attn_l + slot * h_->l_elems; };
+        auto run_pv = [&](const Band& bd) {
+          if (!live()) return;
+          if (overlap) check(cudaStreamWaitEvent(st_, h_->ev_p[bd.slot], 0), "attention join");
+          // O[q, c] = inv_l[q] * (V^T P^T)[c, q], channels on the lanes, keys split
+          const int splits = pv_splits(Ntok);
+          GemmArgs pa;
+          pa.A = static_cast<char*>(h_->attn_vt) + (size_t)bd.f * C * Ntok * oes;
+          pa.lda = Ntok;
+          pa.B = p_slot(bd.slot);
+          pa.ldb = Ntok;
+          pa.M = C;
+          pa.N = bd.nr;
+          pa.K = (int)Ntok;
+          pa.ldo = C;
+          pa.scale_n = l_slot(bd.slot);
+          pa.splits = splits;
+          if (splits > 1) {
+            pa.out = s_slot(bd.slot);   // fp32 partials; this band's scores are no longer needed
+            pa.out_f32 = 1;
+            pa.split_stride = (long long)bd.nr * C;
+            gemm(pa, "attention pv");
+            count();
+            check(launch_splitk_reduce(static_cast<const float*>(s_slot(bd.slot)), splits, (long long)bd.nr * C,
+                                       (long long)bd.nr * C, odt_, bd.o_band, st_),
+                  "attention pv reduce");
+          } else {
+            pa.out = bd.o_band;
+            pa.out_f32 = odt_ == kF32;
+            gemm(pa, "attention pv");
+          }
+        };
+        if (overlap) {
+          check(cudaEventRecord(h_->ev_fork, st_), "attention fork");
+          check(cudaStreamWaitEvent(h_->side, h_->ev_fork, 0), "attention fork");
+        }
+        int seq = 0;
         for (int f = 0; f < F && live(); ++f) {
           int r0 = 0;
           for (int band = 0; band < n_bands_ && live(); ++band) {
@@ -788,6 +846,7 @@ class Walker {
             const size_t qoff = ((size_t)f * Ntok + (size_t)r0 * x.W) * C;
             void* o_band = static_cast<char*>(ptr(hn)) + qoff * oes;   // O overwrites the band's normalised rows
             if (tc) {
+              const int slot = seq & 1;
               // S[q, key] = (K Q^T)[key, q] / sqrt(C), keys on the accumulator lanes, stored fp16
               GemmArgs sa;
               sa.A = static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes;
@@ -797,41 +856,24 @@ class Walker {
               sa.M = (int)Ntok;
               sa.N = nr;
               sa.K = C;
-              sa.out = h_->attn_s;
+              sa.out = s_slot(slot);
               sa.ldo = Ntok;
               sa.out_f32 = 0;
               sa.out_f16 = 1;
               sa.scale = scale;
               gemm(sa, "attention scores");
               count();
-              check(launch_softmax_rows(odt_, h_->attn_s, 1, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
-              // O[q, c] = inv_l[q] * (V^T P^T)[c, q], channels on the lanes, keys split
-              const int splits = pv_splits(Ntok);
-              GemmArgs pa;
-              pa.A = static_cast<char*>(h_->attn_vt) + (size_t)f * C * Ntok * oes;
-              pa.lda = Ntok;
-              pa.B = h_->attn_p;
-              pa.ldb = Ntok;
-              pa.M = C;
-              pa.N = nr;
-              pa.K = (int)Ntok;
-              pa.ldo = C;
-              pa.scale_n = h_->attn_l;
-              pa.splits = splits;
-              if (splits > 1) {
-                pa.out = h_->attn_s;   // fp32 partials; the scores are no longer needed
-                pa.out_f32 = 1;
-                pa.split_stride = (long long)nr * C;
-                gemm(pa, "attention pv");
-                count();
-                check(launch_splitk_reduce(static_cast<const float*>(h_->attn_s), splits, (long long)nr * C,
-                                           (long long)nr * C, odt_, o_band, st_),
-                      "attention pv reduce");
-              } else {
-                pa.out = o_band;
-                pa.out_f32 = odt_ == kF32;
-                gemm(pa, "attention pv");
+              if (overlap) {
+                check(cudaEventRecord(h_->ev_s[slot], st_), "attention scores event");
+                check(cudaStreamWaitEvent(h_->side, h_->ev_s[slot], 0), "attention scores event");
               }
+              check(launch_softmax_rows(odt_, s_slot(slot), 1, p_slot(slot), l_slot(slot), nr, (int)Ntok, sm_st),
+                    "softmax");
+              if (overlap) check(cudaEventRecord(h_->ev_p[slot], h_->side), "attention softmax event");
+              if (have_pend) run_pv(pend);
+              pend = Band{f, nr, slot, qoff, o_band};
+              have_pend = true;
+              ++seq;
             } else {
               ConvGeom gs;
               std::memset(&gs, 0, sizeof(gs));
@@ -866,6 +908,12 @@ class Walker {
             }
             r0 += rows[band];
           }
+        }
+        if (have_pend) run_pv(pend);
+        if (overlap) {
+          // the side stream's work is part of this op: join it back (also after a stop)
+          check(cudaEventRecord(h_->ev_join, h_->side), "attention join");
+          check(cudaStreamWaitEvent(st_, h_->ev_join, 0), "attention join");
         }
         // output projection + residual in fp32
         ConvGeom gp = g;
@@ -1333,8 +1381,8 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
   void* tmp = nullptr;
   if (s == VAEDEC_OK) s = h->dalloc(&tmp, plan.s * sizeof(float), "attention scores");
   h->attn_s = static_cast<float*>(tmp);
-  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_p, plan.s * h->es, "attention probabilities");
-  if (s == VAEDEC_OK) s = h->dalloc(&tmp, plan.l * sizeof(float), "attention row sums");
+  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_p, 2 * plan.s * h->es, "attention probabilities");
+  if (s == VAEDEC_OK) s = h->dalloc(&tmp, 2 * plan.l * sizeof(float), "attention row sums");
   h->attn_l = static_cast<float*>(tmp);
   h->s_elems = plan.s;
   h->l_elems = plan.l;
@@ -1351,7 +1399,13 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
   if (s != VAEDEC_OK) return bail(s);
   cudaError_t e = cudaMemset(h->status, 0, sizeof(int));
   if (e != cudaSuccess) return bail(cuda_fail(e, "status init"));
-  h->ws_bytes = kNumAct * plan.act + 3 * plan.qkv + plan.s * (4 + h->es) + plan.l * 4 + plan.part * sizeof(GnPartial) +
+  if (s == VAEDEC_OK && plan.s > 0) {
+    cudaError_t es = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_join, &h->ev_s[0], &h->ev_s[1], &h->ev_p[0], &h->ev_p[1]})
+      if (es == cudaSuccess) es = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (es != cudaSuccess) return bail(cuda_fail(es, "attention stream"));
+  }
+  h->ws_bytes = kNumAct * plan.act + 3 * plan.qkv + plan.s * (4 + 2 * h->es) + plan.l * 8 + plan.part * sizeof(GnPartial) +
                 2 * plan.sc * 4 + h->io_latent_bytes + h->io_out_bytes;
   *out = h;
   return VAEDEC_OK;
