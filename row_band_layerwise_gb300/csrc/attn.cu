@@ -8,6 +8,8 @@
 #include <cuda_fp16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
+#include "launch.h"
 
 namespace vd {
 
@@ -68,6 +70,8 @@ __device__ __forceinline__ float4 load_s4(const __half* p) {
 template <typename SIn, typename P>
 __global__ void __launch_bounds__(kSmThreads) softmax_rows_kernel(const SIn* __restrict__ S, P* __restrict__ Pm,
                                                                   float* __restrict__ inv_l, int nk) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
   __shared__ float red[32];
   const long long row = blockIdx.x;
   const SIn* s = S + row * nk;
@@ -107,6 +111,8 @@ __device__ __forceinline__ float store_p4<__nv_bfloat16>(__nv_bfloat16* p, float
 template <typename SIn, typename P, int NV>
 __global__ void __launch_bounds__(kSmThreads) softmax_rows_reg_kernel(const SIn* __restrict__ S, P* __restrict__ Pm,
                                                                       float* __restrict__ inv_l, int nk) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
   __shared__ float red[32];
   const long long row = blockIdx.x;
   const SIn* srow = S + row * nk;
@@ -143,6 +149,8 @@ __global__ void __launch_bounds__(kSmThreads) softmax_rows_reg_kernel(const SIn*
 template <typename T>
 __global__ void to_channels_last_kernel(const T* __restrict__ x, T* __restrict__ y, int C, long long spatial,
                                         long long total) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int c = static_cast<int>(i % C);
@@ -159,6 +167,8 @@ __global__ void to_channels_last_kernel(const T* __restrict__ x, T* __restrict__
 template <typename P, int NV>
 __global__ void __launch_bounds__(kSmThreads) softmax_rows_h8_kernel(const __half* __restrict__ S, P* __restrict__ Pm,
                                                                      float* __restrict__ inv_l, int nk) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
   __shared__ float red[32];
   const long long row = blockIdx.x;
   const uint4* s8 = reinterpret_cast<const uint4*>(S + row * nk);
@@ -208,10 +218,10 @@ cudaError_t softmax_rows_t(int p_dtype, const SIn* S, void* P, float* inv_l, int
 #define VD_SOFTMAX_REG(NV)                                                                                         \
   if (nv <= NV) {                                                                                                  \
     if (bf)                                                                                                        \
-      softmax_rows_reg_kernel<SIn, __nv_bfloat16, NV>                                                              \
-          <<<rows, kSmThreads, 0, stream>>>(S, static_cast<__nv_bfloat16*>(P), inv_l, nk);                         \
+      launch_pdl(softmax_rows_reg_kernel<SIn, __nv_bfloat16, NV>,                                                              \
+          rows, kSmThreads, 0, stream, S, static_cast<__nv_bfloat16*>(P), inv_l, nk);                         \
     else                                                                                                           \
-      softmax_rows_reg_kernel<SIn, float, NV><<<rows, kSmThreads, 0, stream>>>(S, static_cast<float*>(P), inv_l, nk); \
+      launch_pdl(softmax_rows_reg_kernel<SIn, float, NV>, rows, kSmThreads, 0, stream, S, static_cast<float*>(P), inv_l, nk); \
     return cudaGetLastError();                                                                                     \
   }
     VD_SOFTMAX_REG(2)
@@ -221,10 +231,10 @@ cudaError_t softmax_rows_t(int p_dtype, const SIn* S, void* P, float* inv_l, int
 #undef VD_SOFTMAX_REG
   }
   if (bf)
-    softmax_rows_kernel<SIn, __nv_bfloat16><<<rows, kSmThreads, 0, stream>>>(S, static_cast<__nv_bfloat16*>(P), inv_l,
+    launch_pdl(softmax_rows_kernel<SIn, __nv_bfloat16>, rows, kSmThreads, 0, stream, S, static_cast<__nv_bfloat16*>(P), inv_l,
                                                                              nk);
   else
-    softmax_rows_kernel<SIn, float><<<rows, kSmThreads, 0, stream>>>(S, static_cast<float*>(P), inv_l, nk);
+    launch_pdl(softmax_rows_kernel<SIn, float>, rows, kSmThreads, 0, stream, S, static_cast<float*>(P), inv_l, nk);
   return cudaGetLastError();
 }
 
@@ -240,10 +250,10 @@ cudaError_t launch_softmax_rows(int p_dtype, const void* S, int s_f16, void* P, 
 #define VD_SOFTMAX_H8(NV)                                                                                     \
   if (nv <= NV) {                                                                                             \
     if (bf)                                                                                                   \
-      softmax_rows_h8_kernel<__nv_bfloat16, NV>                                                               \
-          <<<rows, kSmThreads, 0, stream>>>(sh, static_cast<__nv_bfloat16*>(P), inv_l, nk);                   \
+      launch_pdl(softmax_rows_h8_kernel<__nv_bfloat16, NV>,                                                               \
+          rows, kSmThreads, 0, stream, sh, static_cast<__nv_bfloat16*>(P), inv_l, nk);                   \
     else                                                                                                      \
-      softmax_rows_h8_kernel<float, NV><<<rows, kSmThreads, 0, stream>>>(sh, static_cast<float*>(P), inv_l, nk); \
+      launch_pdl(softmax_rows_h8_kernel<float, NV>, rows, kSmThreads, 0, stream, sh, static_cast<float*>(P), inv_l, nk); \
     return cudaGetLastError();                                                                                \
   }
     VD_SOFTMAX_H8(1)
@@ -264,10 +274,10 @@ cudaError_t launch_to_channels_last(int dtype, const void* x, void* y, int B, in
   long long blocks = (total + threads - 1) / threads;
   if (blocks > 152LL * 32) blocks = 152LL * 32;
   if (dtype == kBF16)
-    to_channels_last_kernel<__nv_bfloat16><<<(int)blocks, threads, 0, stream>>>(
+    launch_pdl(to_channels_last_kernel<__nv_bfloat16>, (int)blocks, threads, 0, stream, 
         static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), C, spatial, total);
   else
-    to_channels_last_kernel<float><<<(int)blocks, threads, 0, stream>>>(static_cast<const float*>(x),
+    launch_pdl(to_channels_last_kernel<float>, (int)blocks, threads, 0, stream, static_cast<const float*>(x),
                                                                        static_cast<float*>(y), C, spatial, total);
   return cudaGetLastError();
 }

@@ -28,6 +28,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tma_host.h"
+#include "launch.h"
 
 namespace vd {
 
@@ -129,6 +130,9 @@ __global__ void __launch_bounds__(kHaloThreads, 1) conv_halo_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the previous kernel on the stream has finished and its writes are visible from here on
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
   const int nac = p.ndt * p.n_kchunks;
 
@@ -381,15 +385,15 @@ cudaError_t launch_conv_halo(const ConvGeom& g, const void* in, const void* wts,
   switch (bk) {
     case 64:
       e = cudaFuncSetAttribute(conv_halo_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_halo_kernel<64><<<(unsigned)nblocks, kHaloThreads, smem, stream>>>(p);
+      if (e == cudaSuccess) launch_pdl(conv_halo_kernel<64>, (unsigned)nblocks, kHaloThreads, smem, stream, p);
       break;
     case 32:
       e = cudaFuncSetAttribute(conv_halo_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_halo_kernel<32><<<(unsigned)nblocks, kHaloThreads, smem, stream>>>(p);
+      if (e == cudaSuccess) launch_pdl(conv_halo_kernel<32>, (unsigned)nblocks, kHaloThreads, smem, stream, p);
       break;
     default:
       e = cudaFuncSetAttribute(conv_halo_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_halo_kernel<16><<<(unsigned)nblocks, kHaloThreads, smem, stream>>>(p);
+      if (e == cudaSuccess) launch_pdl(conv_halo_kernel<16>, (unsigned)nblocks, kHaloThreads, smem, stream, p);
       break;
   }
   if (e != cudaSuccess) return e;

@@ -31,6 +31,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tma_host.h"
+#include "launch.h"
 
 namespace vd {
 
@@ -257,6 +258,9 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the previous kernel on the stream has finished and its writes are visible from here on
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
   const int nac = p.ndt * p.n_kchunks;   // staged activation chunks per tile
   const int ngrp = nsp / 3;              // weight stages per chunk (kernel rows)
@@ -963,7 +967,7 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
   cudaError_t e;
   auto go = [&](auto kern) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (r == cudaSuccess) kern<<<(unsigned)nblocks, kThreadsT, smem, stream>>>(p);
+    if (r == cudaSuccess) launch_pdl(kern, (unsigned)nblocks, kThreadsT, smem, stream, p);
     return r;
   };
   switch (bk * 4 + p.tma_out) {

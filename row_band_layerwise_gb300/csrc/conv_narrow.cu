@@ -30,6 +30,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tma_host.h"
+#include "launch.h"
 
 namespace vd {
 
@@ -100,6 +101,9 @@ __global__ void __launch_bounds__(kThreadsN, 1) conv_narrow_kernel(const __grid_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the previous kernel on the stream has finished and its writes are visible from here on
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
 
   // tile t -> (tx, ty, frame, sample)
@@ -366,15 +370,15 @@ cudaError_t launch_conv_narrow(const ConvGeom& g, const void* in, const void* w_
   switch (bk) {
     case 64:
       e = cudaFuncSetAttribute(conv_narrow_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_narrow_kernel<64><<<grid, kThreadsN, smem, stream>>>(p);
+      if (e == cudaSuccess) launch_pdl(conv_narrow_kernel<64>, grid, kThreadsN, smem, stream, p);
       break;
     case 32:
       e = cudaFuncSetAttribute(conv_narrow_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_narrow_kernel<32><<<grid, kThreadsN, smem, stream>>>(p);
+      if (e == cudaSuccess) launch_pdl(conv_narrow_kernel<32>, grid, kThreadsN, smem, stream, p);
       break;
     default:
       e = cudaFuncSetAttribute(conv_narrow_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_narrow_kernel<16><<<grid, kThreadsN, smem, stream>>>(p);
+      if (e == cudaSuccess) launch_pdl(conv_narrow_kernel<16>, grid, kThreadsN, smem, stream, p);
       break;
   }
   if (e != cudaSuccess) return e;

@@ -7,6 +7,8 @@
 
 #include "conv.h"
 #include "kernels.h"
+#include "ptx.cuh"
+#include "launch.h"
 
 namespace vd {
 
@@ -14,6 +16,8 @@ __global__ void conv_simple_f32_kernel(const ConvGeom g, const float* __restrict
                                        const float* __restrict__ w, int ntaps_w, const float* __restrict__ bias,
                                        const float* __restrict__ residual, const float* __restrict__ rowscale,
                                        float* __restrict__ out, long long total) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     long long r = idx;
@@ -69,7 +73,7 @@ cudaError_t launch_conv_simple_f32(const ConvGeom& g, const float* in, const flo
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   const int grid = static_cast<int>(blocks < 152LL * 64 ? blocks : 152LL * 64);
-  conv_simple_f32_kernel<<<grid, threads, 0, stream>>>(g, in, wts, ntaps_w, bias, residual, rowscale, out, total);
+  launch_pdl(conv_simple_f32_kernel, grid, threads, 0, stream, g, in, wts, ntaps_w, bias, residual, rowscale, out, total);
   return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tma_host.h"
+#include "launch.h"
 
 namespace vd {
 
@@ -116,6 +117,9 @@ __global__ void __launch_bounds__(kThreads) conv_tc_kernel(const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the previous kernel on the stream has finished and its writes are visible from here on
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
 
   const int ksteps = g.ntaps * p.n_kchunks;
@@ -379,15 +383,15 @@ cudaError_t launch_conv_tc(const ConvGeom& g, const void* in, const void* wts, i
   switch (bk) {
     case 64:
       e = cudaFuncSetAttribute(conv_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_tc_kernel<64><<<(unsigned)nblocks, kThreads, smem, stream>>>(p);
+      if (e == cudaSuccess) launch_pdl(conv_tc_kernel<64>, (unsigned)nblocks, kThreads, smem, stream, p);
       break;
     case 32:
       e = cudaFuncSetAttribute(conv_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_tc_kernel<32><<<(unsigned)nblocks, kThreads, smem, stream>>>(p);
+      if (e == cudaSuccess) launch_pdl(conv_tc_kernel<32>, (unsigned)nblocks, kThreads, smem, stream, p);
       break;
     default:
       e = cudaFuncSetAttribute(conv_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) conv_tc_kernel<16><<<(unsigned)nblocks, kThreads, smem, stream>>>(p);
+      if (e == cudaSuccess) launch_pdl(conv_tc_kernel<16>, (unsigned)nblocks, kThreads, smem, stream, p);
       break;
   }
   if (e != cudaSuccess) return e;

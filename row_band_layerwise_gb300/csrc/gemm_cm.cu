@@ -28,6 +28,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tma_host.h"
+#include "launch.h"
 
 namespace vd {
 
@@ -135,6 +136,9 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the previous kernel on the stream has finished and its writes are visible from here on
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
 
   if (warp == 0) {
@@ -404,6 +408,8 @@ int round_up_g(int a, int b) { return (a + b - 1) / b * b; }
 template <typename O>
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, long long stride, long long n4,
                                      O* __restrict__ out) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
     float4 acc = reinterpret_cast<const float4*>(part)[i];
     for (int s = 1; s < splits; ++s) {
@@ -436,10 +442,10 @@ cudaError_t launch_splitk_reduce(const float* part, int splits, long long split_
   long long blocks = (n4 + 255) / 256;
   if (blocks > 152LL * 8) blocks = 152LL * 8;
   if (out_dtype == kBF16)
-    splitk_reduce_kernel<__nv_bfloat16><<<(int)blocks, 256, 0, stream>>>(part, splits, split_stride, n4,
+    launch_pdl(splitk_reduce_kernel<__nv_bfloat16>, (int)blocks, 256, 0, stream, part, splits, split_stride, n4,
                                                                           static_cast<__nv_bfloat16*>(out));
   else
-    splitk_reduce_kernel<float><<<(int)blocks, 256, 0, stream>>>(part, splits, split_stride, n4,
+    launch_pdl(splitk_reduce_kernel<float>, (int)blocks, 256, 0, stream, part, splits, split_stride, n4,
                                                                   static_cast<float*>(out));
   return cudaGetLastError();
 }
@@ -550,7 +556,7 @@ cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, 
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(std::min<long long>(ntiles, std::max(1, sms)));
-  gemm_cm_kernel<<<grid, kGThreads, smem, stream>>>(p);
+  launch_pdl(gemm_cm_kernel, grid, kGThreads, smem, stream, p);
   return cudaGetLastError();
 }
 

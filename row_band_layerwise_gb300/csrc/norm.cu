@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
+#include "launch.h"
 
 namespace vd {
 
@@ -98,6 +100,8 @@ template <typename T>
 __global__ void __launch_bounds__(kGnThreads) gn_partials_kernel(const T* __restrict__ x, int rows, int W, int C,
                                                                  int G, int chunk_rows, int n_chunks,
                                                                  GnPartial* __restrict__ part) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
   extern __shared__ float sh[];   // [nthreads][8][3]
   const int chunk = blockIdx.x, b = blockIdx.y;
   const int vpp = C / 8;                        // vectors per pixel
@@ -179,6 +183,8 @@ __global__ void __launch_bounds__(kFinThreads) gn_finalize_kernel(const GnPartia
                                                                   const float* __restrict__ beta, float eps,
                                                                   float* __restrict__ scale,
                                                                   float* __restrict__ shift) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
   __shared__ float sn[kFinThreads], sm[kFinThreads], s2[kFinThreads];
   const int b = blockIdx.x / G, g = blockIdx.x % G;
   const int t = threadIdx.x;
@@ -240,6 +246,8 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const Tin* __restrict__ x
                                                        uint32_t vec_per_sample, int C, int vpp_log2,
                                                        const float* __restrict__ scale,
                                                        const float* __restrict__ shift, int silu) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
   // 32-bit vector indices (the launcher guarantees nvec < 2^31); the channel of a vector is a
   // mask when C / 8 is a power of two (every GroupNorm width here), else a 32-bit remainder
   const uint32_t vpp = static_cast<uint32_t>(C / 8);
@@ -305,6 +313,8 @@ template <typename Tin, typename Tout, int V>
 __global__ void __launch_bounds__(256) rms_norm_kernel(const Tin* __restrict__ x, Tout* __restrict__ y,
                                                        Tout* __restrict__ y_raw, long long pixels, int C, int gs,
                                                        const float* __restrict__ gamma, int silu) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int j = lane & (gs - 1);          // position in the group
   const int ppw = 32 / gs;                // pixels per warp step
@@ -390,17 +400,17 @@ cudaError_t launch_gn_partials(int dtype, const void* x, int B, int rows, int W,
   dim3 grid(n_chunks, B);
   const size_t smem = kGnThreads * 24 * sizeof(float);
   if (dtype == kBF16)
-    gn_partials_kernel<__nv_bfloat16><<<grid, kGnThreads, smem, stream>>>(
+    launch_pdl(gn_partials_kernel<__nv_bfloat16>, grid, kGnThreads, smem, stream, 
         static_cast<const __nv_bfloat16*>(x), rows, W, C, G, chunk_rows, n_chunks, part);
   else
-    gn_partials_kernel<float><<<grid, kGnThreads, smem, stream>>>(static_cast<const float*>(x), rows, W, C, G,
+    launch_pdl(gn_partials_kernel<float>, grid, kGnThreads, smem, stream, static_cast<const float*>(x), rows, W, C, G,
                                                                   chunk_rows, n_chunks, part);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gn_finalize(const GnPartial* part, int B, int n_chunks, int C, int G, const float* gamma,
                                const float* beta, float eps, float* scale, float* shift, cudaStream_t stream) {
-  gn_finalize_kernel<<<B * G, kFinThreads, 0, stream>>>(part, B, n_chunks, C, G, gamma, beta, eps, scale, shift);
+  launch_pdl(gn_finalize_kernel, B * G, kFinThreads, 0, stream, part, B, n_chunks, C, G, gamma, beta, eps, scale, shift);
   return cudaGetLastError();
 }
 
@@ -411,7 +421,7 @@ void gn_apply_t(const void* x, void* y, void* y_raw, long long nvec, long long v
   const int vpp = C / 8;
   const int vpp_log2 = (vpp & (vpp - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(vpp)) : -1;
   static const int occ = blocks_per_sm(gn_apply_kernel<Tin, Tout>, threads);
-  gn_apply_kernel<Tin, Tout><<<grid_for(nvec, threads, occ), threads, 0, stream>>>(
+  launch_pdl(gn_apply_kernel<Tin, Tout>, grid_for(nvec, threads, occ), threads, 0, stream, 
       static_cast<const Tin*>(x), static_cast<Tout*>(y), static_cast<Tout*>(y_raw), static_cast<uint32_t>(nvec),
       static_cast<uint32_t>(vps), C, vpp_log2, scale, shift, silu);
 }
@@ -440,7 +450,7 @@ void rms_launch(const Tin* x, Tout* y, Tout* y_raw, long long warps, long long p
                 const float* gamma, int silu, cudaStream_t stream) {
   const int threads = 256;
   static const int occ = blocks_per_sm(rms_norm_kernel<Tin, Tout, V>, threads);
-  rms_norm_kernel<Tin, Tout, V><<<grid_for(warps * 32, threads, occ), threads, 0, stream>>>(x, y, y_raw, pixels, C, gs,
+  launch_pdl(rms_norm_kernel<Tin, Tout, V>, grid_for(warps * 32, threads, occ), threads, 0, stream, x, y, y_raw, pixels, C, gs,
                                                                                             gamma, silu);
 }
 

@@ -120,6 +120,13 @@ __device__ __forceinline__ bool bar_sync_or(int id, int count, bool v) {
   return r != 0;
 }
 
+// Programmatic dependent launch.  Every kernel of this library is launched so that it may start while
+// the previous kernel on its stream is still finishing; it calls pdl_wait() before its first access to
+// global memory (the wait returns once the previous grid has completed and its writes are visible),
+// and pdl_trigger() to let the next kernel start its own prologue early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
