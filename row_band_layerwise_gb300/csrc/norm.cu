@@ -168,14 +168,14 @@ __global__ void __launch_bounds__(kGnThreads) gn_partials_kernel(const T* __rest
 }
 
 // One CTA per (sample, group), in one pass over the chunk moments.  Thread t folds
-// chunks t, t + 512, ... in order into (n, mean, M2) with the two-part form of the
+// chunks t, t + 1024, ... in order into (n, mean, M2) with the two-part form of the
 // weighted rule (for parts a, b: mean = w_a mean_a + w_b mean_b and
 // M2 = M2_a + M2_b + (mean_b - mean_a)^2 n_a n_b / n, which is the rule
-// var = sum w_i (var_i + (mean_i - mean)^2) for two parts times n); the 512
+// var = sum w_i (var_i + (mean_i - mean)^2) for two parts times n); the 1024
 // thread results are then combined with the same two-part rule along a fixed
 // tree.  Every step is fixed by the chunk geometry, so the result does not
 // depend on how the tensor was produced (band count, tile order).
-constexpr int kFinThreads = 512;
+constexpr int kFinThreads = 1024;   // with eight loads in flight per thread: one pass of latency
 
 __global__ void __launch_bounds__(kFinThreads) gn_finalize_kernel(const GnPartial* __restrict__ part, int B,
                                                                   int n_chunks, int C, int G,
@@ -191,13 +191,13 @@ __global__ void __launch_bounds__(kFinThreads) gn_finalize_kernel(const GnPartia
   const GnPartial* pp = part + ((long long)b * G + g) * n_chunks;   // [sample][group][chunk]
   float n = 0.f, mean = 0.f, m2 = 0.f;
   int c = t;
-  // four loads in flight per step, folded in chunk order
-  for (; c + 3 * kFinThreads < n_chunks; c += 4 * kFinThreads) {
-    GnPartial e[4];
+  // eight loads in flight per step, folded in chunk order
+  for (; c + 7 * kFinThreads < n_chunks; c += 8 * kFinThreads) {
+    GnPartial e[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) e[i] = pp[c + i * kFinThreads];
+    for (int i = 0; i < 8; ++i) e[i] = pp[c + i * kFinThreads];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) merge_into(n, mean, m2, e[i].n, e[i].mean, e[i].m2);
+    for (int i = 0; i < 8; ++i) merge_into(n, mean, m2, e[i].n, e[i].mean, e[i].m2);
   }
   for (; c < n_chunks; c += kFinThreads) {
     const GnPartial e = pp[c];
