@@ -28,7 +28,10 @@ from the adjacent bands and zero padding only at the global top/bottom edge
 merges them with the element-count-weighted rule (section GroupNorm：合并全局统计量);
 attention keeps Q band-local and attends over K/V gathered from all bands
 (section Attention：本地 Q，全局 K/V); pointwise ops, channel RMSNorm and
-nearest upsample run per band.
+nearest upsample run per band.  The same algorithm runs over width column bands
+(the pages' second spatial split axis, "Parallel modes": spatial_shard_width):
+halo columns from the left/right neighbours, zero padding only at the global
+left/right edge, height padded as in the original.
 
 TEST INFRASTRUCTURE ONLY: see the package docstring.
 """
@@ -39,6 +42,29 @@ from typing import Dict, List, Optional, Sequence, Tuple
 import numpy as np
 
 from . import ops
+
+
+def band_axis(h: int, w: int, n_bands: int, axis: str) -> str:
+    """The split axis a request gets: "height", "width", or for "auto" the longer latent axis
+    that can hold every band (at least one latent row or column each), width winning ties
+    ("Parallel modes", auto: the longer axis that can cover every rank, width wins ties).
+    Raises ValueError when the requested axis (or, for auto, neither axis) can hold n_bands."""
+    if n_bands < 1:
+        raise ValueError("n_bands must be >= 1")
+    if axis == "height":
+        if n_bands > h:
+            raise ValueError(f"n_bands={n_bands} exceeds the latent height {h}")
+        return axis
+    if axis == "width":
+        if n_bands > w:
+            raise ValueError(f"n_bands={n_bands} exceeds the latent width {w}")
+        return axis
+    if axis != "auto":
+        raise ValueError(axis)
+    fits = [a for a, n in (("width", w), ("height", h)) if n >= n_bands]
+    if not fits:
+        raise ValueError(f"neither axis ({h} x {w}) can hold {n_bands} bands")
+    return max(fits, key=lambda a: w if a == "width" else h)   # first maximum: width on ties
 
 
 def band_rows(h: int, n_bands: int) -> List[int]:
@@ -100,54 +126,67 @@ class Dense:
 
 
 class Banded:
-    """The pages' layer-wise algorithm over height row bands."""
+    """The pages' layer-wise algorithm over height row bands or width column bands."""
 
-    def __init__(self, n_bands: int):
+    def __init__(self, n_bands: int, axis: str = "height"):
+        if axis not in ("height", "width"):
+            raise ValueError(axis)
         self.n_bands = n_bands
+        self.ax = -2 if axis == "height" else -1
 
     def split(self, z):
         z = ops._f64(z)
-        rows = band_rows(z.shape[-2], self.n_bands)
+        sizes = band_rows(z.shape[self.ax], self.n_bands)
         out, y = [], 0
-        for r in rows:
-            out.append(z[..., y:y + r, :].copy())
+        for r in sizes:
+            sl = [slice(None)] * z.ndim
+            sl[self.ax] = slice(y, y + r)
+            out.append(z[tuple(sl)].copy())
             y += r
         return out
 
     def join(self, xs):
-        return np.concatenate(xs, axis=-2)
+        return np.concatenate(xs, axis=self.ax)
 
     def conv(self, xs, w, b):
-        """Each band convolves [top halo, own rows, bottom halo] with no height padding.
+        """Each band convolves [halo, own rows or columns, halo] with no padding along the split axis.
 
-        The halo is the kernel radius (k_h - 1) / 2 rows of the neighbouring
-        band; at the global top and bottom edge it is zeros (the original
-        padding).  Width keeps its original zero padding.
+        The halo is the kernel radius of the neighbouring band along the split
+        axis; at the global edge it is zeros (the original padding).  The other
+        spatial axis keeps its original zero padding.
         """
         w = np.asarray(w)
         kh, kw = w.shape[-2], w.shape[-1]
         if kh % 2 != 1 or kw % 2 != 1:
             raise ValueError("banded conv needs centred odd kernels")
-        r = kh // 2
-        pw = kw // 2
+        ax = self.ax
+        r = (kh if ax == -2 else kw) // 2
+        pad = (0, 0, kw // 2, kw // 2) if ax == -2 else (kh // 2, kh // 2, 0, 0)
+
+        def take(a, lo, hi):
+            sl = [slice(None)] * a.ndim
+            sl[ax] = slice(lo, hi)
+            return a[tuple(sl)]
+
         outs = []
         for i, xb in enumerate(xs):
-            if r > 0 and xb.shape[-2] < r:
+            if r > 0 and xb.shape[ax] < r:
                 raise ValueError("band smaller than the conv halo")
-            zshape = xb.shape[:-2] + (r, xb.shape[-1])
-            top = xs[i - 1][..., -r:, :] if (i > 0 and r > 0) else np.zeros(zshape)
-            bot = xs[i + 1][..., :r, :] if (i + 1 < len(xs) and r > 0) else np.zeros(zshape)
-            xin = np.concatenate([top, xb, bot], axis=-2) if r > 0 else xb
+            zshape = list(xb.shape)
+            zshape[ax] = r
+            lo = take(xs[i - 1], -r, None) if (i > 0 and r > 0) else np.zeros(zshape)
+            hi = take(xs[i + 1], 0, r) if (i + 1 < len(xs) and r > 0) else np.zeros(zshape)
+            xin = np.concatenate([lo, xb, hi], axis=ax) if r > 0 else xb
             if w.ndim == 5:
-                y = ops.causal_conv3d(xin, w, b, pad_hw=(0, 0, pw, pw))
+                y = ops.causal_conv3d(xin, w, b, pad_hw=pad)
             elif xin.ndim == 5:
                 n, c, t, h, wd = xin.shape
                 xf = xin.transpose(0, 2, 1, 3, 4).reshape(n * t, c, h, wd)
-                y = ops.conv2d(xf, w, b, (0, 0, pw, pw))
+                y = ops.conv2d(xf, w, b, pad)
                 y = y.reshape(n, t, -1, y.shape[-2], y.shape[-1]).transpose(0, 2, 1, 3, 4)
             else:
-                y = ops.conv2d(xin, w, b, (0, 0, pw, pw))
-            assert y.shape[-2] == xb.shape[-2]
+                y = ops.conv2d(xin, w, b, pad)
+            assert y.shape[ax] == xb.shape[ax]
             outs.append(y)
         return outs
 
@@ -320,9 +359,12 @@ def decode_wan3d(arch, W: Dict[str, np.ndarray], z: np.ndarray, ex) -> np.ndarra
 
 
 def decode(arch, W: Dict[str, np.ndarray], z: np.ndarray,
-           n_bands: Optional[int] = None) -> np.ndarray:
-    """Decode ``z`` in float64; unbanded when ``n_bands`` is None, else banded."""
-    ex = Dense() if n_bands is None else Banded(n_bands)
+           n_bands: Optional[int] = None, axis: str = "height") -> np.ndarray:
+    """Decode ``z`` in float64; unbanded when ``n_bands`` is None, else banded along ``axis``
+    ("height", "width" or "auto", see band_axis)."""
+    if n_bands is not None:
+        axis = band_axis(z.shape[-2], z.shape[-1], n_bands, axis)
+    ex = Dense() if n_bands is None else Banded(n_bands, axis)
     if arch.family == "kl2d":
         return decode_kl2d(arch, W, z, ex)
     if arch.family == "wan3d":

@@ -216,3 +216,58 @@ def test_too_many_bands_rejected():
     W, z, _ = None, synth.make_latent((1, 16, 3, 4), "fp32"), None
     with pytest.raises(ValueError):
         decoder.decode(KL_SMALL, synth.make_weights(KL_SMALL, "fp32"), z, 4)
+
+
+# ---- width column bands (the pages' second spatial split axis) -------------------------------
+@pytest.mark.parametrize("n_bands", [2, 3])
+def test_kl_width_banded_equals_unbanded(kl_small, n_bands):
+    W, z, y = kl_small
+    yb = decoder.decode(KL_SMALL, W, z, n_bands, axis="width")
+    np.testing.assert_allclose(yb, y, rtol=0, atol=1e-12 * np.abs(y).max())
+
+
+def test_wan_width_banded_equals_unbanded(wan_small):
+    W, z, y = wan_small
+    yb = decoder.decode(WAN_SMALL, W, z, 2, axis="width")
+    np.testing.assert_allclose(yb, y, rtol=0, atol=1e-12 * np.abs(y).max())
+
+
+def test_width_banded_conv_needs_the_column_halo():
+    """Zero padding at an interior column cut differs from the whole conv near the cut; the
+    banded conv with neighbour columns as halo equals it."""
+    W = synth.make_weights(KL_SMALL, "fp32", seed=5)
+    x = synth.make_latent((1, 16, 5, 6), "fp32", seed=9).astype(np.float64)
+    from oracle import ops
+    w, b = W["conv_in.weight"], W["conv_in.bias"]
+    whole = ops.conv2d_same(x, w, b)
+    cut = np.concatenate([ops.conv2d_same(x[..., :3], w, b), ops.conv2d_same(x[..., 3:], w, b)], axis=-1)
+    ex = decoder.Banded(2, "width")
+    halo = ex.join(ex.conv(ex.split(x), w, b))
+    assert np.abs(cut - whole)[..., 2:4].max() > 1e-3
+    np.testing.assert_allclose(halo, whole, rtol=0, atol=1e-13)
+
+
+def test_width_bands_take_the_remainder_first():
+    ex = decoder.Banded(3, "width")
+    parts = ex.split(np.zeros((1, 2, 4, 136)))
+    assert [p.shape[-1] for p in parts] == [46, 45, 45]
+
+
+@pytest.mark.parametrize("h,w,n,axis,want", [
+    (128, 128, 8, "auto", "width"),      # square: width wins the tie
+    (100, 136, 3, "auto", "width"),      # the longer axis
+    (136, 100, 3, "auto", "height"),
+    (20, 3, 4, "auto", "height"),        # width cannot hold 4 bands
+    (3, 20, 4, "auto", "width"),
+    (16, 16, 4, "height", "height"),
+    (16, 16, 4, "width", "width"),
+])
+def test_band_axis_rule(h, w, n, axis, want):
+    assert decoder.band_axis(h, w, n, axis) == want
+
+
+@pytest.mark.parametrize("h,w,n,axis", [(3, 3, 4, "auto"), (3, 20, 4, "height"), (20, 3, 4, "width"),
+                                        (8, 8, 0, "auto"), (8, 8, 2, "diagonal")])
+def test_band_axis_rejects(h, w, n, axis):
+    with pytest.raises(ValueError):
+        decoder.band_axis(h, w, n, axis)
