@@ -127,6 +127,33 @@ vaedec_status vaedec_decode(vaedec_t* h, const void* latent, const int64_t* late
                             int n_bands, void* stream);
 
 /*
+ * Band split axis ("VAE Parallel", Strategy Selection Contract: spatial_shard_height,
+ * spatial_shard_width, auto).  On one GPU a band only decides which queries one attention pass
+ * holds; no result depends on the axis or the band count.
+ */
+enum { VAEDEC_BANDS_HEIGHT = 0, VAEDEC_BANDS_WIDTH = 1, VAEDEC_BANDS_AUTO = 2 };
+
+/*
+ * The axis a request is split along ("VAE Parallel", Spatially-Sharded Decode): HEIGHT or WIDTH as
+ * asked when that latent axis holds n_bands bands (at least one latent row or column each); AUTO:
+ * the longer latent axis that can, width on ties.  latent_shape as for vaedec_decode (only its last
+ * two entries, H and W, are read).  *axis_out receives VAEDEC_BANDS_HEIGHT or VAEDEC_BANDS_WIDTH.
+ * Host only, no handle or device needed.  Errors: INVALID_ARG (NULL pointer, ndim not 4 or 5,
+ * unknown axis, n_bands < 1, or no allowed axis can hold n_bands).
+ */
+vaedec_status vaedec_band_axis(const int64_t* latent_shape, int ndim, int n_bands, int axis, int* axis_out);
+
+/*
+ * vaedec_decode with the band split axis `axis` (VAEDEC_BANDS_*; AUTO resolved as in
+ * vaedec_band_axis).  Width band b holds floor(W/n) latent columns, the first W mod n bands one
+ * more; its queries are gathered into a dense buffer and its attention output scattered back.  The
+ * output is bit-identical for every axis and band count.  Same arguments, ownership and errors as
+ * vaedec_decode (n_bands must fit the chosen axis).
+ */
+vaedec_status vaedec_decode_bands(vaedec_t* h, const void* latent, const int64_t* latent_shape, int ndim, void* out,
+                                  int n_bands, int axis, void* stream);
+
+/*
  * Same as vaedec_decode with HOST buffers: copies the latent host->device, decodes,
  * copies the output device->host, and synchronises `stream` before returning.
  * Host buffers should be pinned for full copy bandwidth.  Also reports kernel-side

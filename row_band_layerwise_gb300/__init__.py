@@ -17,6 +17,7 @@ import numpy as np
 from .build import lib_path
 
 __all__ = ["Decoder", "VaedecError", "load_library", "EXPORTED_SYMBOLS", "STATUS_NAMES", "inject_fault",
+           "band_axis", "BAND_AXES",
            "set_wait_limit"]
 
 FAMILY = {"kl2d": 1, "wan3d": 2}
@@ -30,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "vaedec_launch_count", "vaedec_profile_enable", "vaedec_profile_read",
     "vaedec_debug_num_ops", "vaedec_debug_op_desc", "vaedec_debug_run_until",
     "vaedec_groupnorm_noalloc", "vaedec_debug_inject_fault", "vaedec_debug_set_wait_limit",
-    "vaedec_debug_wait_probe",
+    "vaedec_debug_wait_probe", "vaedec_band_axis", "vaedec_decode_bands",
 )
 
 
@@ -92,6 +93,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.vaedec_debug_inject_fault.argtypes = [i, i]
     lib.vaedec_debug_set_wait_limit.argtypes = [ctypes.c_uint64]
     lib.vaedec_debug_wait_probe.argtypes = [vp, vp]
+    lib.vaedec_band_axis.argtypes = [i64p, i, i, i, ctypes.POINTER(i)]
+    lib.vaedec_decode_bands.argtypes = [vp, vp, i64p, i, vp, i, i, vp]
     for name in EXPORTED_SYMBOLS:
         if name not in ("vaedec_destroy", "vaedec_last_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -152,6 +155,20 @@ def set_wait_limit(ns: int) -> None:
     """Set the limit of the kernels' bounded waits in nanoseconds (0 restores the default)."""
     lib = load_library()
     _check(lib, lib.vaedec_debug_set_wait_limit(int(ns)))
+
+
+BAND_AXES = {"height": 0, "width": 1, "auto": 2}
+
+
+def band_axis(latent_shape, n_bands: int, axis: str = "auto") -> str:
+    """The axis ("height" or "width") a decode of ``latent_shape`` in ``n_bands`` bands is split
+    along for the requested ``axis`` (vaedec_band_axis: auto takes the longer latent axis that can
+    hold every band, width on ties).  Host only."""
+    lib = load_library()
+    out = ctypes.c_int(-1)
+    _check(lib, lib.vaedec_band_axis(_shape_arg(latent_shape), len(latent_shape), int(n_bands),
+                                     BAND_AXES[axis], ctypes.byref(out)))
+    return "height" if out.value == 0 else "width"
 
 
 def groupnorm_noalloc(x, y, groups: int, gamma, beta, eps: float, silu: bool, stream=None) -> None:
@@ -243,8 +260,9 @@ class Decoder:
         return int(stream.cuda_stream)
 
     # ------------------------------------------------------------------ decode
-    def decode(self, latent, n_bands: int, out=None, stream=None):
-        """Decode a device latent (torch tensor, channels-first, model dtype) on ``stream``."""
+    def decode(self, latent, n_bands: int, out=None, stream=None, axis: str = "height"):
+        """Decode a device latent (torch tensor, channels-first, model dtype) on ``stream``, split
+        into ``n_bands`` bands along ``axis`` ("height", "width" or "auto"; see band_axis)."""
         torch = _torch()
         if not latent.is_cuda or latent.dtype != self.torch_dtype or not latent.is_contiguous():
             raise ValueError("latent must be a contiguous CUDA tensor in the model dtype")
@@ -253,9 +271,14 @@ class Decoder:
             out = torch.empty(oshape, dtype=self.torch_dtype, device=latent.device)
         elif tuple(out.shape) != oshape or out.dtype != self.torch_dtype or not out.is_contiguous():
             raise ValueError("out has the wrong shape, dtype or layout")
-        _check(self.lib, self.lib.vaedec_decode(self._h, latent.data_ptr(), _shape_arg(latent.shape),
-                                                latent.dim(), out.data_ptr(), int(n_bands),
-                                                self._stream_ptr(stream)))
+        if axis == "height":
+            _check(self.lib, self.lib.vaedec_decode(self._h, latent.data_ptr(), _shape_arg(latent.shape),
+                                                    latent.dim(), out.data_ptr(), int(n_bands),
+                                                    self._stream_ptr(stream)))
+        else:
+            _check(self.lib, self.lib.vaedec_decode_bands(self._h, latent.data_ptr(), _shape_arg(latent.shape),
+                                                          latent.dim(), out.data_ptr(), int(n_bands),
+                                                          BAND_AXES[axis], self._stream_ptr(stream)))
         return out
 
     def decode_host(self, latent_host, out_host, n_bands: int, stream=None):

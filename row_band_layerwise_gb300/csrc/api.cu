@@ -125,6 +125,9 @@ struct vaedec {
   // the decode stream; scores, probabilities and row sums have two slots (events order them)
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_s[2] = {}, ev_p[2] = {};
+  // width bands: a band's queries gathered dense, and its output before the scatter back
+  void* attn_qg = nullptr;
+  void* attn_ob = nullptr;
   GnPartial* gn_part = nullptr;
   size_t part_elems = 0;
   float* gn_scale = nullptr;
@@ -173,8 +176,10 @@ struct Plan {
 
 class Walker {
  public:
-  Walker(vaedec* h, cudaStream_t st, bool dry, int n_bands)
-      : h_(h), st_(st), dry_(dry), n_bands_(n_bands), odt_(h->dtype), sdt_(kF32) {}
+  // axis: 0 = height row bands, 1 = width column bands (on one GPU only attention's query
+  // partition depends on it, and no result does)
+  Walker(vaedec* h, cudaStream_t st, bool dry, int n_bands, int axis = 0)
+      : h_(h), st_(st), dry_(dry), n_bands_(n_bands), axis_(axis), odt_(h->dtype), sdt_(kF32) {}
 
   // configuration of a debug stop
   int stop_at = -1;
@@ -218,6 +223,7 @@ class Walker {
   cudaStream_t st_;
   bool dry_;
   int n_bands_;
+  int axis_;
   int odt_;   // operand dtype: what the MMAs read (the model dtype)
   int sdt_;   // storage dtype of the residual stream and every pre-norm tensor (fp32)
   int nest_ = 0;
@@ -775,8 +781,11 @@ class Walker {
         ConvGeom gv = g;
         gv.out_chfirst = 1;
         launch(gv, ptr(hn), wv, wv.w, wv.b, nullptr, nullptr, h_->attn_vt, nullptr, "attention v");
-        // band-local queries against every key/value of the frame
-        const std::vector<int> rows = band_rows(x.H, n_bands_);
+        // band-local queries against every key/value of the frame; width bands are gathered into a
+        // dense query buffer and their output scattered back (each query's arithmetic is the same
+        // whichever band holds it)
+        const bool wband = axis_ == 1;
+        const std::vector<int> rows = band_rows(wband ? x.W : x.H, n_bands_);
         DevConv kview;
         kview.ntaps = 1;
         kview.cin = C;
@@ -797,6 +806,14 @@ class Walker {
           int f, nr, slot;
           size_t qoff;
           void* o_band;
+          int c0, nc;   // width band: columns [c0, c0 + nc) of frame f, output scattered from o_band
+        };
+        auto scatter = [&](const Band& bd) {
+          if (!wband || !live()) return;
+          count();
+          check(launch_band_cols(odt_, bd.o_band, static_cast<char*>(ptr(hn)) + (size_t)bd.f * Ntok * C * oes, x.H,
+                                 x.W, C, bd.c0, bd.nc, 0, st_),
+                "attention band scatter");
         };
         bool have_pend = false;
         Band pend{};
@@ -833,6 +850,7 @@ class Walker {
             pa.out_f32 = odt_ == kF32;
             gemm(pa, "attention pv");
           }
+          scatter(bd);
         };
         if (overlap) {
           check(cudaEventRecord(h_->ev_fork, st_), "attention fork");
@@ -842,16 +860,25 @@ class Walker {
         for (int f = 0; f < F && live(); ++f) {
           int r0 = 0;
           for (int band = 0; band < n_bands_ && live(); ++band) {
-            const int nr = rows[band] * x.W;
-            const size_t qoff = ((size_t)f * Ntok + (size_t)r0 * x.W) * C;
-            void* o_band = static_cast<char*>(ptr(hn)) + qoff * oes;   // O overwrites the band's normalised rows
+            const int nr = wband ? x.H * rows[band] : rows[band] * x.W;
+            // height band: its queries and its output are contiguous rows of the frame (O overwrites
+            // the band's normalised rows); width band: gathered / scattered through dense buffers
+            const size_t qoff = wband ? 0 : ((size_t)f * Ntok + (size_t)r0 * x.W) * C;
+            void* q_band = static_cast<char*>(wband ? h_->attn_qg : h_->attn_q) + qoff * oes;
+            void* o_band = wband ? h_->attn_ob : static_cast<void*>(static_cast<char*>(ptr(hn)) + qoff * oes);
+            if (wband) {
+              count();
+              check(launch_band_cols(odt_, static_cast<char*>(h_->attn_q) + (size_t)f * Ntok * C * oes, h_->attn_qg,
+                                     x.H, x.W, C, r0, rows[band], 1, st_),
+                    "attention band gather");
+            }
             if (tc) {
               const int slot = seq & 1;
               // S[q, key] = (K Q^T)[key, q] / sqrt(C), keys on the accumulator lanes, stored fp16
               GemmArgs sa;
               sa.A = static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes;
               sa.lda = C;
-              sa.B = static_cast<char*>(h_->attn_q) + qoff * oes;
+              sa.B = q_band;
               sa.ldb = C;
               sa.M = (int)Ntok;
               sa.N = nr;
@@ -871,7 +898,7 @@ class Walker {
                     "softmax");
               if (overlap) check(cudaEventRecord(h_->ev_p[slot], h_->side), "attention softmax event");
               if (have_pend) run_pv(pend);
-              pend = Band{f, nr, slot, qoff, o_band};
+              pend = Band{f, nr, slot, qoff, o_band, r0, rows[band]};
               have_pend = true;
               ++seq;
             } else {
@@ -892,7 +919,7 @@ class Walker {
               gs.osy = gs.osx = 1;
               gs.out_f32 = 1;
               gs.scale = scale;
-              launch(gs, static_cast<char*>(h_->attn_q) + qoff * oes, kview,
+              launch(gs, q_band, kview,
                      static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes, nullptr, nullptr, nullptr,
                      h_->attn_s, nullptr, "attention scores");
               count();
@@ -905,6 +932,7 @@ class Walker {
               go.scale = 1.f;
               launch(go, h_->attn_p, vview, static_cast<char*>(h_->attn_vt) + (size_t)f * C * Ntok * oes, nullptr,
                      nullptr, h_->attn_l, o_band, nullptr, "attention pv");
+              scatter(Band{f, nr, 0, qoff, o_band, r0, rows[band]});
             }
             r0 += rows[band];
           }
@@ -1183,7 +1211,27 @@ vaedec_status validate_config(const vaedec_config* c) {
   return VAEDEC_OK;
 }
 
-vaedec_status check_latent(const vaedec* h, const int64_t* shape, int ndim, int n_bands) {
+// The split axis of a request ("VAE Parallel", Strategy Selection Contract and Spatially-Sharded
+// Decode): height or width as asked when that latent axis holds n_bands (one latent row or column
+// per band at least); auto: the longer axis that can, width on ties.
+vaedec_status resolve_band_axis(int64_t H, int64_t W, int n_bands, int axis, int* out) {
+  if (n_bands < 1) return fail(VAEDEC_ERR_INVALID_ARG, "n_bands must be >= 1");
+  if (axis == VAEDEC_BANDS_HEIGHT || axis == VAEDEC_BANDS_WIDTH) {
+    const int64_t n = axis == VAEDEC_BANDS_HEIGHT ? H : W;
+    if (n_bands > n)
+      return fail(VAEDEC_ERR_INVALID_ARG, std::string("n_bands must be in [1, latent ") +
+                                              (axis == VAEDEC_BANDS_HEIGHT ? "H" : "W") + "]");
+    *out = axis;
+    return VAEDEC_OK;
+  }
+  if (axis != VAEDEC_BANDS_AUTO) return fail(VAEDEC_ERR_INVALID_ARG, "unknown band axis");
+  const bool w_ok = n_bands <= W, h_ok = n_bands <= H;
+  if (!w_ok && !h_ok) return fail(VAEDEC_ERR_INVALID_ARG, "neither latent axis can hold n_bands bands");
+  *out = (w_ok && (!h_ok || W >= H)) ? VAEDEC_BANDS_WIDTH : VAEDEC_BANDS_HEIGHT;
+  return VAEDEC_OK;
+}
+
+vaedec_status check_latent(const vaedec* h, const int64_t* shape, int ndim, int n_bands, int axis = 0) {
   if (shape == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "latent shape is NULL");
   const int want = h->cfg.family == VAEDEC_FAMILY_KL2D ? 4 : 5;
   if (ndim != want) return fail(VAEDEC_ERR_INVALID_ARG, "latent ndim must be " + std::to_string(want));
@@ -1195,7 +1243,11 @@ vaedec_status check_latent(const vaedec* h, const int64_t* shape, int ndim, int 
   if (B > m[0] || T > m[1] || H > m[2] || W > m[3]) return fail(VAEDEC_ERR_INVALID_ARG, "latent shape exceeds max_latent");
   // the workspace was planned for max_latent: B*T*H*W and H*W must also fit
   if (B * T * H * W > m[0] * m[1] * m[2] * m[3]) return fail(VAEDEC_ERR_INVALID_ARG, "latent shape exceeds max_latent");
-  if (n_bands < 1 || n_bands > H) return fail(VAEDEC_ERR_INVALID_ARG, "n_bands must be in [1, latent H]");
+  if (axis == VAEDEC_BANDS_WIDTH) {
+    if (n_bands < 1 || n_bands > W) return fail(VAEDEC_ERR_INVALID_ARG, "n_bands must be in [1, latent W]");
+  } else if (n_bands < 1 || n_bands > H) {
+    return fail(VAEDEC_ERR_INVALID_ARG, "n_bands must be in [1, latent H]");
+  }
   // the tensor-core attention streams keys as 16-byte-aligned rows
   if (h->dtype == kBF16 && (H * W) % 8 != 0)
     return fail(VAEDEC_ERR_UNSUPPORTED, "bf16 path needs latent H*W to be a multiple of 8");
@@ -1377,6 +1429,8 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
   if (s == VAEDEC_OK) s = h->dalloc(&h->attn_q, plan.qkv, "attention q");
   if (s == VAEDEC_OK) s = h->dalloc(&h->attn_k, plan.qkv, "attention k");
   if (s == VAEDEC_OK) s = h->dalloc(&h->attn_vt, plan.qkv, "attention v");
+  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_qg, plan.qkv, "attention width-band queries");
+  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_ob, plan.qkv, "attention width-band output");
   h->qkv_bytes = plan.qkv;
   void* tmp = nullptr;
   if (s == VAEDEC_OK) s = h->dalloc(&tmp, plan.s * sizeof(float), "attention scores");
@@ -1405,7 +1459,7 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
       if (es == cudaSuccess) es = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (es != cudaSuccess) return bail(cuda_fail(es, "attention stream"));
   }
-  h->ws_bytes = kNumAct * plan.act + 3 * plan.qkv + plan.s * (4 + 2 * h->es) + plan.l * 8 + plan.part * sizeof(GnPartial) +
+  h->ws_bytes = kNumAct * plan.act + 5 * plan.qkv + plan.s * (4 + 2 * h->es) + plan.l * 8 + plan.part * sizeof(GnPartial) +
                 2 * plan.sc * 4 + h->io_latent_bytes + h->io_out_bytes;
   *out = h;
   return VAEDEC_OK;
@@ -1451,6 +1505,26 @@ vaedec_status vaedec_decode(vaedec_t* h, const void* latent, const int64_t* shap
   vaedec_status s = check_latent(h, shape, ndim, n_bands);
   if (s != VAEDEC_OK) return s;
   Walker w(h, static_cast<cudaStream_t>(stream), false, n_bands);
+  return w.run(latent, shape, ndim, out);
+}
+
+vaedec_status vaedec_band_axis(const int64_t* latent_shape, int ndim, int n_bands, int axis, int* axis_out) {
+  if (latent_shape == nullptr || axis_out == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  if (ndim != 4 && ndim != 5) return fail(VAEDEC_ERR_INVALID_ARG, "latent ndim must be 4 or 5");
+  return resolve_band_axis(latent_shape[ndim - 2], latent_shape[ndim - 1], n_bands, axis, axis_out);
+}
+
+vaedec_status vaedec_decode_bands(vaedec_t* h, const void* latent, const int64_t* shape, int ndim, void* out,
+                                  int n_bands, int axis, void* stream) {
+  if (h == nullptr || latent == nullptr || out == nullptr || shape == nullptr)
+    return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  if (ndim != 4 && ndim != 5) return fail(VAEDEC_ERR_INVALID_ARG, "latent ndim must be 4 or 5");
+  int ax = 0;
+  vaedec_status s = resolve_band_axis(shape[ndim - 2], shape[ndim - 1], n_bands, axis, &ax);
+  if (s != VAEDEC_OK) return s;
+  s = check_latent(h, shape, ndim, n_bands, ax);
+  if (s != VAEDEC_OK) return s;
+  Walker w(h, static_cast<cudaStream_t>(stream), false, n_bands, ax);
   return w.run(latent, shape, ndim, out);
 }
 

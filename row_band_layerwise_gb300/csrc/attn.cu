@@ -4,6 +4,7 @@
 // Also the small layout kernel that turns the caller's channels-first latent
 // into the channels-last activation layout.
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -279,6 +280,55 @@ cudaError_t launch_to_channels_last(int dtype, const void* x, void* y, int B, in
   else
     launch_pdl(to_channels_last_kernel<float>, (int)blocks, threads, 0, stream, static_cast<const float*>(x),
                                                                        static_cast<float*>(y), C, spatial, total);
+  return cudaGetLastError();
+}
+
+
+namespace {
+
+// Copy one width band of a channels-last frame [H][W][C] to or from a dense [H][nc][C] buffer
+// (16-byte vectors; C * sizeof(T) is a multiple of 16).
+template <typename T>
+__global__ void band_cols_kernel(const T* __restrict__ src, T* __restrict__ dst, int H, int W, int C, int c0, int nc,
+                                 int to_band) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
+  const int vpp = C * static_cast<int>(sizeof(T)) / 16;   // vectors per pixel
+  const long long n = static_cast<long long>(H) * nc * vpp;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int v = static_cast<int>(i % vpp);
+    const long long px = i / vpp;
+    const int j = static_cast<int>(px % nc);
+    const int h = static_cast<int>(px / nc);
+    const long long band_off = (static_cast<long long>(h) * nc + j) * vpp + v;
+    const long long full_off = (static_cast<long long>(h) * W + c0 + j) * vpp + v;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    if (to_band)
+      d4[band_off] = s4[full_off];
+    else
+      d4[full_off] = s4[band_off];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_band_cols(int dtype, const void* src, void* dst, int H, int W, int C, int c0, int nc, int to_band,
+                             cudaStream_t stream) {
+  const int es = dtype == kBF16 ? 2 : 4;
+  if ((C * es) % 16 != 0 || c0 < 0 || nc < 1 || c0 + nc > W) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) return cudaErrorInvalidValue;
+  const long long n = static_cast<long long>(H) * nc * (C * es / 16);
+  if (n <= 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = std::min<long long>((n + threads - 1) / threads, 152LL * 16);
+  if (dtype == kBF16)
+    launch_pdl(band_cols_kernel<__nv_bfloat16>, (int)blocks, threads, 0, stream,
+               static_cast<const __nv_bfloat16*>(src), static_cast<__nv_bfloat16*>(dst), H, W, C, c0, nc, to_band);
+  else
+    launch_pdl(band_cols_kernel<float>, (int)blocks, threads, 0, stream, static_cast<const float*>(src),
+               static_cast<float*>(dst), H, W, C, c0, nc, to_band);
   return cudaGetLastError();
 }
 

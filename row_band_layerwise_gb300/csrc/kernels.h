@@ -10,6 +10,13 @@ namespace vd {
 
 enum DType : int { kF32 = 1, kBF16 = 2 };
 
+// ---------------------------------------------------------------- width bands
+// Copy the width band [c0, c0 + nc) of a channels-last frame [H][W][C] into a dense
+// [H][nc][C] buffer (to_band = 1) or back (to_band = 0).  C * element size must be a
+// multiple of 16 and both pointers 16-byte aligned.
+cudaError_t launch_band_cols(int dtype, const void* src, void* dst, int H, int W, int C, int c0, int nc, int to_band,
+                             cudaStream_t stream);
+
 // ---------------------------------------------------------------- convolution
 // Tensor-core implicit GEMM (bf16 in, fp32 accumulate, bf16/fp32 out).
 // `wts` is [w_rows][ntaps_w][Cin] bf16 (K-major per output channel).  `out2`

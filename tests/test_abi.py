@@ -68,3 +68,30 @@ def test_fault_injection_arguments_checked_without_cuda(lib):
     assert lib.vaedec_debug_inject_fault(7, 1) == 1
     assert lib.vaedec_debug_inject_fault(1, 0) == 1
     assert lib.vaedec_debug_inject_fault(0, 0) == 0
+
+
+@pytest.mark.parametrize("shape", [(1, 16, 128, 128), (2, 16, 100, 136), (1, 16, 136, 100), (1, 16, 5, 60, 104),
+                                   (1, 4, 20, 3), (1, 4, 3, 20)])
+@pytest.mark.parametrize("n_bands", [1, 3, 4, 8])
+@pytest.mark.parametrize("axis", ["height", "width", "auto"])
+def test_band_axis_rule_matches_the_oracle(lib, shape, n_bands, axis):
+    """vaedec_band_axis (host logic) makes the same choice as the oracle's rule, and rejects
+    exactly the requests the rule rejects."""
+    from oracle import decoder
+    h, w = shape[-2], shape[-1]
+    try:
+        want = decoder.band_axis(h, w, n_bands, axis)
+    except ValueError:
+        with pytest.raises(rbl.VaedecError):
+            rbl.band_axis(shape, n_bands, axis)
+        return
+    assert rbl.band_axis(shape, n_bands, axis) == want
+
+
+def test_band_axis_rejects_bad_arguments(lib):
+    out = ctypes.c_int(-1)
+    shp = (ctypes.c_int64 * 4)(1, 16, 8, 8)
+    assert lib.vaedec_band_axis(shp, 4, 2, 7, ctypes.byref(out)) != 0      # unknown axis
+    assert lib.vaedec_band_axis(shp, 3, 2, 0, ctypes.byref(out)) != 0      # ndim
+    assert lib.vaedec_band_axis(shp, 4, 0, 2, ctypes.byref(out)) != 0      # n_bands < 1
+    assert lib.vaedec_band_axis(None, 4, 2, 2, ctypes.byref(out)) != 0
