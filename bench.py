@@ -267,8 +267,9 @@ def run_ours(args, w: synth.Workload):
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
+    axis = rbl.band_axis(shp, nb, args.band_axis)
     for _ in range(args.warmup):
-        dec.decode(zd, nb, out=out)
+        dec.decode(zd, nb, out=out, axis=axis)
     dec.sync()
 
     # op list (for the per-kernel-kind roofline)
@@ -284,7 +285,7 @@ def run_ours(args, w: synth.Workload):
     for i in range(args.steps):
         flush.zero_()                       # evict L2 between steps (outside the step events)
         starts[i].record(stream)
-        dec.decode(zd, nb, out=out, stream=stream)
+        dec.decode(zd, nb, out=out, stream=stream, axis=axis)
         ends[i].record(stream)
     barrier()
     clock_info = clocks.stop()
@@ -340,7 +341,7 @@ def run_ours(args, w: synth.Workload):
             "vs_baseline": value / PAGES_DENSE_MPIXS if w.name == "kl_zimage_1024" else None,
             "dtype": "bf16" if w.dtype == "bf16" else "f32",
             "data": "synthetic (seeded N(0,1) latent, seeded fan-in uniform weights)",
-            "config": {"workload": w.name, "description": w.description, "n_bands": nb,
+            "config": {"workload": w.name, "description": w.description, "n_bands": nb, "band_axis": axis,
                        "latent": list(shp), "output_pixels_per_step": px,
                        "l2": f"{L2_FLUSH_BYTES >> 20} MiB buffer written between steps, outside the step events",
                        "parallelism": "replicas" if ws > 1 else "single GPU",
@@ -378,6 +379,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="kl_zimage_1024", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--bands", type=int, default=0, help="override the workload's band count")
+    ap.add_argument("--band-axis", default="height", choices=["height", "width", "auto"],
+                    help="band split axis of the device-timed decodes (e2e always uses height bands)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
