@@ -86,6 +86,7 @@ def output_shape(arch, latent_shape: Sequence[int]) -> Tuple[int, ...]:
     f = 2 ** n_up
     if arch.family == "kl2d":
         b, _, h, w = latent_shape
+        f *= arch.latent_patch          # the front-end's unpatchify doubles the grid when patched
         return (b, arch.out_channels, h * f, w * f)
     b, _, t, h, w = latent_shape
     for u in arch.stage_upsample:
@@ -251,8 +252,18 @@ def _kl_attention(ex, W, p, x, groups, eps):
     return out_fn(x, q_fn(hn), *kv_fn(hn))
 
 
+def latent_frontend(arch, W: Dict[str, np.ndarray], z: np.ndarray) -> np.ndarray:
+    """AutoencoderKLFlux2 front-end (kl2d with latent_patch > 1): undo the latent BatchNorm over the
+    patchified channels, then unpatchify to the decoder's latent grid.  Identity otherwise."""
+    if arch.latent_patch <= 1:
+        return z
+    x = ops.inverse_batch_norm(z, W["bn.running_mean"], W["bn.running_var"], arch.latent_bn_eps)
+    return ops.unpatchify(x, arch.latent_patch)
+
+
 def decode_kl2d(arch, W: Dict[str, np.ndarray], z: np.ndarray, ex) -> np.ndarray:
     G, eps = arch.norm_groups, arch.eps
+    z = latent_frontend(arch, W, z)
     x = ex.split(z)
     x = ex.conv(x, W["conv_in.weight"], W["conv_in.bias"])
     x = _kl_resnet(ex, W, "mid_block.resnets.0", x, G, eps)
@@ -363,7 +374,8 @@ def decode(arch, W: Dict[str, np.ndarray], z: np.ndarray,
     """Decode ``z`` in float64; unbanded when ``n_bands`` is None, else banded along ``axis``
     ("height", "width" or "auto", see band_axis)."""
     if n_bands is not None:
-        axis = band_axis(z.shape[-2], z.shape[-1], n_bands, axis)
+        p = arch.latent_patch if arch.family == "kl2d" else 1   # bands split the decoder's latent grid
+        axis = band_axis(z.shape[-2] * p, z.shape[-1] * p, n_bands, axis)
     ex = Dense() if n_bands is None else Banded(n_bands, axis)
     if arch.family == "kl2d":
         return decode_kl2d(arch, W, z, ex)

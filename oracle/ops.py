@@ -92,6 +92,29 @@ def causal_conv3d(x: np.ndarray, w: np.ndarray, b: np.ndarray,
 # ---------------------------------------------------------------------------
 # Pointwise and local operators
 # ---------------------------------------------------------------------------
+def unpatchify(x: np.ndarray, p: int) -> np.ndarray:
+    """[B, C p^2, H, W] -> [B, C, p H, p W]: input channel c p^2 + py p + px holds output pixel
+    (p y + py, p x + px) of channel c (the inverse of the p x p space-to-depth that groups each
+    channel's p x p patch into consecutive channels; AutoencoderKLFlux2's latent patch conversion,
+    "VAEP：VAE 并行解码", 不同模型如何复用)."""
+    x = _f64(x)
+    b, cp, h, w = x.shape
+    c = cp // (p * p)
+    out = np.empty((b, c, h * p, w * p))
+    for py in range(p):
+        for px in range(p):
+            out[:, :, py::p, px::p] = x[:, py * p + px::p * p]
+    return out
+
+
+def inverse_batch_norm(x: np.ndarray, mean: np.ndarray, var: np.ndarray, eps: float) -> np.ndarray:
+    """Undo an inference BatchNorm without affine terms, per channel (axis 1):
+    x sqrt(var + eps) + mean (the latent BatchNorm the AutoencoderKLFlux2 front-end keeps)."""
+    x = _f64(x)
+    shape = (1, -1) + (1,) * (x.ndim - 2)
+    return x * np.sqrt(_f64(var) + eps).reshape(shape) + _f64(mean).reshape(shape)
+
+
 def silu(x: np.ndarray) -> np.ndarray:
     """SiLU(x) = x / (1 + exp(-x))."""
     x = _f64(x)

@@ -50,6 +50,11 @@ class Arch:
     norm_groups: int = 32            # GroupNorm groups (kl2d only)
     eps: float = 1e-6                # GroupNorm epsilon (kl2d only)
     out_channels: int = 3
+    # AutoencoderKLFlux2-style front-end (kl2d only): the decode input is the 2x2-patchified latent
+    # (latent_patch**2 * latent_channels channels on a half-size grid) normalised by an inference
+    # BatchNorm without affine terms (weights bn.running_mean / bn.running_var)
+    latent_patch: int = 1
+    latent_bn_eps: float = 1e-4
 
     def stage_in_channels(self) -> List[int]:
         cins = []
@@ -80,6 +85,16 @@ KL_ZIMAGE = Arch(
     stage_channels=(512, 512, 256, 128), stage_resnets=(3, 3, 3, 3),
     stage_upsample=(1, 1, 1, 0), stage_up_channels=(512, 512, 256, 0),
     norm_groups=32, eps=1e-6,
+)
+
+# FLUX.2-style AutoencoderKLFlux2 decoder: the Z-Image / FLUX.1 decoder body with 32 latent
+# channels, fed through the latent front-end (inverse BatchNorm over the 128 patchified channels,
+# then 2x2 unpatchify).
+FLUX2 = Arch(
+    family="kl2d", latent_channels=32, mid_channels=512,
+    stage_channels=(512, 512, 256, 128), stage_resnets=(3, 3, 3, 3),
+    stage_upsample=(1, 1, 1, 0), stage_up_channels=(512, 512, 256, 0),
+    norm_groups=32, eps=1e-6, latent_patch=2, latent_bn_eps=1e-4,
 )
 
 # Wan 2.1 VAE decoder: base dim 96, dim_mult (1,2,4,4); stages 0 and 1 end in a
@@ -116,6 +131,9 @@ WORKLOADS: Dict[str, Workload] = {
                  "3 uneven bands (34/33/33)"),
         Workload("wan_17x480x832", WAN, "bf16", (1, 16, 5, 60, 104), 4,
                  "Wan causal 3D decoder, 5x60x104 latent -> 17x480x832, bf16, 4 bands"),
+        Workload("flux2_1024", FLUX2, "bf16", (1, 128, 64, 64), 8,
+                 "FLUX.2-style decoder, patchified 128x64x64 latent (32x128x128 after the front-end) "
+                 "-> 1024x1024, bf16, 8 bands"),
     ]
 }
 
@@ -158,6 +176,9 @@ def weight_spec(arch: Arch) -> List[Tuple[str, Tuple[int, ...], int, str]]:
             return e
 
         C = arch.mid_channels
+        if arch.latent_patch > 1:
+            cp = arch.latent_channels * arch.latent_patch ** 2
+            spec += [("bn.running_mean", (cp,), 0, "bn_mean"), ("bn.running_var", (cp,), 0, "bn_var")]
         spec += _conv_entries("conv_in", arch.latent_channels, C, k3)
         spec += resnet("mid_block.resnets.0", C, C)
         a = "mid_block.attentions.0"
@@ -224,6 +245,10 @@ def make_weights(arch: Arch, dtype: str, seed: int = 1) -> Dict[str, np.ndarray]
             v = rng.uniform(-bound, bound, size=shape).astype(np.float32)
         elif kind == "ones":
             v = np.ones(shape, np.float32)
+        elif kind == "bn_mean":
+            v = rng.normal(0.0, 0.5, size=shape).astype(np.float32)
+        elif kind == "bn_var":
+            v = rng.uniform(0.25, 4.0, size=shape).astype(np.float32)
         else:
             v = np.zeros(shape, np.float32)
         out[name] = round_bf16(v) if dtype == "bf16" else v

@@ -271,3 +271,48 @@ def test_band_axis_rule(h, w, n, axis, want):
 def test_band_axis_rejects(h, w, n, axis):
     with pytest.raises(ValueError):
         decoder.band_axis(h, w, n, axis)
+
+
+# ---- AutoencoderKLFlux2 latent front-end (inverse latent BatchNorm, 2x2 unpatchify) -----------
+def test_unpatchify_inverts_pixel_unshuffle():
+    """torch's pixel_unshuffle groups each channel's 2x2 patch into channels c*4 + py*2 + px; the
+    oracle's unpatchify must invert it exactly."""
+    x = np.random.default_rng(2).standard_normal((2, 3, 8, 6))
+    from oracle import ops
+    patched = F.pixel_unshuffle(torch.from_numpy(x), 2).numpy()
+    np.testing.assert_array_equal(ops.unpatchify(patched, 2), x)
+    np.testing.assert_array_equal(F.pixel_shuffle(torch.from_numpy(patched), 2).numpy(), ops.unpatchify(patched, 2))
+
+
+def test_inverse_batch_norm_inverts_torch_batch_norm():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((2, 12, 5, 7))
+    mean, var, eps = rng.normal(0, 0.5, 12), rng.uniform(0.25, 4.0, 12), 1e-4
+    from oracle import ops
+    y = ops.inverse_batch_norm(x, mean, var, eps)
+    back = F.batch_norm(torch.from_numpy(y), torch.from_numpy(mean), torch.from_numpy(var), training=False,
+                        eps=eps).numpy()
+    np.testing.assert_allclose(back, x, rtol=1e-13, atol=1e-13)
+
+
+FLUX2_SMALL = dataclasses.replace(KL_SMALL, latent_channels=8, latent_patch=2, latent_bn_eps=1e-4)
+
+
+def test_flux2_decode_is_the_kl_decode_of_the_frontend_output():
+    """The front-end is a pure prefix: decoding the patchified, normalised latent equals decoding
+    (with the same decoder body) the latent that torch's batch_norm + pixel_unshuffle would turn
+    into it."""
+    W = synth.make_weights(FLUX2_SMALL, "fp32", seed=3)
+    rng = np.random.default_rng(6)
+    z = rng.standard_normal((1, 8, 6, 4))                                  # decoder-grid latent
+    zp = F.pixel_unshuffle(torch.from_numpy(z), 2)
+    zp = F.batch_norm(zp, torch.from_numpy(W["bn.running_mean"].astype(np.float64)),
+                      torch.from_numpy(W["bn.running_var"].astype(np.float64)), training=False,
+                      eps=FLUX2_SMALL.latent_bn_eps).numpy()                # what the pipeline hands in
+    body = dataclasses.replace(FLUX2_SMALL, latent_patch=1)
+    want = decoder.decode(body, W, z)
+    got = decoder.decode(FLUX2_SMALL, W, zp)
+    assert got.shape == decoder.output_shape(FLUX2_SMALL, zp.shape) == want.shape
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12 * np.abs(want).max())
+    np.testing.assert_allclose(decoder.decode(FLUX2_SMALL, W, zp, 3), got, rtol=0,
+                               atol=1e-12 * np.abs(got).max())
