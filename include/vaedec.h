@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define VAEDEC_ABI_VERSION 1
+#define VAEDEC_ABI_VERSION 2
 #define VAEDEC_MAX_STAGES 6
 
 typedef struct vaedec vaedec_t; /* opaque: device weights + workspace */
@@ -90,6 +90,16 @@ typedef struct {
   int norm_groups;
   float eps;
   int64_t max_latent[4];
+  /* AutoencoderKLFlux2 latent front-end ("VAEP：VAE 并行解码", 不同模型如何复用: keep the latent
+   * BatchNorm and patch conversion), KL2D only.  latent_patch 0 or 1: none.  latent_patch 2: the
+   * decode input is the transformer-side latent, 4 * latent_channels channels on an (H, W) grid
+   * normalised by an inference BatchNorm without affine terms (weights "bn.running_mean" and
+   * "bn.running_var", 4 * latent_channels values each, eps latent_bn_eps); the decode first computes
+   * x * sqrt(var + eps) + mean per channel and unpatchifies channel c*4 + py*2 + px to pixel
+   * (2y + py, 2x + px) of channel c, then runs the decoder on the (2H, 2W) grid.  Latent shapes,
+   * max_latent and output shapes are in the input's (H, W) units; bands split the (2H, 2W) grid. */
+  int latent_patch;
+  float latent_bn_eps;
 } vaedec_config;
 
 /*

@@ -55,7 +55,8 @@ class _Config(ctypes.Structure):
                 ("stage_upsample", ctypes.c_int * MAX_STAGES),
                 ("stage_up_channels", ctypes.c_int * MAX_STAGES),
                 ("norm_groups", ctypes.c_int), ("eps", ctypes.c_float),
-                ("max_latent", ctypes.c_int64 * 4)]
+                ("max_latent", ctypes.c_int64 * 4),
+                ("latent_patch", ctypes.c_int), ("latent_bn_eps", ctypes.c_float)]
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -117,7 +118,8 @@ def make_config(arch, dtype: str, max_latent: Sequence[int]) -> _Config:
 
     ``arch`` needs the attributes family, latent_channels, mid_channels,
     out_channels, stage_channels, stage_resnets, stage_upsample,
-    stage_up_channels, norm_groups and eps; ``max_latent`` is (B, T, H, W).
+    stage_up_channels, norm_groups and eps, and optionally latent_patch and latent_bn_eps (the
+    AutoencoderKLFlux2 latent front-end); ``max_latent`` is (B, T, H, W) in the decode input's units.
     """
     c = _Config()
     c.family = FAMILY[arch.family]
@@ -138,6 +140,8 @@ def make_config(arch, dtype: str, max_latent: Sequence[int]) -> _Config:
     c.eps = arch.eps
     for k in range(4):
         c.max_latent[k] = int(max_latent[k])
+    c.latent_patch = int(getattr(arch, "latent_patch", 1))
+    c.latent_bn_eps = float(getattr(arch, "latent_bn_eps", 0.0))
     return c
 
 

@@ -128,6 +128,11 @@ struct vaedec {
   // width bands: a band's queries gathered dense, and its output before the scatter back
   void* attn_qg = nullptr;
   void* attn_ob = nullptr;
+  // AutoencoderKLFlux2 latent front-end: patch size (1 = none) and the inverse latent BatchNorm
+  // per patched channel, scale = sqrt(var + eps) and shift = mean
+  int patch = 1;
+  float* bn_scale = nullptr;
+  float* bn_shift = nullptr;
   GnPartial* gn_part = nullptr;
   size_t part_elems = 0;
   float* gn_scale = nullptr;
@@ -344,17 +349,25 @@ class Walker {
 
   // ---------------------------------------------------------------- ops
   Act latent_in(const void* latent, const Act& z) {
+    const int p = h_->patch;
     Act y = z;
     y.buf = 0;
     y.dt = odt_;
+    y.C = z.C / (p * p);   // the front-end's unpatchify (p = 1: a plain layout change)
+    y.H = z.H * p;
+    y.W = z.W * p;
     note_act(y);
     Act zin = z;
     zin.buf = -1;
     zin.ext = const_cast<void*>(latent);
     if (begin("kind=latent name=latent" + io(zin, nullptr, y))) {
       count();
-      check(launch_to_channels_last(odt_, latent, ptr(y), z.B, z.C, (long long)z.T * z.H * z.W, st_),
-            "latent layout");
+      if (p > 1)
+        check(launch_latent_frontend(odt_, latent, ptr(y), z.B, y.C, z.H, z.W, p, h_->bn_scale, h_->bn_shift, st_),
+              "latent front-end");
+      else
+        check(launch_to_channels_last(odt_, latent, ptr(y), z.B, z.C, (long long)z.T * z.H * z.W, st_),
+              "latent layout");
     }
     end(&zin, nullptr, y);
     return y;
@@ -1208,6 +1221,10 @@ vaedec_status validate_config(const vaedec_config* c) {
   if (c->dtype == VAEDEC_DTYPE_BF16 && c->latent_channels % 16 != 0)
     return fail(VAEDEC_ERR_UNSUPPORTED, "bf16 path needs latent channels that are a multiple of 16");
   if (c->family == VAEDEC_FAMILY_KL2D && !(c->eps > 0.f)) return fail(VAEDEC_ERR_INVALID_ARG, "eps must be positive");
+  if (c->latent_patch < 0 || c->latent_patch > 2) return fail(VAEDEC_ERR_UNSUPPORTED, "latent_patch must be 0, 1 or 2");
+  if (c->latent_patch == 2 && c->family != VAEDEC_FAMILY_KL2D)
+    return fail(VAEDEC_ERR_INVALID_ARG, "the latent front-end is a KL2D option");
+  if (c->latent_patch == 2 && !(c->latent_bn_eps > 0.f)) return fail(VAEDEC_ERR_INVALID_ARG, "latent_bn_eps must be positive");
   return VAEDEC_OK;
 }
 
@@ -1237,19 +1254,22 @@ vaedec_status check_latent(const vaedec* h, const int64_t* shape, int ndim, int 
   if (ndim != want) return fail(VAEDEC_ERR_INVALID_ARG, "latent ndim must be " + std::to_string(want));
   for (int i = 0; i < ndim; ++i)
     if (shape[i] < 1) return fail(VAEDEC_ERR_INVALID_ARG, "latent dims must be positive");
-  if (shape[1] != h->cfg.latent_channels) return fail(VAEDEC_ERR_INVALID_ARG, "latent channel count mismatch");
+  if (shape[1] != (int64_t)h->cfg.latent_channels * h->patch * h->patch)
+    return fail(VAEDEC_ERR_INVALID_ARG, "latent channel count mismatch");
   const int64_t B = shape[0], T = ndim == 5 ? shape[2] : 1, H = shape[ndim - 2], W = shape[ndim - 1];
   const int64_t* m = h->cfg.max_latent;
   if (B > m[0] || T > m[1] || H > m[2] || W > m[3]) return fail(VAEDEC_ERR_INVALID_ARG, "latent shape exceeds max_latent");
   // the workspace was planned for max_latent: B*T*H*W and H*W must also fit
   if (B * T * H * W > m[0] * m[1] * m[2] * m[3]) return fail(VAEDEC_ERR_INVALID_ARG, "latent shape exceeds max_latent");
+  // bands split the decoder's latent grid (after the front-end's unpatchify, when there is one)
+  const int64_t gh = H * h->patch, gw = W * h->patch;
   if (axis == VAEDEC_BANDS_WIDTH) {
-    if (n_bands < 1 || n_bands > W) return fail(VAEDEC_ERR_INVALID_ARG, "n_bands must be in [1, latent W]");
-  } else if (n_bands < 1 || n_bands > H) {
+    if (n_bands < 1 || n_bands > gw) return fail(VAEDEC_ERR_INVALID_ARG, "n_bands must be in [1, latent W]");
+  } else if (n_bands < 1 || n_bands > gh) {
     return fail(VAEDEC_ERR_INVALID_ARG, "n_bands must be in [1, latent H]");
   }
   // the tensor-core attention streams keys as 16-byte-aligned rows
-  if (h->dtype == kBF16 && (H * W) % 8 != 0)
+  if (h->dtype == kBF16 && (gh * gw) % 8 != 0)
     return fail(VAEDEC_ERR_UNSUPPORTED, "bf16 path needs latent H*W to be a multiple of 8");
   return VAEDEC_OK;
 }
@@ -1273,6 +1293,7 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
   if (s != VAEDEC_OK) return s;
   vaedec* h = new vaedec();
   h->cfg = *config;
+  h->patch = config->latent_patch == 2 ? 2 : 1;
   h->dtype = config->dtype == VAEDEC_DTYPE_BF16 ? kBF16 : kF32;
   h->es = h->dtype == kBF16 ? 2 : 4;
   auto bail = [&](vaedec_status st) {
@@ -1398,6 +1419,33 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
     }
   }
 
+  if (h->patch > 1) {
+    // inverse latent BatchNorm of the front-end: per patched channel scale = sqrt(var + eps), shift = mean
+    const int cp = config->latent_channels * h->patch * h->patch;
+    const vaedec_tensor* mt = find_tensor(weights, n_weights, "bn.running_mean");
+    const vaedec_tensor* vt = find_tensor(weights, n_weights, "bn.running_var");
+    if (!mt || !vt || mt->ndim != 1 || vt->ndim != 1 || mt->shape[0] != cp || vt->shape[0] != cp ||
+        mt->data == nullptr || vt->data == nullptr)
+      return bail(fail(VAEDEC_ERR_INVALID_ARG, "missing or mis-shaped bn.running_mean / bn.running_var"));
+    std::vector<float> sc(cp), sh(cp);
+    for (int i = 0; i < cp; ++i) {
+      const float var = to_f32(*vt, i);
+      if (!(var + config->latent_bn_eps > 0.f)) return bail(fail(VAEDEC_ERR_INVALID_ARG, "bn.running_var + eps must be positive"));
+      sc[i] = std::sqrt(var + config->latent_bn_eps);
+      sh[i] = to_f32(*mt, i);
+    }
+    void* tmp = nullptr;
+    s = h->dalloc(&tmp, cp * sizeof(float), "latent batchnorm scale");
+    if (s != VAEDEC_OK) return bail(s);
+    h->bn_scale = static_cast<float*>(tmp);
+    s = h->dalloc(&tmp, cp * sizeof(float), "latent batchnorm shift");
+    if (s != VAEDEC_OK) return bail(s);
+    h->bn_shift = static_cast<float*>(tmp);
+    cudaError_t e = cudaMemcpy(h->bn_scale, sc.data(), cp * sizeof(float), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(h->bn_shift, sh.data(), cp * sizeof(float), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "latent batchnorm upload"));
+  }
+
   // workspace plan: a dry walk at max_latent with one band (the largest score buffer)
   Plan plan;
   {
@@ -1406,7 +1454,7 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
     const int64_t* m = config->max_latent;
     if (config->family == VAEDEC_FAMILY_KL2D) {
       ndim = 4;
-      shape[0] = m[0]; shape[1] = config->latent_channels; shape[2] = m[2]; shape[3] = m[3];
+      shape[0] = m[0]; shape[1] = (int64_t)config->latent_channels * h->patch * h->patch; shape[2] = m[2]; shape[3] = m[3];
     } else {
       ndim = 5;
       shape[0] = m[0]; shape[1] = config->latent_channels; shape[2] = m[1]; shape[3] = m[2]; shape[4] = m[3];
@@ -1480,6 +1528,7 @@ vaedec_status vaedec_output_shape(const vaedec_t* h, const int64_t* shape, int n
     if (h->cfg.stage_upsample[s]) f *= 2;
     if (h->cfg.stage_upsample[s] == VAEDEC_UP_SPATIOTEMPORAL) T = 2 * T - 1;
   }
+  f *= h->patch;   // the front-end's unpatchify (KL2D with a patched latent)
   out_shape[0] = shape[0];
   out_shape[1] = h->cfg.out_channels;
   if (ndim == 5) {
@@ -1520,7 +1569,7 @@ vaedec_status vaedec_decode_bands(vaedec_t* h, const void* latent, const int64_t
     return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
   if (ndim != 4 && ndim != 5) return fail(VAEDEC_ERR_INVALID_ARG, "latent ndim must be 4 or 5");
   int ax = 0;
-  vaedec_status s = resolve_band_axis(shape[ndim - 2], shape[ndim - 1], n_bands, axis, &ax);
+  vaedec_status s = resolve_band_axis(shape[ndim - 2] * h->patch, shape[ndim - 1] * h->patch, n_bands, axis, &ax);
   if (s != VAEDEC_OK) return s;
   s = check_latent(h, shape, ndim, n_bands, ax);
   if (s != VAEDEC_OK) return s;

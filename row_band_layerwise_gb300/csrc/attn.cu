@@ -332,4 +332,49 @@ cudaError_t launch_band_cols(int dtype, const void* src, void* dst, int H, int W
   return cudaGetLastError();
 }
 
+
+namespace {
+
+// AutoencoderKLFlux2 front-end: undo the inference BatchNorm of the patchified latent (per patched
+// channel: x * scale + shift with scale = sqrt(var + eps), shift = mean) and unpatchify channel
+// c*p*p + py*p + px of the (Hp, Wp) grid to pixel (p*y + py, p*x + px) of channel c, written
+// channels-last on the (p*Hp, p*Wp) grid.  fp32 arithmetic, one rounding to T.
+template <typename T>
+__global__ void latent_frontend_kernel(const T* __restrict__ zp, T* __restrict__ y, int B, int C, int Hp, int Wp,
+                                       int p, const float* __restrict__ scale, const float* __restrict__ shift) {
+  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
+  pdl_trigger();
+  const int H = Hp * p, W = Wp * p;
+  const long long n = static_cast<long long>(B) * H * W * C;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % C);
+    const long long px = i / C;
+    const int X = static_cast<int>(px % W);
+    const int Y = static_cast<int>((px / W) % H);
+    const int b = static_cast<int>(px / (static_cast<long long>(W) * H));
+    const int cp = (c * p + Y % p) * p + X % p;
+    const long long src = ((static_cast<long long>(b) * C * p * p + cp) * Hp + Y / p) * Wp + X / p;
+    const float v = static_cast<float>(zp[src]) * scale[cp] + shift[cp];
+    y[i] = static_cast<T>(v);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_latent_frontend(int dtype, const void* zp, void* y, int B, int C, int Hp, int Wp, int p,
+                                   const float* scale, const float* shift, cudaStream_t stream) {
+  const long long n = static_cast<long long>(B) * Hp * p * Wp * p * C;
+  if (n <= 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = std::min<long long>((n + threads - 1) / threads, 152LL * 16);
+  if (dtype == kBF16)
+    launch_pdl(latent_frontend_kernel<__nv_bfloat16>, (int)blocks, threads, 0, stream,
+               static_cast<const __nv_bfloat16*>(zp), static_cast<__nv_bfloat16*>(y), B, C, Hp, Wp, p, scale, shift);
+  else
+    launch_pdl(latent_frontend_kernel<float>, (int)blocks, threads, 0, stream, static_cast<const float*>(zp),
+               static_cast<float*>(y), B, C, Hp, Wp, p, scale, shift);
+  return cudaGetLastError();
+}
+
 }  // namespace vd

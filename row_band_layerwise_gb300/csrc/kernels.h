@@ -10,6 +10,12 @@ namespace vd {
 
 enum DType : int { kF32 = 1, kBF16 = 2 };
 
+// ---------------------------------------------------------------- latent front-end
+// Inverse latent BatchNorm (x * scale[cp] + shift[cp] per patched channel cp) and p x p unpatchify
+// of a channels-first [B][C*p*p][Hp][Wp] latent into channels-last [B][p*Hp][p*Wp][C].
+cudaError_t launch_latent_frontend(int dtype, const void* zp, void* y, int B, int C, int Hp, int Wp, int p,
+                                   const float* scale, const float* shift, cudaStream_t stream);
+
 // ---------------------------------------------------------------- width bands
 // Copy the width band [c0, c0 + nc) of a channels-last frame [H][W][C] into a dense
 // [H][nc][C] buffer (to_band = 1) or back (to_band = 0).  C * element size must be a

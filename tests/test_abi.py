@@ -95,3 +95,18 @@ def test_band_axis_rejects_bad_arguments(lib):
     assert lib.vaedec_band_axis(shp, 3, 2, 0, ctypes.byref(out)) != 0      # ndim
     assert lib.vaedec_band_axis(shp, 4, 0, 2, ctypes.byref(out)) != 0      # n_bands < 1
     assert lib.vaedec_band_axis(None, 4, 2, 2, ctypes.byref(out)) != 0
+
+
+def test_latent_frontend_config_checked_without_cuda(lib):
+    import dataclasses
+    h = ctypes.c_void_p()
+    flux = dataclasses.replace(synth.KL_TINY, latent_patch=2, latent_bn_eps=1e-4)
+    cfg = rbl.make_config(flux, "fp32", (1, 1, 8, 8))
+    cfg.latent_patch = 3                                    # only 2x2 patches
+    assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 2
+    cfg = rbl.make_config(flux, "fp32", (1, 1, 8, 8))
+    cfg.latent_bn_eps = 0.0
+    assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 1
+    cfg = rbl.make_config(dataclasses.replace(synth.WAN, latent_patch=2), "bf16", (1, 2, 8, 8))
+    assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 1   # a KL2D option only
+    assert not h.value
