@@ -48,6 +48,7 @@ def out_pixels(w: synth.Workload) -> int:
     shp = w.latent_shape
     f = 2 ** sum(1 for u in w.arch.stage_upsample if u)
     if w.arch.family == "kl2d":
+        f *= w.arch.latent_patch          # a patched latent is unpatchified to twice the grid first
         return shp[0] * shp[2] * f * shp[3] * f
     t = shp[2]
     for u in w.arch.stage_upsample:
