@@ -468,7 +468,12 @@ class Walker {
   // Key-dimension split of the probabilities x values product: a function of the
   // number of keys only, so every band count sums the same partial products in
   // the same order.
-  static int pv_splits(long long ntok) { return (int)std::max(1LL, std::min(8LL, (ntok + 4095) / 4096)); }
+  // Up to 8192 keys the band GEMMs are small (a few 128 x 256 tiles): 8 splits of >= 512 keys (fewer
+  // when there are fewer keys) keep the SMs busy; above, one split per 4096 keys, at most 8.
+  static int pv_splits(long long ntok) {
+    const long long s = ntok <= 8192 ? (ntok + 511) / 512 : (ntok + 4095) / 4096;
+    return (int)std::max(1LL, std::min(8LL, s));
+  }
 
   static void fill_taps(ConvGeom& g, ConvKind kind, const DevConv& w) {
     std::memset(g.taps, 0, sizeof(g.taps));
