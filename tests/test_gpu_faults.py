@@ -78,3 +78,41 @@ def test_bounded_wait_runs_out_and_the_handle_recovers(case, clean):
     finally:
         rbl.set_wait_limit(0)
     assert bool((case.decode(2).cpu() == clean).all())
+
+
+@pytest.mark.parametrize("axis", ["height", "width"])
+def test_refused_launch_at_every_point_of_the_attention_op(case, clean, axis):
+    """A decode stopped at any launch inside the attention op (whose band softmax runs on the
+    handle's second stream, forked from and joined back to the caller's stream) leaves nothing
+    running on that stream: the next decode on the same handle is bit-identical to a clean one."""
+    torch, rbl = require_gpu()
+    n_bands = 4
+    ops = case.dec.ops(SHAPE, n_bands)
+    # launches before the attention op = launches of a decode stopped just before it
+    first = None
+    total = 0
+    counts = []
+    for i, d in enumerate(ops):
+        if d["kind"] == "attention":
+            first = i
+            break
+    assert first is not None
+    before = case.dec.launch_count()
+    case.dec.run_until(case.z_dev, n_bands, first - 1)
+    torch.cuda.synchronize()
+    n_pre = case.dec.launch_count() - before
+    before = case.dec.launch_count()
+    case.dec.run_until(case.z_dev, n_bands, first)
+    torch.cuda.synchronize()
+    n_attn = case.dec.launch_count() - before - n_pre
+    assert n_attn > 6
+    for k in range(1, n_attn + 1):
+        rbl.inject_fault("launch", n_pre + k)
+        with pytest.raises(rbl.VaedecError):
+            case.dec.decode(case.z_dev, n_bands, axis=axis)
+        rbl.inject_fault("off")
+        torch.cuda.synchronize()
+        out = case.dec.decode(case.z_dev, n_bands, axis=axis)
+        torch.cuda.synchronize()
+        case.dec.sync()
+        assert bool((out.cpu() == clean).all()), f"stop at attention launch {k}"
