@@ -174,3 +174,31 @@ class Case:
         y = to_numpy(t_out)
         aux = to_numpy(t_aux).reshape(aux_shape) if t_aux is not None else None
         return d, x, aux, y
+
+
+# Per-op tolerances: one bf16 rounding of the output dominates (2^-9 relative).
+OP_TOL = {"bf16": dict(rel=6e-3, attn_rel=1.2e-2), "fp32": dict(rel=1e-5, attn_rel=1e-5)}
+
+
+def check_all_ops(case: Case, n_bands: int, stride: int = 1):
+    """Every traced op of one decode (every `stride`-th) against the oracle applied to that
+    op's own GPU input, within OP_TOL; returns the set of "kind:conv" seen."""
+    n_ops = case.dec.num_ops(case.shape, n_bands)
+    assert n_ops > 5
+    tol = OP_TOL[case.dtype]
+    seen = set()
+    for op in range(0, n_ops, stride):
+        d, x, aux, y = case.capture(n_bands, op)
+        seen.add(d["kind"] + ":" + d.get("conv", ""))
+        in_shape = parse_shape(d["in"])
+        if d["kind"] == "latent":
+            xin = x.reshape(case.shape)
+            exp = np.moveaxis(xin, 1, -1)
+            np.testing.assert_array_equal(y.reshape(exp.shape), exp)
+            continue
+        ref = oracle_op(d, case.W, case.arch, x.reshape(in_shape), aux)
+        got = y.reshape(ref.shape)
+        lim = tol["attn_rel"] if d["kind"] == "attention" else tol["rel"]
+        err = rel_l2(got, ref)
+        assert err <= lim, f"op {op} {d}: rel-L2 {err:.3e} > {lim}"
+    return seen

@@ -12,39 +12,13 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_helpers import Case, assert_bf16_parity, max_abs, oracle_op, parse_shape, rel_l2
+from gpu_helpers import Case, assert_bf16_parity, check_all_ops, rel_l2
 
 pytestmark = pytest.mark.gpu
 
 BF16_MAX_ABS = 3e-2
 BF16_REL_L2 = 1e-2
 F32_REL_L2 = 1e-4
-
-# Per-op tolerances: one bf16 rounding of the output dominates (2^-9 relative).
-OP_TOL = {"bf16": dict(rel=6e-3, attn_rel=1.2e-2), "fp32": dict(rel=1e-5, attn_rel=1e-5)}
-
-
-def check_all_ops(case: Case, n_bands: int, stride: int = 1):
-    n_ops = case.dec.num_ops(case.shape, n_bands)
-    assert n_ops > 5
-    tol = OP_TOL[case.dtype]
-    seen = set()
-    for op in range(0, n_ops, stride):
-        d, x, aux, y = case.capture(n_bands, op)
-        seen.add(d["kind"] + ":" + d.get("conv", ""))
-        in_shape = parse_shape(d["in"])
-        if d["kind"] == "latent":
-            xin = x.reshape(case.shape)
-            exp = np.moveaxis(xin, 1, -1) if xin.ndim == 4 else np.moveaxis(xin, 1, -1)
-            np.testing.assert_array_equal(y.reshape(exp.shape), exp)
-            continue
-        ref = oracle_op(d, case.W, case.arch, x.reshape(in_shape), aux)
-        got = y.reshape(ref.shape)
-        lim = tol["attn_rel"] if d["kind"] == "attention" else tol["rel"]
-        err = rel_l2(got, ref)
-        assert err <= lim, f"op {op} {d}: rel-L2 {err:.3e} > {lim}"
-    return seen
-
 
 # ---------------------------------------------------------------- fp32 path
 @pytest.fixture(scope="module")
