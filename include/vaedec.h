@@ -217,6 +217,31 @@ vaedec_status vaedec_groupnorm_noalloc(int in_dtype, int out_dtype, const void* 
                                        int C, int G, const float* gamma, const float* beta, float eps, int silu,
                                        void* stream);
 
+/* ---- Band attention core ------------------------------------------------------------
+ * The fused kernel the bf16 decode runs for its mid-block attention, on caller buffers:
+ *   O[q, :] = softmax_k(Q[q, :] . K[k, :] / sqrt(C)) V[k, :]
+ * for every query row q of F frames of ntok = grid_h * grid_w tokens, each query against every
+ * key and value of its own frame ("VAEP：VAE 并行解码", Attention：本地 Q，全局 K/V).  The query
+ * rows of a frame are split into n_bands height bands of the grid_h x grid_w token grid (band b:
+ * floor(grid_h / n_bands) grid rows, the first grid_h mod n_bands bands one more); query tiles
+ * never cross a band.  The result does not depend on n_bands, bit for bit.
+ *   q, k   DEVICE bf16 [F][ntok][C] (token-major, channels contiguous)
+ *   vt     DEVICE bf16 [F][C][ntok] (V transposed: tokens contiguous)
+ *   o      DEVICE bf16 [F][ntok][C]; must not overlap q, k, vt or work
+ *   C a multiple of 128, at most 512; ntok a multiple of 8; 1 <= n_bands <= grid_h; all device
+ *   pointers 16-byte aligned
+ *   work   DEVICE scratch of work_bytes >= vaedec_band_attention_work_bytes(F, grid_h, grid_w, C)
+ *          (fp32 partials of the key splits; may be NULL when that size is 0)
+ *   status DEVICE int the kernel ORs a nonzero error bit into if one of its bounded waits runs out
+ *          (read it after the stream completes; the caller owns and clears it)
+ *   stream a cudaStream_t (NULL = legacy default stream); asynchronous, allocates nothing
+ * INVALID_ARG for a NULL pointer, a size or alignment outside these limits or too small a work
+ * buffer (before any launch); CUDA for a failed launch. */
+vaedec_status vaedec_band_attention_work_bytes(int F, int grid_h, int grid_w, int C, size_t* bytes);
+vaedec_status vaedec_band_attention(const void* q, const void* k, const void* vt, void* o, int F, int grid_h,
+                                    int grid_w, int C, int n_bands, void* work, size_t work_bytes, int* status,
+                                    void* stream);
+
 /* ---- Inspection (tests and profiling) ------------------------------------------------
  * The decode is a fixed list of ops (latent layout, conv, groupnorm, rmsnorm,
  * attention block, temporal upsample).  These calls describe that list for a latent

@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "vaedec_debug_num_ops", "vaedec_debug_op_desc", "vaedec_debug_run_until",
     "vaedec_groupnorm_noalloc", "vaedec_debug_inject_fault", "vaedec_debug_set_wait_limit",
     "vaedec_debug_wait_probe", "vaedec_band_axis", "vaedec_decode_bands",
+    "vaedec_band_attention_work_bytes", "vaedec_band_attention",
 )
 
 
@@ -96,6 +97,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.vaedec_debug_wait_probe.argtypes = [vp, vp]
     lib.vaedec_band_axis.argtypes = [i64p, i, i, i, ctypes.POINTER(i)]
     lib.vaedec_decode_bands.argtypes = [vp, vp, i64p, i, vp, i, i, vp]
+    lib.vaedec_band_attention_work_bytes.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+    lib.vaedec_band_attention.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp, ctypes.c_size_t, vp, vp]
     for name in EXPORTED_SYMBOLS:
         if name not in ("vaedec_destroy", "vaedec_last_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -189,6 +192,32 @@ def groupnorm_noalloc(x, y, groups: int, gamma, beta, eps: float, silu: bool, st
     _check(lib, lib.vaedec_groupnorm_noalloc(dt[x.dtype], dt[y.dtype], x.data_ptr(), y.data_ptr(), B, rows, W, C,
                                              int(groups), gamma.data_ptr(), beta.data_ptr(), float(eps),
                                              1 if silu else 0, int(st.cuda_stream)))
+
+
+def band_attention_work_bytes(F: int, grid_h: int, grid_w: int, C: int) -> int:
+    """Device scratch bytes ``band_attention`` needs for these sizes (0: none)."""
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    _check(lib, lib.vaedec_band_attention_work_bytes(int(F), int(grid_h), int(grid_w), int(C), ctypes.byref(n)))
+    return int(n.value)
+
+
+def band_attention(q, k, vt, out, grid_h: int, grid_w: int, n_bands: int, work, status, stream=None) -> None:
+    """softmax(Q K^T / sqrt(C)) V per frame with band-local queries, on the fused attention kernel.
+
+    ``q``/``k``/``out``: bf16 device tensors [F, ntok, C]; ``vt``: bf16 [F, C, ntok];
+    ``work``: a device tensor of at least ``band_attention_work_bytes`` bytes, or None when that is 0;
+    ``status``: an int32 device tensor the kernel ORs a timeout bit into.  Asynchronous on ``stream``.
+    """
+    lib = load_library()
+    torch = _torch()
+    F, ntok, C = (int(v) for v in q.shape)
+    st = torch.cuda.current_stream() if stream is None else stream
+    wp = work.data_ptr() if work is not None else None
+    wb = work.numel() * work.element_size() if work is not None else 0
+    _check(lib, lib.vaedec_band_attention(q.data_ptr(), k.data_ptr(), vt.data_ptr(), out.data_ptr(), F, int(grid_h),
+                                          int(grid_w), C, int(n_bands), wp, wb, status.data_ptr(),
+                                          int(st.cuda_stream)))
 
 
 def _torch():

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libvaedec.so"
-SOURCES = ["api.cu", "conv_tc.cu", "conv_halo.cu", "conv_halo_t.cu", "conv_narrow.cu", "conv_simple.cu", "norm.cu", "attn.cu", "gemm_cm.cu", "gn_noalloc.cu"]
+SOURCES = ["api.cu", "conv_tc.cu", "conv_halo.cu", "conv_halo_t.cu", "conv_narrow.cu", "conv_simple.cu", "norm.cu", "attn.cu", "attn_flash.cu", "gemm_cm.cu", "gn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

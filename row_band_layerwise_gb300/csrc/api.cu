@@ -7,9 +7,10 @@
 //    appears only outside the image ("VAEP：VAE 并行解码", 卷积：交换边界行);
 //  * GroupNorm statistics come from fixed one-row chunks merged with the
 //    weighted rule (GroupNorm：合并全局统计量), independent of the band split;
-//  * attention runs band by band: the band's query rows against every key and
-//    value of the frame (Attention：本地 Q，全局 K/V), so the score buffer is
-//    bounded by the largest band;
+//  * attention takes each band's query rows against every key and value of the
+//    frame (Attention：本地 Q，全局 K/V): on the bf16 path one fused kernel covers
+//    all bands, its query tiles never crossing a band, and no scores reach
+//    memory; the fp32 path runs band by band with one band's scores in memory;
 //  * SiLU, RMSNorm and upsampling are local (the upsample is folded into the
 //    next conv's addressing).
 #include <cuda_runtime.h>
@@ -117,14 +118,14 @@ struct vaedec {
   void* attn_k = nullptr;
   void* attn_vt = nullptr;
   size_t qkv_bytes = 0;
+  // fp32 path: one band's scores, probabilities and row sums
   float* attn_s = nullptr;
   void* attn_p = nullptr;
   float* attn_l = nullptr;
   size_t s_elems = 0, l_elems = 0;
-  // attention pipeline: each band's softmax runs on `side` while the next band's score GEMM runs on
-  // the decode stream; scores, probabilities and row sums have two slots (events order them)
-  cudaStream_t side = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_s[2] = {}, ev_p[2] = {};
+  // bf16 path: fp32 partial outputs and row maxima / sums of the fused attention's key splits
+  void* attn_work = nullptr;
+  size_t attn_work_bytes = 0;
   // width bands: a band's queries gathered dense, and its output before the scatter back
   void* attn_qg = nullptr;
   void* attn_ob = nullptr;
@@ -165,9 +166,6 @@ struct vaedec {
   }
   ~vaedec() {
     for (cudaEvent_t e : prof_ev) cudaEventDestroy(e);
-    for (cudaEvent_t e : {ev_fork, ev_join, ev_s[0], ev_s[1], ev_p[0], ev_p[1]})
-      if (e != nullptr) cudaEventDestroy(e);
-    if (side != nullptr) cudaStreamDestroy(side);
     for (void* p : allocs) cudaFree(p);
   }
 };
@@ -176,7 +174,7 @@ namespace {
 
 // Sizes a dry walk records for workspace planning.
 struct Plan {
-  size_t act = 0, qkv = 0, s = 0, l = 0, part = 0, sc = 0;
+  size_t act = 0, qkv = 0, s = 0, l = 0, part = 0, sc = 0, attn_work = 0;
 };
 
 class Walker {
@@ -465,16 +463,6 @@ class Walker {
     if (e != cudaSuccess) set_err(VAEDEC_ERR_CUDA, std::string(what) + ": " + (why ? why : cudaGetErrorString(e)));
   }
 
-  // Key-dimension split of the probabilities x values product: a function of the
-  // number of keys only, so every band count sums the same partial products in
-  // the same order.
-  // Up to 8192 keys the band GEMMs are small (a few 128 x 256 tiles): 8 splits of >= 512 keys (fewer
-  // when there are fewer keys) keep the SMs busy; above, one split per 4096 keys, at most 8.
-  static int pv_splits(long long ntok) {
-    const long long s = ntok <= 8192 ? (ntok + 511) / 512 : (ntok + 4095) / 4096;
-    return (int)std::max(1LL, std::min(8LL, s));
-  }
-
   static void fill_taps(ConvGeom& g, ConvKind kind, const DevConv& w) {
     std::memset(g.taps, 0, sizeof(g.taps));
     g.nphase = 1;
@@ -728,13 +716,15 @@ class Walker {
     const size_t oes = esz(odt_);
     if (plan) {
       plan->qkv = std::max(plan->qkv, (size_t)F * (size_t)Ntok * (size_t)C * oes);
-      int maxrows = 0;
-      for (int r : band_rows(x.H, n_bands_)) maxrows = std::max(maxrows, r);
-      plan->s = std::max(plan->s, (size_t)maxrows * (size_t)x.W * (size_t)Ntok);
-      if (pv_splits(Ntok) > 1)   // fp32 partials of the split probabilities x values product, in one
-                                 // fp16 score slot (half of the scores buffer)
-        plan->s = std::max(plan->s, 2 * (size_t)pv_splits(Ntok) * (size_t)maxrows * (size_t)x.W * (size_t)C);
-      plan->l = std::max(plan->l, (size_t)maxrows * x.W);
+      if (h_->dtype == kBF16) {
+        plan->attn_work = std::max(plan->attn_work, flash_work_bytes(F, Ntok, C));
+      } else {
+        // fp32 path: one band's scores, probabilities and row sums (the plan walks one band)
+        int maxrows = 0;
+        for (int r : band_rows(x.H, n_bands_)) maxrows = std::max(maxrows, r);
+        plan->s = std::max(plan->s, (size_t)maxrows * (size_t)x.W * (size_t)Ntok);
+        plan->l = std::max(plan->l, (size_t)maxrows * x.W);
+      }
     }
     note_act(y);
     // projections 4 x (2 N C^2) plus scores and probabilities x values 2 x (2 N^2 C), per sequence
@@ -804,122 +794,98 @@ class Walker {
         // whichever band holds it)
         const bool wband = axis_ == 1;
         const std::vector<int> rows = band_rows(wband ? x.W : x.H, n_bands_);
-        DevConv kview;
-        kview.ntaps = 1;
-        kview.cin = C;
-        kview.rows = (int)Ntok;
-        kview.cout = (int)Ntok;
-        DevConv vview;
-        vview.ntaps = 1;
-        vview.cin = (int)Ntok;
-        vview.rows = C;
-        vview.cout = C;
-        const float scale = 1.f / std::sqrt((float)C);
-        const bool tc = h_->dtype == kBF16;
-        // tensor-core path, pipelined over bands: S(b) on the decode stream, softmax(b) on the side
-        // stream (slot b % 2) while S(b + 1) runs, then P(b) x V on the decode stream
-        const bool overlap = tc && h_->side != nullptr;
-        cudaStream_t sm_st = overlap ? h_->side : st_;
-        struct Band {
-          int f, nr, slot;
-          size_t qoff;
-          void* o_band;
-          int c0, nc;   // width band: columns [c0, c0 + nc) of frame f, output scattered from o_band
-        };
-        auto scatter = [&](const Band& bd) {
-          if (!wband || !live()) return;
-          count();
-          check(launch_band_cols(odt_, bd.o_band, static_cast<char*>(ptr(hn)) + (size_t)bd.f * Ntok * C * oes, x.H,
-                                 x.W, C, bd.c0, bd.nc, 0, st_),
-                "attention band scatter");
-        };
-        bool have_pend = false;
-        Band pend{};
-        auto s_slot = [&](int slot) { return static_cast<void*>(reinterpret_cast<char*>(h_->attn_s) + slot * h_->s_elems * 2); };
-        auto p_slot = [&](int slot) { return static_cast<void*>(static_cast<char*>(h_->attn_p) + slot * h_->s_elems * oes); };
-        auto l_slot = [&](int slot) { return h_->attn_l + slot * h_->l_elems; };
-        auto run_pv = [&](const Band& bd) {
-          if (!live()) return;
-          if (overlap) check(cudaStreamWaitEvent(st_, h_->ev_p[bd.slot], 0), "attention join");
-          // O[q, c] = inv_l[q] * (V^T P^T)[c, q], channels on the lanes, keys split
-          const int splits = pv_splits(Ntok);
-          GemmArgs pa;
-          pa.A = static_cast<char*>(h_->attn_vt) + (size_t)bd.f * C * Ntok * oes;
-          pa.lda = Ntok;
-          pa.B = p_slot(bd.slot);
-          pa.ldb = Ntok;
-          pa.M = C;
-          pa.N = bd.nr;
-          pa.K = (int)Ntok;
-          pa.ldo = C;
-          pa.scale_n = l_slot(bd.slot);
-          pa.splits = splits;
-          if (splits > 1) {
-            pa.out = s_slot(bd.slot);   // fp32 partials; this band's scores are no longer needed
-            pa.out_f32 = 1;
-            pa.split_stride = (long long)bd.nr * C;
-            gemm(pa, "attention pv");
-            count();
-            check(launch_splitk_reduce(static_cast<const float*>(s_slot(bd.slot)), splits, (long long)bd.nr * C,
-                                       (long long)bd.nr * C, odt_, bd.o_band, st_),
-                  "attention pv reduce");
-          } else {
-            pa.out = bd.o_band;
-            pa.out_f32 = odt_ == kF32;
-            gemm(pa, "attention pv");
-          }
-          scatter(bd);
-        };
-        if (overlap) {
-          check(cudaEventRecord(h_->ev_fork, st_), "attention fork");
-          check(cudaStreamWaitEvent(h_->side, h_->ev_fork, 0), "attention fork");
-        }
-        int seq = 0;
-        for (int f = 0; f < F && live(); ++f) {
-          int r0 = 0;
-          for (int band = 0; band < n_bands_ && live(); ++band) {
-            const int nr = wband ? x.H * rows[band] : rows[band] * x.W;
-            // height band: its queries and its output are contiguous rows of the frame (O overwrites
-            // the band's normalised rows); width band: gathered / scattered through dense buffers
-            const size_t qoff = wband ? 0 : ((size_t)f * Ntok + (size_t)r0 * x.W) * C;
-            void* q_band = static_cast<char*>(wband ? h_->attn_qg : h_->attn_q) + qoff * oes;
-            void* o_band = wband ? h_->attn_ob : static_cast<void*>(static_cast<char*>(ptr(hn)) + qoff * oes);
-            if (wband) {
-              count();
-              check(launch_band_cols(odt_, static_cast<char*>(h_->attn_q) + (size_t)f * Ntok * C * oes, h_->attn_qg,
-                                     x.H, x.W, C, r0, rows[band], 1, st_),
-                    "attention band gather");
-            }
-            if (tc) {
-              const int slot = seq & 1;
-              // S[q, key] = (K Q^T)[key, q] / sqrt(C), keys on the accumulator lanes, stored fp16
-              GemmArgs sa;
-              sa.A = static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes;
-              sa.lda = C;
-              sa.B = q_band;
-              sa.ldb = C;
-              sa.M = (int)Ntok;
-              sa.N = nr;
-              sa.K = C;
-              sa.out = s_slot(slot);
-              sa.ldo = Ntok;
-              sa.out_f32 = 0;
-              sa.out_f16 = 1;
-              sa.scale = scale;
-              gemm(sa, "attention scores");
-              count();
-              if (overlap) {
-                check(cudaEventRecord(h_->ev_s[slot], st_), "attention scores event");
-                check(cudaStreamWaitEvent(h_->side, h_->ev_s[slot], 0), "attention scores event");
+        if (h_->dtype == kBF16) {
+          // fused tensor-core attention: one launch covers every band of every frame (query tiles
+          // never cross a band), then the merge of its key splits
+          void* q_src = h_->attn_q;
+          void* o_dst = ptr(hn);
+          if (wband) {
+            // frame f's width band b goes to rows f * Ntok + H * c0 of the gathered buffer
+            for (int f = 0; f < F && live(); ++f) {
+              int c0 = 0;
+              for (int band = 0; band < n_bands_ && live(); ++band) {
+                count();
+                if (live())
+                  check(launch_band_cols(odt_, static_cast<char*>(h_->attn_q) + (size_t)f * Ntok * C * oes,
+                                         static_cast<char*>(h_->attn_qg) + ((size_t)f * Ntok + (size_t)x.H * c0) * C * oes,
+                                         x.H, x.W, C, c0, rows[band], 1, st_),
+                        "attention band gather");
+                c0 += rows[band];
               }
-              check(launch_softmax_rows(odt_, s_slot(slot), 1, p_slot(slot), l_slot(slot), nr, (int)Ntok, sm_st),
-                    "softmax");
-              if (overlap) check(cudaEventRecord(h_->ev_p[slot], h_->side), "attention softmax event");
-              if (have_pend) run_pv(pend);
-              pend = Band{f, nr, slot, qoff, o_band, r0, rows[band]};
-              have_pend = true;
-              ++seq;
-            } else {
+            }
+            q_src = h_->attn_qg;
+            o_dst = h_->attn_ob;
+          }
+          FlashArgs fa;
+          fa.q = q_src;
+          fa.k = h_->attn_k;
+          fa.vt = h_->attn_vt;
+          fa.out = o_dst;
+          fa.part = static_cast<float*>(h_->attn_work);
+          fa.ml = static_cast<char*>(h_->attn_work) +
+                  (size_t)flash_splits(Ntok) * (size_t)F * (size_t)Ntok * (size_t)C * sizeof(float);
+          fa.F = F;
+          fa.ntok = Ntok;
+          fa.C = C;
+          fa.U = wband ? x.H : x.W;
+          fa.n_seg = n_bands_;
+          fa.seg_q = (wband ? x.W : x.H) / n_bands_;
+          fa.seg_rem = (wband ? x.W : x.H) % n_bands_;
+          if (flash_splits(Ntok) > 1 && h_->attn_work_bytes < flash_work_bytes(F, Ntok, C))
+            set_err(VAEDEC_ERR_INVALID_ARG, "attention workspace too small for this shape");
+          if (live()) {
+            count();
+            const char* why = nullptr;
+            cudaError_t e = live() ? launch_attn_flash(fa, h_->status, st_, &why) : cudaSuccess;
+            if (e != cudaSuccess)
+              set_err(VAEDEC_ERR_CUDA, std::string("attention: ") + (why ? why : cudaGetErrorString(e)));
+          }
+          if (live() && flash_splits(Ntok) > 1) {
+            count();
+            if (live()) check(launch_attn_combine(fa, st_), "attention key-split merge");
+          }
+          if (wband) {
+            for (int f = 0; f < F && live(); ++f) {
+              int c0 = 0;
+              for (int band = 0; band < n_bands_ && live(); ++band) {
+                count();
+                if (live())
+                  check(launch_band_cols(odt_, static_cast<char*>(h_->attn_ob) + ((size_t)f * Ntok + (size_t)x.H * c0) * C * oes,
+                                         static_cast<char*>(ptr(hn)) + (size_t)f * Ntok * C * oes, x.H, x.W, C, c0,
+                                         rows[band], 0, st_),
+                        "attention band scatter");
+                c0 += rows[band];
+              }
+            }
+          }
+        } else {
+          // fp32 path on the CUDA cores: per band, scores = Q K^T / sqrt(C), row softmax, P V
+          DevConv kview;
+          kview.ntaps = 1;
+          kview.cin = C;
+          kview.rows = (int)Ntok;
+          kview.cout = (int)Ntok;
+          DevConv vview;
+          vview.ntaps = 1;
+          vview.cin = (int)Ntok;
+          vview.rows = C;
+          vview.cout = C;
+          const float scale = 1.f / std::sqrt((float)C);
+          for (int f = 0; f < F && live(); ++f) {
+            int r0 = 0;
+            for (int band = 0; band < n_bands_ && live(); ++band) {
+              const int nr = wband ? x.H * rows[band] : rows[band] * x.W;
+              // height band: its queries and its output are contiguous rows of the frame (O overwrites
+              // the band's normalised rows); width band: gathered / scattered through dense buffers
+              const size_t qoff = wband ? 0 : ((size_t)f * Ntok + (size_t)r0 * x.W) * C;
+              void* q_band = static_cast<char*>(wband ? h_->attn_qg : h_->attn_q) + qoff * oes;
+              void* o_band = wband ? h_->attn_ob : static_cast<void*>(static_cast<char*>(ptr(hn)) + qoff * oes);
+              if (wband) {
+                count();
+                check(launch_band_cols(odt_, static_cast<char*>(h_->attn_q) + (size_t)f * Ntok * C * oes, h_->attn_qg,
+                                       x.H, x.W, C, r0, rows[band], 1, st_),
+                      "attention band gather");
+              }
               ConvGeom gs;
               std::memset(&gs, 0, sizeof(gs));
               gs.B = 1;
@@ -941,7 +907,7 @@ class Walker {
                      static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes, nullptr, nullptr, nullptr,
                      h_->attn_s, nullptr, "attention scores");
               count();
-              check(launch_softmax_rows(odt_, h_->attn_s, 0, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
+              check(launch_softmax_rows(odt_, h_->attn_s, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
               ConvGeom go = gs;
               go.Cin = (int)Ntok;
               go.Cout = C;
@@ -950,16 +916,15 @@ class Walker {
               go.scale = 1.f;
               launch(go, h_->attn_p, vview, static_cast<char*>(h_->attn_vt) + (size_t)f * C * Ntok * oes, nullptr,
                      nullptr, h_->attn_l, o_band, nullptr, "attention pv");
-              scatter(Band{f, nr, 0, qoff, o_band, r0, rows[band]});
+              if (wband && live()) {
+                count();
+                check(launch_band_cols(odt_, o_band, static_cast<char*>(ptr(hn)) + (size_t)f * Ntok * C * oes, x.H,
+                                       x.W, C, r0, rows[band], 0, st_),
+                      "attention band scatter");
+              }
+              r0 += rows[band];
             }
-            r0 += rows[band];
           }
-        }
-        if (have_pend) run_pv(pend);
-        if (overlap) {
-          // the side stream's work is part of this op: join it back (also after a stop)
-          check(cudaEventRecord(h_->ev_join, h_->side), "attention join");
-          check(cudaStreamWaitEvent(st_, h_->ev_join, 0), "attention join");
         }
         // output projection + residual in fp32
         ConvGeom gp = g;
@@ -1225,6 +1190,9 @@ vaedec_status validate_config(const vaedec_config* c) {
   }
   if (c->dtype == VAEDEC_DTYPE_BF16 && c->latent_channels % 16 != 0)
     return fail(VAEDEC_ERR_UNSUPPORTED, "bf16 path needs latent channels that are a multiple of 16");
+  if (c->dtype == VAEDEC_DTYPE_BF16 && (c->mid_channels % 128 != 0 || c->mid_channels > 512))
+    return fail(VAEDEC_ERR_UNSUPPORTED, "bf16 path: the fused mid-block attention needs a multiple of 128 channels, "
+                                        "at most 512");
   if (c->family == VAEDEC_FAMILY_KL2D && !(c->eps > 0.f)) return fail(VAEDEC_ERR_INVALID_ARG, "eps must be positive");
   if (c->latent_patch < 0 || c->latent_patch > 2) return fail(VAEDEC_ERR_UNSUPPORTED, "latent_patch must be 0, 1 or 2");
   if (c->latent_patch == 2 && c->family != VAEDEC_FAMILY_KL2D)
@@ -1488,11 +1456,13 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
   void* tmp = nullptr;
   if (s == VAEDEC_OK) s = h->dalloc(&tmp, plan.s * sizeof(float), "attention scores");
   h->attn_s = static_cast<float*>(tmp);
-  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_p, 2 * plan.s * h->es, "attention probabilities");
-  if (s == VAEDEC_OK) s = h->dalloc(&tmp, 2 * plan.l * sizeof(float), "attention row sums");
+  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_p, plan.s * h->es, "attention probabilities");
+  if (s == VAEDEC_OK) s = h->dalloc(&tmp, plan.l * sizeof(float), "attention row sums");
   h->attn_l = static_cast<float*>(tmp);
   h->s_elems = plan.s;
   h->l_elems = plan.l;
+  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_work, plan.attn_work, "attention key-split partials");
+  h->attn_work_bytes = plan.attn_work;
   if (s == VAEDEC_OK) s = h->dalloc(&tmp, std::max<size_t>(plan.part, 1) * sizeof(GnPartial), "groupnorm partials");
   h->gn_part = static_cast<GnPartial*>(tmp);
   if (s == VAEDEC_OK) s = h->dalloc(&tmp, std::max<size_t>(plan.sc, 1) * sizeof(float), "groupnorm scale");
@@ -1506,13 +1476,7 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
   if (s != VAEDEC_OK) return bail(s);
   cudaError_t e = cudaMemset(h->status, 0, sizeof(int));
   if (e != cudaSuccess) return bail(cuda_fail(e, "status init"));
-  if (s == VAEDEC_OK && plan.s > 0) {
-    cudaError_t es = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
-    for (cudaEvent_t* ev : {&h->ev_fork, &h->ev_join, &h->ev_s[0], &h->ev_s[1], &h->ev_p[0], &h->ev_p[1]})
-      if (es == cudaSuccess) es = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-    if (es != cudaSuccess) return bail(cuda_fail(es, "attention stream"));
-  }
-  h->ws_bytes = kNumAct * plan.act + 5 * plan.qkv + plan.s * (4 + 2 * h->es) + plan.l * 8 + plan.part * sizeof(GnPartial) +
+  h->ws_bytes = kNumAct * plan.act + 5 * plan.qkv + plan.s * (4 + h->es) + plan.l * 4 + plan.attn_work + plan.part * sizeof(GnPartial) +
                 2 * plan.sc * 4 + h->io_latent_bytes + h->io_out_bytes;
   *out = h;
   return VAEDEC_OK;
@@ -1620,6 +1584,57 @@ vaedec_status vaedec_decode_host(vaedec_t* h, const void* latent_host, const int
   return vaedec_sync(h, stream);
 }
 
+vaedec_status vaedec_band_attention_work_bytes(int F, int grid_h, int grid_w, int C, size_t* bytes) {
+  if (bytes == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  if (F < 1 || grid_h < 1 || grid_w < 1 || C < 1) return fail(VAEDEC_ERR_INVALID_ARG, "sizes must be positive");
+  *bytes = flash_work_bytes(F, (long long)grid_h * grid_w, C);
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_band_attention(const void* q, const void* k, const void* vt, void* o, int F, int grid_h,
+                                    int grid_w, int C, int n_bands, void* work, size_t work_bytes, int* status,
+                                    void* stream) {
+  if (q == nullptr || k == nullptr || vt == nullptr || o == nullptr || status == nullptr)
+    return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  if (F < 1 || grid_h < 1 || grid_w < 1) return fail(VAEDEC_ERR_INVALID_ARG, "sizes must be positive");
+  if (C < 128 || C > 512 || C % 128 != 0) return fail(VAEDEC_ERR_INVALID_ARG, "C must be a multiple of 128, at most 512");
+  const long long ntok = (long long)grid_h * grid_w;
+  if (ntok % 8 != 0) return fail(VAEDEC_ERR_INVALID_ARG, "grid_h * grid_w must be a multiple of 8");
+  if (n_bands < 1 || n_bands > grid_h) return fail(VAEDEC_ERR_INVALID_ARG, "n_bands must be in [1, grid_h]");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(vt) |
+       reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(work)) & 15)
+    return fail(VAEDEC_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  const size_t need = flash_work_bytes(F, ntok, C);
+  if (need > 0 && (work == nullptr || work_bytes < need))
+    return fail(VAEDEC_ERR_INVALID_ARG, "work buffer smaller than vaedec_band_attention_work_bytes (" +
+                                            std::to_string(need) + " bytes)");
+  FlashArgs fa;
+  fa.q = q;
+  fa.k = k;
+  fa.vt = vt;
+  fa.out = o;
+  fa.part = static_cast<float*>(work);
+  fa.ml = need > 0 ? static_cast<char*>(work) + (size_t)flash_splits(ntok) * (size_t)F * (size_t)ntok * C * sizeof(float)
+                   : nullptr;
+  fa.F = F;
+  fa.ntok = ntok;
+  fa.C = C;
+  fa.U = grid_w;
+  fa.n_seg = n_bands;
+  fa.seg_q = grid_h / n_bands;
+  fa.seg_rem = grid_h % n_bands;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const char* why = nullptr;
+  cudaError_t e = launch_attn_flash(fa, status, st, &why);
+  if (e == cudaSuccess) e = launch_attn_combine(fa, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(why ? VAEDEC_ERR_INVALID_ARG : VAEDEC_ERR_CUDA,
+                std::string("band attention: ") + (why ? why : cudaGetErrorString(e)));
+  }
+  return VAEDEC_OK;
+}
+
 vaedec_status vaedec_debug_inject_fault(int kind, int nth) {
   if (kind < 0 || kind > 2 || (kind != 0 && nth < 1)) return fail(VAEDEC_ERR_INVALID_ARG, "bad fault kind or count");
   g_fault_kind.store(0);
@@ -1634,6 +1649,7 @@ vaedec_status vaedec_debug_set_wait_limit(uint64_t ns) {
   if (e == cudaSuccess) e = set_wait_limit_conv_halo_t(ns);
   if (e == cudaSuccess) e = set_wait_limit_conv_narrow(ns);
   if (e == cudaSuccess) e = set_wait_limit_gemm_cm(ns);
+  if (e == cudaSuccess) e = set_wait_limit_attn_flash(ns);
   if (e != cudaSuccess) return fail(VAEDEC_ERR_CUDA, std::string("setting the wait limit: ") + cudaGetErrorString(e));
   return VAEDEC_OK;
 }

@@ -6,7 +6,6 @@
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -57,16 +56,9 @@ __device__ __forceinline__ float store_p<__nv_bfloat16>(__nv_bfloat16* p, float 
 }
 
 __device__ __forceinline__ float load_s(const float* p) { return *p; }
-__device__ __forceinline__ float load_s(const __half* p) { return __half2float(*p); }
 
-// Four consecutive scores (16-byte aligned for fp32, 8-byte for fp16), streamed once.
+// Four consecutive scores (16-byte aligned), streamed once.
 __device__ __forceinline__ float4 load_s4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
-__device__ __forceinline__ float4 load_s4(const __half* p) {
-  const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-  return make_float4(a.x, a.y, b.x, b.y);
-}
 
 template <typename SIn, typename P>
 __global__ void __launch_bounds__(kSmThreads) softmax_rows_kernel(const SIn* __restrict__ S, P* __restrict__ Pm,
@@ -162,55 +154,6 @@ __global__ void to_channels_last_kernel(const T* __restrict__ x, T* __restrict__
   }
 }
 
-// fp16 scores kept packed: a row of up to 8 * 8 * kSmThreads scores lives in registers as
-// __half2 pairs (half the registers of the fp32 form, so more rows are in flight per SM); the
-// maximum is taken on the stored values, the exponentials in fp32.
-template <typename P, int NV>
-__global__ void __launch_bounds__(kSmThreads) softmax_rows_h8_kernel(const __half* __restrict__ S, P* __restrict__ Pm,
-                                                                     float* __restrict__ inv_l, int nk) {
-  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
-  __shared__ float red[32];
-  const long long row = blockIdx.x;
-  const uint4* s8 = reinterpret_cast<const uint4*>(S + row * nk);
-  P* p = Pm + row * nk;
-  const int n8 = nk >> 3;
-  uint4 v[NV];
-  __half2 m2 = __float2half2_rn(-65504.f);
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int idx = threadIdx.x + i * kSmThreads;
-    if (idx < n8) {
-      v[i] = __ldcs(s8 + idx);
-      const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
-      m2 = __hmax2(m2, __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3])));
-    }
-  }
-  float m = fmaxf(__low2float(m2), __high2float(m2));
-  m = block_reduce_max(m, red);
-  float l = 0.f;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int idx = threadIdx.x + i * kSmThreads;
-    if (idx < n8) {
-      const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const float2 a = __half22float2(h[2 * q]);
-        const float2 b = __half22float2(h[2 * q + 1]);
-        float4 e;
-        e.x = __expf(a.x - m);
-        e.y = __expf(a.y - m);
-        e.z = __expf(b.x - m);
-        e.w = __expf(b.y - m);
-        l += store_p4<P>(p + 8 * idx + 4 * q, e);
-      }
-    }
-  }
-  l = block_reduce_sum(l, red);
-  if (threadIdx.x == 0) inv_l[row] = 1.f / l;
-}
-
 template <typename SIn>
 cudaError_t softmax_rows_t(int p_dtype, const SIn* S, void* P, float* inv_l, int rows, int nk, cudaStream_t stream) {
   const bool bf = p_dtype == kBF16;
@@ -241,30 +184,10 @@ cudaError_t softmax_rows_t(int p_dtype, const SIn* S, void* P, float* inv_l, int
 
 }  // namespace
 
-cudaError_t launch_softmax_rows(int p_dtype, const void* S, int s_f16, void* P, float* inv_l, int rows, int nk,
+cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv_l, int rows, int nk,
                                 cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  if (s_f16 && nk % 8 == 0 && nk <= 8 * 8 * kSmThreads) {
-    const int nv = (nk + 8 * kSmThreads - 1) / (8 * kSmThreads);
-    const __half* sh = static_cast<const __half*>(S);
-    const bool bf = p_dtype == kBF16;
-#define VD_SOFTMAX_H8(NV)                                                                                     \
-  if (nv <= NV) {                                                                                             \
-    if (bf)                                                                                                   \
-      launch_pdl(softmax_rows_h8_kernel<__nv_bfloat16, NV>,                                                               \
-          rows, kSmThreads, 0, stream, sh, static_cast<__nv_bfloat16*>(P), inv_l, nk);                   \
-    else                                                                                                      \
-      launch_pdl(softmax_rows_h8_kernel<float, NV>, rows, kSmThreads, 0, stream, sh, static_cast<float*>(P), inv_l, nk); \
-    return cudaGetLastError();                                                                                \
-  }
-    VD_SOFTMAX_H8(1)
-    VD_SOFTMAX_H8(2)
-    VD_SOFTMAX_H8(4)
-    VD_SOFTMAX_H8(8)
-#undef VD_SOFTMAX_H8
-  }
-  if (s_f16) return softmax_rows_t(p_dtype, static_cast<const __half*>(S), P, inv_l, rows, nk, stream);
-  return softmax_rows_t(p_dtype, static_cast<const float*>(S), P, inv_l, rows, nk, stream);
+  return softmax_rows_t(p_dtype, S, P, inv_l, rows, nk, stream);
 }
 
 cudaError_t launch_to_channels_last(int dtype, const void* x, void* y, int B, int C, long long spatial,

@@ -135,10 +135,41 @@ cudaError_t launch_splitk_reduce(const float* part, int splits, long long split_
 
 // ---------------------------------------------------------------- attention
 // Row softmax numerators: P[r, k] = exp(S[r, k] - max_k S[r, :]) stored as
-// `p_dtype`, inv_l[r] = 1 / sum_k P[r, k] (sum of the stored values).  S is fp32,
-// or fp16 when `s_f16`.
-cudaError_t launch_softmax_rows(int p_dtype, const void* S, int s_f16, void* P, float* inv_l, int rows, int nk,
+// `p_dtype`, inv_l[r] = 1 / sum_k P[r, k] (sum of the stored values); S fp32.
+cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv_l, int rows, int nk,
                                 cudaStream_t stream);
+
+// Fused (flash-style) band attention, bf16 operands, fp32 softmax and accumulation:
+//   O[q, :] = softmax_k(Q[q, :] . K[k, :] / sqrt(C)) V[k, :]
+// for every query row q of `q` ([F * ntok][C] channels-last, frame f's rows at f * ntok) against
+// every key of its own frame (`k` [F][ntok][C]; `vt` = V transposed, [F][C][ntok]).  The queries of
+// a frame form n_seg consecutive band segments: the first seg_rem hold (seg_q + 1) * U rows, the
+// others seg_q * U; query tiles never cross a segment.  A query row's arithmetic depends only on its
+// row and on ntok, not on the segments.  Output bf16 [F * ntok][C] at `out` (the same row index as
+// the query).  With flash_splits(ntok) > 1 the keys are split into that many ranges whose fp32
+// partial outputs (`part`, [splits][F * ntok][C]) and row maxima/sums (`ml`, [splits][F * ntok]
+// float2) are merged in split order by a second kernel.  C a multiple of 128 up to 512, ntok a
+// multiple of 8, all pointers 16-byte aligned.
+struct FlashArgs {
+  const void* q = nullptr;
+  const void* k = nullptr;
+  const void* vt = nullptr;
+  void* out = nullptr;
+  float* part = nullptr;
+  void* ml = nullptr;
+  int F = 0;
+  long long ntok = 0;
+  int C = 0;
+  int U = 0, seg_q = 0, seg_rem = 0, n_seg = 0;
+};
+int flash_splits(long long ntok);
+// Bytes of `part` plus `ml` that launch_attn_flash needs (0 when flash_splits(ntok) == 1).
+size_t flash_work_bytes(int F, long long ntok, int C);
+// The attention kernel, then (a separate launch, nothing when there is one split) the merge of the
+// key splits into `out`.
+cudaError_t launch_attn_flash(const FlashArgs& a, int* status, cudaStream_t stream, const char** why);
+cudaError_t launch_attn_combine(const FlashArgs& a, cudaStream_t stream);
+cudaError_t set_wait_limit_attn_flash(unsigned long long ns);
 
 // ---------------------------------------------------------------- layout
 // [B][C][S] -> [B][S][C] (same dtype).
