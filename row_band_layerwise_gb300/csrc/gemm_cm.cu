@@ -20,7 +20,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <cstring>
@@ -50,7 +49,7 @@ struct GemmParams {
   uint32_t a_stage, b_stage, acc_cols, tmem_cols;
   void* out;
   long long ldo, split_stride;
-  int out_f32, out_f16, res_f32;   // output fp32, fp16, else bf16
+  int out_f32, res_f32;   // output fp32, else bf16
   const float* bias_m;
   const float* bias_n;
   const float* scale_n;
@@ -291,10 +290,6 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
             float* sp = reinterpret_cast<float*>(stg) + ml;
 #pragma unroll
             for (int j = 0; j < 32; ++j) sp[j * 128] = v[j];
-          } else if (p.out_f16) {
-            __half* sp = reinterpret_cast<__half*>(stg) + ml;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sp[j * 128] = __float2half_rn(v[j]);
           } else {
             __nv_bfloat16* sp = reinterpret_cast<__nv_bfloat16*>(stg) + ml;
 #pragma unroll
@@ -367,11 +362,6 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
 #pragma unroll
               for (int j = 0; j < kGCols; ++j)
                 if (j < nvalid) op[j * p.ldo] = v[j];
-            } else if (p.out_f16) {
-              __half* op = reinterpret_cast<__half*>(outp) + e0;
-#pragma unroll
-              for (int j = 0; j < kGCols; ++j)
-                if (j < nvalid) op[j * p.ldo] = __float2half_rn(v[j]);
             } else {
               __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(outp) + e0;
 #pragma unroll
@@ -404,51 +394,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
 
 int round_up_g(int a, int b) { return (a + b - 1) / b * b; }
 
-// out[i] = sum over splits s (in order) of part[s * stride + i]; four values per thread.
-template <typename O>
-__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, long long stride, long long n4,
-                                     O* __restrict__ out) {
-  pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
-    float4 acc = reinterpret_cast<const float4*>(part)[i];
-    for (int s = 1; s < splits; ++s) {
-      const float4 v = reinterpret_cast<const float4*>(part + s * stride)[i];
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    if constexpr (sizeof(O) == 4) {
-      reinterpret_cast<float4*>(out)[i] = acc;
-    } else {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&lo);
-      u.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(out)[i] = u;
-    }
-  }
-}
-
 }  // namespace
-
-cudaError_t launch_splitk_reduce(const float* part, int splits, long long split_stride, long long count,
-                                 int out_dtype, void* out, cudaStream_t stream) {
-  if (count <= 0) return cudaSuccess;
-  if ((count % 4) || (split_stride % 4)) return cudaErrorInvalidValue;
-  const long long n4 = count / 4;
-  long long blocks = (n4 + 255) / 256;
-  if (blocks > 152LL * 8) blocks = 152LL * 8;
-  if (out_dtype == kBF16)
-    launch_pdl(splitk_reduce_kernel<__nv_bfloat16>, (int)blocks, 256, 0, stream, part, splits, split_stride, n4,
-                                                                          static_cast<__nv_bfloat16*>(out));
-  else
-    launch_pdl(splitk_reduce_kernel<float>, (int)blocks, 256, 0, stream, part, splits, split_stride, n4,
-                                                                  static_cast<float*>(out));
-  return cudaGetLastError();
-}
 
 cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, const char** why) {
   *why = nullptr;
@@ -496,7 +442,6 @@ cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, 
   p.ldo = a.ldo;
   p.split_stride = a.split_stride;
   p.out_f32 = a.out_f32;
-  p.out_f16 = a.out_f32 ? 0 : a.out_f16;
   p.res_f32 = a.res_f32;
   p.bias_m = a.bias_m;
   p.bias_n = a.bias_n;
@@ -533,8 +478,7 @@ cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, 
     const cuuint64_t strides[2] = {(cuuint64_t)(a.ldo * oes),
                                    (cuuint64_t)(p.splits > 1 ? a.split_stride * oes : a.ldo * oes * a.N)};
     const cuuint32_t box[3] = {128, 32, 1};
-    const CUtensorMapDataType odt = a.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                   : (a.out_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    const CUtensorMapDataType odt = a.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (enc(&p.tmO, odt, 3, a.out, dims,
             strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {

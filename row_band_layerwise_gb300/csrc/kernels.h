@@ -107,7 +107,7 @@ cudaError_t launch_rms_norm(int in_dtype, int out_dtype, const void* x, void* y,
 // (+ residual), stored channel-major: out[n * ldo + m].  A is [M][lda] and B
 // [N][ldb] bf16, K contiguous, rows 16-byte aligned.  With splits > 1 the K range
 // is divided among `splits` CTAs that write fp32 partials to
-// out + s * split_stride (combine them with launch_splitk_reduce).
+// out + s * split_stride (for the caller to sum in split order).
 struct GemmArgs {
   const void* A = nullptr;
   long long lda = 0;
@@ -117,7 +117,6 @@ struct GemmArgs {
   void* out = nullptr;
   long long ldo = 0;
   int out_f32 = 1;
-  int out_f16 = 0;                  // with out_f32 == 0: fp16 output instead of bf16
   int splits = 1;
   long long split_stride = 0;
   const float* bias_m = nullptr;
@@ -129,9 +128,6 @@ struct GemmArgs {
   void* out2 = nullptr;             // optional bf16 copy of out
 };
 cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, const char** why);
-// out[i] = sum_s part[s * split_stride + i] for i < count (count, split_stride multiples of 4).
-cudaError_t launch_splitk_reduce(const float* part, int splits, long long split_stride, long long count,
-                                 int out_dtype, void* out, cudaStream_t stream);
 
 // ---------------------------------------------------------------- attention
 // Row softmax numerators: P[r, k] = exp(S[r, k] - max_k S[r, :]) stored as

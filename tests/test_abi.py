@@ -110,3 +110,18 @@ def test_latent_frontend_config_checked_without_cuda(lib):
     cfg = rbl.make_config(dataclasses.replace(synth.WAN, latent_patch=2), "bf16", (1, 2, 8, 8))
     assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 1   # a KL2D option only
     assert not h.value
+
+
+def test_bf16_attention_width_checked_without_cuda(lib):
+    """The bf16 path's fused mid-block attention takes a multiple of 128 channels up to 512:
+    other widths are refused at create time, before any device work."""
+    import dataclasses
+    h = ctypes.c_void_p()
+    narrow = dataclasses.replace(synth.KL_TINY, latent_channels=16, mid_channels=64, stage_channels=(64,))
+    cfg = rbl.make_config(narrow, "bf16", (1, 1, 16, 16))
+    assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 2
+    assert b"128" in lib.vaedec_last_error()
+    wide = dataclasses.replace(narrow, mid_channels=640, stage_channels=(640,))
+    cfg = rbl.make_config(wide, "bf16", (1, 1, 16, 16))
+    assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 2
+    assert not h.value

@@ -1,9 +1,8 @@
 """GPU parity of the attention block at sizes that span many tensor-core tiles.
 
-4608 keys per frame is above the point where the probabilities x values product
-is split along the keys (fp32 partials combined in a fixed order), and 72 rows
-cut into 5 bands gives ragged band heights (15, 15, 14, 14, 14), so query tiles
-end mid-band.  The attention op's output is compared with the oracle's
+4608 keys per frame is above the point where the fused attention splits the keys
+into ranges (fp32 partials merged in a fixed order), and 72 rows cut into 5 bands
+gives ragged band heights (15, 15, 14, 14, 14), so query tiles end mid-band.  The attention op's output is compared with the oracle's
 attention block applied to the same captured input, and the op output must not
 depend on the band count at all (band-local queries against global keys).
 """
