@@ -82,9 +82,10 @@ def test_bounded_wait_runs_out_and_the_handle_recovers(case, clean):
 
 @pytest.mark.parametrize("axis", ["height", "width"])
 def test_refused_launch_at_every_point_of_the_attention_op(case, clean, axis):
-    """A decode stopped at any launch inside the attention op (whose band softmax runs on the
-    handle's second stream, forked from and joined back to the caller's stream) leaves nothing
-    running on that stream: the next decode on the same handle is bit-identical to a clean one."""
+    """A decode stopped at any launch inside the attention op (norm, projections, width-band
+    gathers, the fused attention kernel, its key-split merge, scatters, output projection) leaves
+    nothing half-done that the next decode could see: the next decode on the same handle is
+    bit-identical to a clean one."""
     torch, rbl = require_gpu()
     n_bands = 4
     ops = case.dec.ops(SHAPE, n_bands)
