@@ -1,9 +1,8 @@
 """A decode captured into a CUDA graph replays with exactly the bits of the eager decode.
 
-The library's decode is stream-ordered device work only (kernel launches, some of them
-programmatically dependent on the previous kernel, and events that fork the attention softmax onto
-an internal stream and join it back), so a caller can capture it once and replay it, the usual way to
-take per-launch host cost out of a serving loop.  The replay must also follow a new latent written
+The library's decode is stream-ordered device work only (kernel launches on the caller's stream,
+each programmatically dependent on the previous kernel), so a caller can capture it once and replay
+it, the usual way to take per-launch host cost out of a serving loop.  The replay must also follow a new latent written
 into the captured input buffer.
 """
 import pytest
