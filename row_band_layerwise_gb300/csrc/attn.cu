@@ -48,12 +48,6 @@ __device__ __forceinline__ float store_p<float>(float* p, float v) {
   *p = v;
   return v;
 }
-template <>
-__device__ __forceinline__ float store_p<__nv_bfloat16>(__nv_bfloat16* p, float v) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(v);
-  *p = h;
-  return __bfloat162float(h);
-}
 
 __device__ __forceinline__ float load_s(const float* p) { return *p; }
 
@@ -88,17 +82,6 @@ template <>
 __device__ __forceinline__ float store_p4<float>(float* p, float4 v) {
   *reinterpret_cast<float4*>(p) = v;
   return (v.x + v.y) + (v.z + v.w);
-}
-template <>
-__device__ __forceinline__ float store_p4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-  uint2 u;
-  u.x = *reinterpret_cast<const uint32_t*>(&lo);
-  u.y = *reinterpret_cast<const uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(p) = u;
-  const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
-  return (a.x + a.y) + (b.x + b.y);
 }
 
 template <typename SIn, typename P, int NV>
@@ -155,18 +138,13 @@ __global__ void to_channels_last_kernel(const T* __restrict__ x, T* __restrict__
 }
 
 template <typename SIn>
-cudaError_t softmax_rows_t(int p_dtype, const SIn* S, void* P, float* inv_l, int rows, int nk, cudaStream_t stream) {
-  const bool bf = p_dtype == kBF16;
+cudaError_t softmax_rows_t(const SIn* S, float* P, float* inv_l, int rows, int nk, cudaStream_t stream) {
   if (nk % 4 == 0 && nk <= 16 * 4 * kSmThreads) {
     const int nv = (nk + 4 * kSmThreads - 1) / (4 * kSmThreads);
-#define VD_SOFTMAX_REG(NV)                                                                                         \
-  if (nv <= NV) {                                                                                                  \
-    if (bf)                                                                                                        \
-      launch_pdl(softmax_rows_reg_kernel<SIn, __nv_bfloat16, NV>,                                                              \
-          rows, kSmThreads, 0, stream, S, static_cast<__nv_bfloat16*>(P), inv_l, nk);                         \
-    else                                                                                                           \
-      launch_pdl(softmax_rows_reg_kernel<SIn, float, NV>, rows, kSmThreads, 0, stream, S, static_cast<float*>(P), inv_l, nk); \
-    return cudaGetLastError();                                                                                     \
+#define VD_SOFTMAX_REG(NV)                                                                                \
+  if (nv <= NV) {                                                                                         \
+    launch_pdl(softmax_rows_reg_kernel<SIn, float, NV>, rows, kSmThreads, 0, stream, S, P, inv_l, nk);    \
+    return cudaGetLastError();                                                                            \
   }
     VD_SOFTMAX_REG(2)
     VD_SOFTMAX_REG(4)
@@ -174,11 +152,7 @@ cudaError_t softmax_rows_t(int p_dtype, const SIn* S, void* P, float* inv_l, int
     VD_SOFTMAX_REG(16)
 #undef VD_SOFTMAX_REG
   }
-  if (bf)
-    launch_pdl(softmax_rows_kernel<SIn, __nv_bfloat16>, rows, kSmThreads, 0, stream, S, static_cast<__nv_bfloat16*>(P), inv_l,
-                                                                             nk);
-  else
-    launch_pdl(softmax_rows_kernel<SIn, float>, rows, kSmThreads, 0, stream, S, static_cast<float*>(P), inv_l, nk);
+  launch_pdl(softmax_rows_kernel<SIn, float>, rows, kSmThreads, 0, stream, S, P, inv_l, nk);
   return cudaGetLastError();
 }
 
@@ -187,7 +161,8 @@ cudaError_t softmax_rows_t(int p_dtype, const SIn* S, void* P, float* inv_l, int
 cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv_l, int rows, int nk,
                                 cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  return softmax_rows_t(p_dtype, S, P, inv_l, rows, nk, stream);
+  if (p_dtype != kF32) return cudaErrorInvalidValue;   // the fp32 path's probabilities
+  return softmax_rows_t(S, static_cast<float*>(P), inv_l, rows, nk, stream);
 }
 
 cudaError_t launch_to_channels_last(int dtype, const void* x, void* y, int B, int C, long long spatial,

@@ -130,8 +130,8 @@ struct GemmArgs {
 cudaError_t launch_gemm_cm(const GemmArgs& a, int* status, cudaStream_t stream, const char** why);
 
 // ---------------------------------------------------------------- attention
-// Row softmax numerators: P[r, k] = exp(S[r, k] - max_k S[r, :]) stored as
-// `p_dtype`, inv_l[r] = 1 / sum_k P[r, k] (sum of the stored values); S fp32.
+// Row softmax numerators of the fp32 path: P[r, k] = exp(S[r, k] - max_k S[r, :]), inv_l[r] =
+// 1 / sum_k P[r, k]; S and P fp32 (p_dtype must be kF32).
 cudaError_t launch_softmax_rows(int p_dtype, const float* S, void* P, float* inv_l, int rows, int nk,
                                 cudaStream_t stream);
 
