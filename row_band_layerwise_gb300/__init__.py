@@ -17,7 +17,7 @@ import numpy as np
 from .build import lib_path
 
 __all__ = ["Decoder", "VaedecError", "load_library", "EXPORTED_SYMBOLS", "STATUS_NAMES", "inject_fault",
-           "band_axis", "BAND_AXES",
+           "band_axis", "BAND_AXES", "band_attention", "band_attention_work_bytes", "groupnorm_noalloc",
            "set_wait_limit"]
 
 FAMILY = {"kl2d": 1, "wan3d": 2}
