@@ -170,6 +170,7 @@ struct vaedec {
   struct HostGraph {
     int64_t shape[5];
     int ndim, n_bands;
+    unsigned long long launches;   // kernels in the graph (added to `launches` per replay)
     cudaGraphExec_t exec;
   };
   std::vector<HostGraph> host_graphs;
@@ -1576,13 +1577,14 @@ vaedec_status vaedec_sync(vaedec_t* h, void* stream) {
 
 namespace {
 
-// The cached graph of the host-path decode for this shape and band count, captured on first use;
+// The cached graph of the host-path decode for this shape and band count, captured on first use (the
+// pointer stays valid until the next capture: the cache only grows);
 // null (decode eagerly) while per-op profiling or fault injection is on, when the cache is full, or
 // if the capture did not succeed (the eager decode then reports whatever went wrong).
-cudaGraphExec_t host_graph(vaedec* h, const int64_t* shape, int ndim, int n_bands) {
+const vaedec::HostGraph* host_graph(vaedec* h, const int64_t* shape, int ndim, int n_bands) {
   if (h->profile || g_fault_kind.load() != 0) return nullptr;
   for (const vaedec::HostGraph& g : h->host_graphs)
-    if (g.ndim == ndim && g.n_bands == n_bands && std::equal(shape, shape + ndim, g.shape)) return g.exec;
+    if (g.ndim == ndim && g.n_bands == n_bands && std::equal(shape, shape + ndim, g.shape)) return &g;
   if (h->host_graphs.size() >= 16) return nullptr;
   if (h->capture_stream == nullptr &&
       cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
@@ -1594,8 +1596,11 @@ cudaGraphExec_t host_graph(vaedec* h, const int64_t* shape, int ndim, int n_band
     cudaGetLastError();
     return nullptr;
   }
+  const unsigned long long before = h->launches;
   Walker w(h, h->capture_stream, false, n_bands);
   const vaedec_status s = w.run(h->io_latent, shape, ndim, h->io_out);
+  const unsigned long long n_launch = h->launches - before;
+  h->launches = before;   // counted when the graph is launched
   cudaGraph_t graph = nullptr;
   cudaError_t e = cudaStreamEndCapture(h->capture_stream, &graph);
   cudaGraphExec_t exec = nullptr;
@@ -1610,9 +1615,10 @@ cudaGraphExec_t host_graph(vaedec* h, const int64_t* shape, int ndim, int n_band
   std::copy(shape, shape + ndim, g.shape);
   g.ndim = ndim;
   g.n_bands = n_bands;
+  g.launches = n_launch;
   g.exec = exec;
   h->host_graphs.push_back(g);
-  return exec;
+  return &h->host_graphs.back();
 }
 
 }  // namespace
@@ -1633,10 +1639,11 @@ vaedec_status vaedec_decode_host(vaedec_t* h, const void* latent_host, const int
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(h->io_latent, latent_host, in_b, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "latent upload");
-  cudaGraphExec_t exec = host_graph(h, shape, ndim, n_bands);
-  if (exec != nullptr) {
-    e = cudaGraphLaunch(exec, st);
+  const vaedec::HostGraph* hg = host_graph(h, shape, ndim, n_bands);
+  if (hg != nullptr) {
+    e = cudaGraphLaunch(hg->exec, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode graph launch");
+    h->launches += hg->launches;
   } else {
     s = vaedec_decode(h, h->io_latent, shape, ndim, h->io_out, n_bands, stream);
     if (s != VAEDEC_OK) return s;

@@ -15,12 +15,17 @@ pytestmark = pytest.mark.gpu
 
 def _check(torch, dec, shape, n_bands, seed):
     z = synth.make_latent(shape, "bf16", seed=seed)
+    n0 = dec.launch_count()
     ref = dec.decode(torch.from_numpy(z).cuda().to(torch.bfloat16), n_bands).cpu()
     torch.cuda.synchronize()
+    n_dev = dec.launch_count() - n0
     zh = torch.from_numpy(z).to(torch.bfloat16).pin_memory()
     oh = torch.empty(dec.output_shape(shape), dtype=torch.bfloat16).pin_memory()
+    n0 = dec.launch_count()
     dec.decode_host(zh, oh, n_bands)
     assert torch.equal(oh, ref), (shape, n_bands)
+    # the launch counter sees the same kernels whether the call decoded eagerly or replayed a graph
+    assert dec.launch_count() - n0 == n_dev
 
 
 @pytest.mark.parametrize("arch_name,shapes,max_latent", [
