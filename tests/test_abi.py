@@ -125,3 +125,31 @@ def test_bf16_attention_width_checked_without_cuda(lib):
     cfg = rbl.make_config(wide, "bf16", (1, 1, 16, 16))
     assert lib.vaedec_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == 2
     assert not h.value
+
+
+def test_band_attention_workspace_and_arguments_checked_without_cuda(lib):
+    """Host logic of vaedec_band_attention: the key-split workspace size (one split per 2048 keys,
+    at most 4; each split holds an fp32 output row and a (max, sum) pair per query) and the argument
+    checks, all before any device work (the pointers below are never dereferenced)."""
+    n = ctypes.c_size_t(7)
+    assert lib.vaedec_band_attention_work_bytes(1, 128, 128, 512, ctypes.byref(n)) == 0
+    assert n.value == 4 * 16384 * (512 * 4 + 8)
+    assert lib.vaedec_band_attention_work_bytes(5, 60, 104, 384, ctypes.byref(n)) == 0
+    assert n.value == 3 * 5 * 6240 * (384 * 4 + 8)
+    assert lib.vaedec_band_attention_work_bytes(1, 32, 32, 512, ctypes.byref(n)) == 0
+    assert n.value == 0                                     # 1024 keys: one split, no workspace
+    assert lib.vaedec_band_attention_work_bytes(0, 8, 8, 512, ctypes.byref(n)) != 0
+    fake = ctypes.c_void_p(1 << 20)                         # 16-byte aligned, never touched
+    st = ctypes.c_void_p(1 << 21)
+    call = lib.vaedec_band_attention
+    assert call(None, fake, fake, fake, 1, 8, 8, 512, 1, None, 0, st, None) == 1           # NULL q
+    assert call(fake, fake, fake, fake, 1, 8, 8, 512, 1, None, 0, None, None) == 1         # NULL status
+    assert call(fake, fake, fake, fake, 1, 8, 8, 96, 1, None, 0, st, None) == 1            # C not x128
+    assert call(fake, fake, fake, fake, 1, 8, 8, 1024, 1, None, 0, st, None) == 1          # C > 512
+    assert call(fake, fake, fake, fake, 1, 3, 5, 512, 1, None, 0, st, None) == 1           # 15 keys
+    assert call(fake, fake, fake, fake, 1, 8, 8, 512, 9, None, 0, st, None) == 1           # bands > rows
+    assert call(fake, fake, fake, fake, 1, 8, 8, 512, 0, None, 0, st, None) == 1           # no bands
+    assert call(ctypes.c_void_p((1 << 20) + 8), fake, fake, fake, 1, 8, 8, 512, 1, None, 0, st,
+                None) == 1                                                                # misaligned
+    assert call(fake, fake, fake, fake, 1, 64, 64, 512, 1, None, 0, st, None) == 1        # needs work
+    assert b"work" in lib.vaedec_last_error()
