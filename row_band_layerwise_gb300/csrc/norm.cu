@@ -241,7 +241,7 @@ __device__ __forceinline__ void load8f(const float* p, float (&o)[8]) {
 }
 
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(256) gn_apply_kernel(const Tin* __restrict__ x, Tout* __restrict__ y,
+__global__ void __launch_bounds__(1024) gn_apply_kernel(const Tin* __restrict__ x, Tout* __restrict__ y,
                                                        Tout* __restrict__ y_raw, uint32_t nvec,
                                                        uint32_t vec_per_sample, int C, int vpp_log2,
                                                        const float* __restrict__ scale,
@@ -421,6 +421,15 @@ void gn_apply_t(const void* x, void* y, void* y_raw, long long nvec, long long v
   const int vpp = C / 8;
   const int vpp_log2 = (vpp & (vpp - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(vpp)) : -1;
   static const int occ = blocks_per_sm(gn_apply_kernel<Tin, Tout>, threads);
+  if (nvec < (8LL << 20)) {
+    // tensors of the small layers (input mostly still in L2): one 1024-thread CTA per SM starts and
+    // drains faster than five 256-thread ones (measured 2.161 -> 2.127 ms for the 1024x1024 decode's
+    // GroupNorms); the kernel is grid-stride, so the result does not depend on the grid
+    launch_pdl(gn_apply_kernel<Tin, Tout>, sm_count(), 1024, 0, stream, static_cast<const Tin*>(x),
+               static_cast<Tout*>(y), static_cast<Tout*>(y_raw), static_cast<uint32_t>(nvec),
+               static_cast<uint32_t>(vps), C, vpp_log2, scale, shift, silu);
+    return;
+  }
   launch_pdl(gn_apply_kernel<Tin, Tout>, grid_for(nvec, threads, occ), threads, 0, stream, 
       static_cast<const Tin*>(x), static_cast<Tout*>(y), static_cast<Tout*>(y_raw), static_cast<uint32_t>(nvec),
       static_cast<uint32_t>(vps), C, vpp_log2, scale, shift, silu);
