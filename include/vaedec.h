@@ -167,11 +167,7 @@ vaedec_status vaedec_decode_bands(vaedec_t* h, const void* latent, const int64_t
  * Same as vaedec_decode with HOST buffers: copies the latent host->device, decodes,
  * copies the output device->host, and synchronises `stream` before returning.
  * Host buffers should be pinned for full copy bandwidth.  Also reports kernel-side
- * failures (TIMEOUT).  The first call for a latent shape and band count captures the
- * decode of the handle's staging buffers into a CUDA graph (on a stream of the handle's
- * own), later calls replay it on `stream`; results are the same bits either way.  The
- * handle keeps up to 16 such graphs until vaedec_destroy; with per-op profiling or
- * fault injection on, the call decodes eagerly.
+ * failures (TIMEOUT).
  */
 vaedec_status vaedec_decode_host(vaedec_t* h, const void* latent_host, const int64_t* latent_shape, int ndim,
                                  void* out_host, int n_bands, void* stream);

@@ -164,21 +164,7 @@ struct vaedec {
     allocs.push_back(*p);
     return VAEDEC_OK;
   }
-  // vaedec_decode_host: the decode of its staging buffers captured once per (latent shape, band
-  // count) into a CUDA graph and replayed (the launches of one decode cost the host more than the
-  // early, small layers take on the GPU when every call starts from an idle stream)
-  struct HostGraph {
-    int64_t shape[5];
-    int ndim, n_bands;
-    unsigned long long launches;   // kernels in the graph (added to `launches` per replay)
-    cudaGraphExec_t exec;
-  };
-  std::vector<HostGraph> host_graphs;
-  cudaStream_t capture_stream = nullptr;
-
   ~vaedec() {
-    for (HostGraph& g : host_graphs) cudaGraphExecDestroy(g.exec);
-    if (capture_stream != nullptr) cudaStreamDestroy(capture_stream);
     for (cudaEvent_t e : prof_ev) cudaEventDestroy(e);
     for (void* p : allocs) cudaFree(p);
   }
@@ -1575,54 +1561,6 @@ vaedec_status vaedec_sync(vaedec_t* h, void* stream) {
   return VAEDEC_OK;
 }
 
-namespace {
-
-// The cached graph of the host-path decode for this shape and band count, captured on first use (the
-// pointer stays valid until the next capture: the cache only grows);
-// null (decode eagerly) while per-op profiling or fault injection is on, when the cache is full, or
-// if the capture did not succeed (the eager decode then reports whatever went wrong).
-const vaedec::HostGraph* host_graph(vaedec* h, const int64_t* shape, int ndim, int n_bands) {
-  if (h->profile || g_fault_kind.load() != 0) return nullptr;
-  for (const vaedec::HostGraph& g : h->host_graphs)
-    if (g.ndim == ndim && g.n_bands == n_bands && std::equal(shape, shape + ndim, g.shape)) return &g;
-  if (h->host_graphs.size() >= 16) return nullptr;
-  if (h->capture_stream == nullptr &&
-      cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
-    h->capture_stream = nullptr;
-    cudaGetLastError();
-    return nullptr;
-  }
-  if (cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  const unsigned long long before = h->launches;
-  Walker w(h, h->capture_stream, false, n_bands);
-  const vaedec_status s = w.run(h->io_latent, shape, ndim, h->io_out);
-  const unsigned long long n_launch = h->launches - before;
-  h->launches = before;   // counted when the graph is launched
-  cudaGraph_t graph = nullptr;
-  cudaError_t e = cudaStreamEndCapture(h->capture_stream, &graph);
-  cudaGraphExec_t exec = nullptr;
-  if (s == VAEDEC_OK && e == cudaSuccess && graph != nullptr) e = cudaGraphInstantiate(&exec, graph, 0);
-  if (graph != nullptr) cudaGraphDestroy(graph);
-  if (s != VAEDEC_OK || e != cudaSuccess || exec == nullptr) {
-    if (exec != nullptr) cudaGraphExecDestroy(exec);
-    cudaGetLastError();
-    return nullptr;
-  }
-  vaedec::HostGraph g{};
-  std::copy(shape, shape + ndim, g.shape);
-  g.ndim = ndim;
-  g.n_bands = n_bands;
-  g.launches = n_launch;
-  g.exec = exec;
-  h->host_graphs.push_back(g);
-  return &h->host_graphs.back();
-}
-
-}  // namespace
-
 vaedec_status vaedec_decode_host(vaedec_t* h, const void* latent_host, const int64_t* shape, int ndim, void* out_host,
                                  int n_bands, void* stream) {
   if (h == nullptr || latent_host == nullptr || out_host == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
@@ -1639,15 +1577,8 @@ vaedec_status vaedec_decode_host(vaedec_t* h, const void* latent_host, const int
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(h->io_latent, latent_host, in_b, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "latent upload");
-  const vaedec::HostGraph* hg = host_graph(h, shape, ndim, n_bands);
-  if (hg != nullptr) {
-    e = cudaGraphLaunch(hg->exec, st);
-    if (e != cudaSuccess) return cuda_fail(e, "decode graph launch");
-    h->launches += hg->launches;
-  } else {
-    s = vaedec_decode(h, h->io_latent, shape, ndim, h->io_out, n_bands, stream);
-    if (s != VAEDEC_OK) return s;
-  }
+  s = vaedec_decode(h, h->io_latent, shape, ndim, h->io_out, n_bands, stream);
+  if (s != VAEDEC_OK) return s;
   e = cudaMemcpyAsync(out_host, h->io_out, out_b, cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e, "output download");
   return vaedec_sync(h, stream);

@@ -1,9 +1,7 @@
 """vaedec_decode_host: host buffers in and out (copies inside the call, synchronous).
 
-The call decodes its staging buffers through a CUDA graph captured on the first call for a latent
-shape and band count and replayed afterwards; with per-op profiling on it decodes eagerly.  Every
-way gives the bits of the device-buffer decode, also on repeated calls and after a change of shape
-or band count.
+It gives the bits of the device-buffer decode and enqueues the same kernels, also on repeated calls,
+after a change of shape or band count, and with per-op profiling on.
 """
 import pytest
 
@@ -24,7 +22,7 @@ def _check(torch, dec, shape, n_bands, seed):
     n0 = dec.launch_count()
     dec.decode_host(zh, oh, n_bands)
     assert torch.equal(oh, ref), (shape, n_bands)
-    # the launch counter sees the same kernels whether the call decoded eagerly or replayed a graph
+    # the same kernels as the device-buffer decode
     assert dec.launch_count() - n0 == n_dev
 
 
@@ -36,10 +34,10 @@ def test_host_decode_matches_device_decode(arch_name, shapes, max_latent):
     torch, rbl = require_gpu()
     arch = synth.KL_ZIMAGE if arch_name == "kl" else synth.WAN
     dec = rbl.Decoder(arch, synth.make_weights(arch, "bf16"), "bf16", max_latent)
-    for rnd in range(2):                  # the second round replays the graphs the first captured
+    for rnd in range(2):
         for i, (shape, nb) in enumerate(shapes):
             _check(torch, dec, shape, nb, seed=10 * rnd + i)
-    dec.profile(True)                     # per-op profiling: the eager path
+    dec.profile(True)
     _check(torch, dec, *shapes[0], seed=3)
     dec.profile(False)
     dec.sync()
