@@ -122,6 +122,22 @@ vaedec_status vaedec_output_shape(const vaedec_t* h, const int64_t* latent_shape
 /* Bytes of device workspace the handle owns (weights excluded). */
 vaedec_status vaedec_workspace_bytes(const vaedec_t* h, size_t* bytes);
 
+/* The workspace a handle created with `config` would own, computed on the host (no CUDA call, no
+ * weights).  The band scheduler keeps every activation and the attention's scratch in one arena:
+ * a dry walk of the decode at config->max_latent lists each tensor with the span of the walk in
+ * which it is alive (from its producer to its last reader), and each is placed at the lowest
+ * 256-byte-aligned offset whose bytes no tensor alive at the same time holds, largest first.
+ * Bounded memory is the pages' concern for a single-GPU decode ("Static Layer-Wise VAE Decode",
+ * Pretrained GPU Measurements: extra peak allocation); here the bound is the live set of the
+ * largest layer, not a whole-image buffer per role.  The walk creates tensors in the same order
+ * for every latent shape up to max_latent, so the layout holds for all of them.
+ *   bytes            total workspace (= vaedec_workspace_bytes of the created handle)
+ *   arena_bytes      the arena within it (may be NULL)
+ *   peak_live_bytes  the largest sum of arena tensors alive at once, a lower bound on the arena (may be NULL)
+ * INVALID_ARG / UNSUPPORTED as vaedec_create for a bad config. */
+vaedec_status vaedec_plan_workspace(const vaedec_config* config, size_t* bytes, size_t* arena_bytes,
+                                    size_t* peak_live_bytes);
+
 /*
  * Decode on `stream` (a cudaStream_t; NULL = legacy default stream).
  * latent: DEVICE pointer, channels-first (NCHW or NCTHW), contiguous, model dtype.
@@ -207,8 +223,10 @@ vaedec_status vaedec_profile_read(vaedec_t* h, float* ms, int max_ops, int* n_op
  * Limits of the fixed scratch: B * rows * G <= 131072 and B * C <= 32768; larger sizes
  * return VAEDEC_ERR_INVALID_ARG with a message naming the limit, before any launch.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- * once per device, with that device current); make that first call before any stream
- * capture.  Every call shares the array and leaves its last contents there; nothing in
+ * with that device current) and caches it under the current context's unique id; a call
+ * in a context not seen before (after cudaDeviceReset, or in a caller's own driver-API
+ * context) looks it up again.  Make the first call on each device, and in each new
+ * context, before any stream capture.  Every call shares the array and leaves its last contents there; nothing in
  * it has to start at zero (each call writes every word it reads), but calls whose
  * kernels overlap on the GPU (e.g. on two streams) race on it and must be ordered by
  * the caller.  Every GPU that loads this library holds the array until process exit.

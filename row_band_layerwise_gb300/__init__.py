@@ -18,6 +18,7 @@ from .build import lib_path
 
 __all__ = ["Decoder", "VaedecError", "load_library", "EXPORTED_SYMBOLS", "STATUS_NAMES", "inject_fault",
            "band_axis", "BAND_AXES", "band_attention", "band_attention_work_bytes", "groupnorm_noalloc",
+           "plan_workspace",
            "set_wait_limit"]
 
 FAMILY = {"kl2d": 1, "wan3d": 2}
@@ -32,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "vaedec_debug_num_ops", "vaedec_debug_op_desc", "vaedec_debug_run_until",
     "vaedec_groupnorm_noalloc", "vaedec_debug_inject_fault", "vaedec_debug_set_wait_limit",
     "vaedec_debug_wait_probe", "vaedec_band_axis", "vaedec_decode_bands",
-    "vaedec_band_attention_work_bytes", "vaedec_band_attention",
+    "vaedec_band_attention_work_bytes", "vaedec_band_attention", "vaedec_plan_workspace",
 )
 
 
@@ -99,6 +100,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.vaedec_decode_bands.argtypes = [vp, vp, i64p, i, vp, i, i, vp]
     lib.vaedec_band_attention_work_bytes.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.vaedec_band_attention.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp, ctypes.c_size_t, vp, vp]
+    szp = ctypes.POINTER(ctypes.c_size_t)
+    lib.vaedec_plan_workspace.argtypes = [ctypes.POINTER(_Config), szp, szp, szp]
     for name in EXPORTED_SYMBOLS:
         if name not in ("vaedec_destroy", "vaedec_last_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -187,11 +190,37 @@ def groupnorm_noalloc(x, y, groups: int, gamma, beta, eps: float, silu: bool, st
     lib = load_library()
     torch = _torch()
     dt = {torch.float32: DTYPE["fp32"], torch.bfloat16: DTYPE["bf16"]}
+    if x.dim() != 4:
+        raise ValueError("x must be a channels-last [B, rows, W, C] tensor")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    for name, t in (("x", x), ("y", y), ("gamma", gamma), ("beta", beta)):
+        if not t.is_cuda or t.device != dev:
+            raise ValueError(f"{name} must be a CUDA tensor on the current device {dev}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if tuple(y.shape) != tuple(x.shape):
+        raise ValueError("y must have the shape of x")
+    if x.dtype not in dt or y.dtype not in dt:
+        raise ValueError("x and y must be float32 or bfloat16")
     B, rows, W, C = (int(v) for v in x.shape)
+    for name, t in (("gamma", gamma), ("beta", beta)):
+        if t.dtype != torch.float32 or t.numel() != C:
+            raise ValueError(f"{name} must be float32 with C = {C} values")
     st = torch.cuda.current_stream() if stream is None else stream
     _check(lib, lib.vaedec_groupnorm_noalloc(dt[x.dtype], dt[y.dtype], x.data_ptr(), y.data_ptr(), B, rows, W, C,
                                              int(groups), gamma.data_ptr(), beta.data_ptr(), float(eps),
                                              1 if silu else 0, int(st.cuda_stream)))
+
+
+def plan_workspace(arch, dtype: str, max_latent: Sequence[int]) -> dict:
+    """Workspace a decoder for ``arch`` / ``dtype`` / ``max_latent`` (B, T, H, W) would own, planned
+    on the host without a GPU: {"bytes": total, "arena": activation arena, "peak_live": the largest
+    sum of activations alive at once}."""
+    lib = load_library()
+    cfg = make_config(arch, dtype, max_latent)
+    b, a, p = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib, lib.vaedec_plan_workspace(ctypes.byref(cfg), ctypes.byref(b), ctypes.byref(a), ctypes.byref(p)))
+    return {"bytes": int(b.value), "arena": int(a.value), "peak_live": int(p.value)}
 
 
 def band_attention_work_bytes(F: int, grid_h: int, grid_w: int, C: int) -> int:

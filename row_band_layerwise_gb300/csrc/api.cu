@@ -45,6 +45,8 @@ vaedec_status cuda_fail(cudaError_t e, const std::string& where) {
 }
 
 constexpr int kNumAct = 5;
+constexpr size_t kSlotAlign = 256;          // every workspace slot starts on a 256-byte boundary
+constexpr size_t kArenaGuard = 1 << 20;     // spare bytes after the last slot
 
 // Process-wide failure injection (vaedec_debug_inject_fault).
 std::atomic<int> g_fault_kind{0};
@@ -76,7 +78,8 @@ struct DevNorm {
 };
 
 struct Act {
-  int buf = -1;          // activation buffer index, or -1 for an external pointer
+  int buf = -1;          // activation role index (>= 0: lives in the workspace arena), or -1 for an external pointer
+  int slot = -1;         // workspace slot of an arena tensor (its offset comes from the liveness plan)
   void* ext = nullptr;
   int dt = kBF16;        // element type (kF32 / kBF16)
   int B = 0, T = 1, H = 0, W = 0, C = 0;
@@ -111,24 +114,14 @@ struct vaedec {
   std::map<std::string, DevConv> conv;
   std::map<std::string, DevNorm> norm;
   std::vector<void*> allocs;
-  // workspace
-  void* act[kNumAct] = {};
-  size_t act_bytes = 0;
-  void* attn_q = nullptr;
-  void* attn_k = nullptr;
-  void* attn_vt = nullptr;
-  size_t qkv_bytes = 0;
-  // fp32 path: one band's scores, probabilities and row sums
-  float* attn_s = nullptr;
-  void* attn_p = nullptr;
-  float* attn_l = nullptr;
-  size_t s_elems = 0, l_elems = 0;
-  // bf16 path: fp32 partial outputs and row maxima / sums of the fused attention's key splits
-  void* attn_work = nullptr;
-  size_t attn_work_bytes = 0;
-  // width bands: a band's queries gathered dense, and its output before the scatter back
-  void* attn_qg = nullptr;
-  void* attn_ob = nullptr;
+  // workspace: one arena holding every activation and the attention's scratch (Q, K, V^T, key-split
+  // partials, width-band gathers; the fp32 path's scores) as slots whose offsets come from a liveness
+  // plan made at create time for max_latent (two slots share bytes only if their lifetimes are disjoint)
+  void* arena = nullptr;
+  size_t arena_bytes = 0;
+  std::vector<size_t> slot_off;     // per slot, in the order a decode walk creates them
+  std::vector<size_t> slot_bytes;   // planned (max_latent) size of each slot
+  size_t act_peak_bytes = 0;        // largest sum of simultaneously live slots in the plan
   // AutoencoderKLFlux2 latent front-end: patch size (1 = none) and the inverse latent BatchNorm
   // per patched channel, scale = sqrt(var + eps) and shift = mean
   int patch = 1;
@@ -173,9 +166,58 @@ struct vaedec {
 namespace {
 
 // Sizes a dry walk records for workspace planning.
-struct Plan {
-  size_t act = 0, qkv = 0, s = 0, l = 0, part = 0, sc = 0, attn_work = 0;
+struct SlotUse {
+  size_t bytes;
+  long long first, last;   // walk ticks of the slot's creation and of its last use
 };
+struct Plan {
+  size_t part = 0, sc = 0;
+  std::vector<SlotUse> slots;
+};
+
+// Offsets of the slots in one arena: largest first, each at the lowest 256-byte-aligned offset
+// that overlaps no placed slot whose lifetime overlaps its own.  Returns the arena size and the
+// largest sum of live slot bytes at any tick (a lower bound on any placement).
+size_t place_slots(const std::vector<SlotUse>& slots, std::vector<size_t>* off, size_t* peak_live) {
+  const size_t n = slots.size();
+  std::vector<size_t> order(n), sz(n);
+  for (size_t i = 0; i < n; ++i) {
+    order[i] = i;
+    sz[i] = (slots[i].bytes + kSlotAlign - 1) / kSlotAlign * kSlotAlign;
+  }
+  std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) {
+    if (sz[a] != sz[b]) return sz[a] > sz[b];
+    return slots[a].first < slots[b].first;
+  });
+  off->assign(n, 0);
+  std::vector<size_t> placed;
+  size_t top = 0;
+  for (size_t i : order) {
+    std::vector<std::pair<size_t, size_t>> busy;   // [begin, end) of placed slots alive at the same time
+    for (size_t j : placed)
+      if (!(slots[j].last < slots[i].first || slots[i].last < slots[j].first))
+        busy.emplace_back((*off)[j], (*off)[j] + sz[j]);
+    std::sort(busy.begin(), busy.end());
+    size_t o = 0;
+    for (const auto& b : busy) {
+      if (o + sz[i] <= b.first) break;
+      o = std::max(o, b.second);
+    }
+    (*off)[i] = o;
+    top = std::max(top, o + sz[i]);
+    placed.push_back(i);
+  }
+  // peak of the live bytes over the ticks where some slot begins
+  size_t peak = 0;
+  for (size_t i = 0; i < n; ++i) {
+    size_t live = 0;
+    for (size_t j = 0; j < n; ++j)
+      if (slots[j].first <= slots[i].first && slots[i].first <= slots[j].last) live += sz[j];
+    peak = std::max(peak, live);
+  }
+  *peak_live = peak;
+  return top;
+}
 
 class Walker {
  public:
@@ -231,11 +273,40 @@ class Walker {
   int sdt_;   // storage dtype of the residual stream and every pre-norm tensor (fp32)
   int nest_ = 0;
   long long stats_epoch_ = 0;   // bumped whenever a conv rewrites the moments buffer
+  int n_slots_ = 0;             // workspace slots created so far by this walk
+  long long tick_ = 0;          // walk clock for slot lifetimes (creations and uses)
 
   bool mixed() const { return odt_ != sdt_; }
 
   // ---------------------------------------------------------------- helpers
-  void* ptr(const Act& a) const { return a.buf >= 0 ? h_->act[a.buf] : a.ext; }
+  void* slot_ptr(int slot) const {
+    if (dry_ || slot < 0 || slot >= (int)h_->slot_off.size()) return nullptr;
+    return static_cast<char*>(h_->arena) + h_->slot_off[slot];
+  }
+  void* ptr(const Act& a) const { return a.buf >= 0 ? slot_ptr(a.slot) : a.ext; }
+
+  // A new workspace slot of `b` bytes.  The walk creates slots in the same order for every latent
+  // shape up to max_latent (no slot depends on the geometry), so the create-time plan gives each
+  // one an offset whose bytes no other slot alive at the same time uses.
+  int new_slot(size_t b) {
+    if (!live()) return -1;   // a stopped walk (debug stop, error) creates nothing more
+    const int id = n_slots_++;
+    const long long t = ++tick_;
+    if (plan) {
+      plan->slots.push_back(SlotUse{b, t, t});
+    } else if (id >= (int)h_->slot_bytes.size() || b > h_->slot_bytes[id]) {
+      set_err(VAEDEC_ERR_INVALID_ARG, "internal: the workspace plan does not cover this decode");
+    }
+    return id;
+  }
+  // Marks a slot (or an arena tensor) as read or written now: its bytes stay reserved until then.
+  void use_slot(int slot) {
+    const long long t = ++tick_;
+    if (plan && slot >= 0 && slot < (int)plan->slots.size()) plan->slots[slot].last = t;
+  }
+  void use(const Act& a) {
+    if (a.buf >= 0) use_slot(a.slot);
+  }
   static size_t esz(int dt) { return dt == kBF16 ? 2 : 4; }
   size_t bytes(const Act& a) const { return (size_t)a.pixels() * a.C * esz(a.dt); }
   static const char* dts(int dt) { return dt == kBF16 ? "bf16" : "f32"; }
@@ -246,8 +317,9 @@ class Walker {
     return -1;
   }
 
-  void note_act(const Act& a) {
-    if (plan && a.buf >= 0) plan->act = std::max(plan->act, bytes(a));
+  // Gives a freshly produced arena tensor its slot (sized for it, alive from now).
+  void note_act(Act& a) {
+    if (a.buf >= 0) a.slot = new_slot(bytes(a));
   }
 
   void set_err(vaedec_status s, const std::string& m) {
@@ -536,6 +608,13 @@ class Walker {
       note_act(yc);
       *copy = yc;
     }
+    // inputs are read after the outputs exist, and the outputs stay reserved to the end of the op:
+    // no two tensors of one op share bytes
+    use(x);
+    if (res) use(*res);
+    if (sc_x) use(*sc_x);
+    use(y);
+    if (copy) use(yc);
     ConvGeom g;
     std::memset(&g, 0, sizeof(g));
     {
@@ -655,6 +734,9 @@ class Walker {
       note_act(yr);
       *raw = yr;
     }
+    use(x);
+    use(y);
+    if (raw) use(yr);
     if (begin("kind=groupnorm name=" + prefix + io(x, nullptr, y) + " silu=" + (silu ? "1" : "0") +
               " groups=" + std::to_string(G) + " fused_stats=" + (have ? "1" : "0"))) {
       count(have ? 2 : 3);
@@ -691,6 +773,9 @@ class Walker {
       note_act(yr);
       *raw = yr;
     }
+    use(x);
+    use(y);
+    if (raw) use(yr);
     if (begin("kind=rmsnorm name=" + prefix + io(x, nullptr, y) + " silu=" + (silu ? "1" : "0"))) {
       count();
       check(launch_rms_norm(x.dt, y.dt, ptr(x), ptr(y), raw ? ptr(yr) : nullptr, x.pixels(), x.C, n->g,
@@ -714,19 +799,33 @@ class Walker {
     const long long Ntok = (long long)x.H * x.W;
     const int F = x.B * x.T;   // sequences
     const size_t oes = esz(odt_);
-    if (plan) {
-      plan->qkv = std::max(plan->qkv, (size_t)F * (size_t)Ntok * (size_t)C * oes);
-      if (h_->dtype == kBF16) {
-        plan->attn_work = std::max(plan->attn_work, flash_work_bytes(F, Ntok, C));
-      } else {
-        // fp32 path: one band's scores, probabilities and row sums (the plan walks one band)
-        int maxrows = 0;
-        for (int r : band_rows(x.H, n_bands_)) maxrows = std::max(maxrows, r);
-        plan->s = std::max(plan->s, (size_t)maxrows * (size_t)x.W * (size_t)Ntok);
-        plan->l = std::max(plan->l, (size_t)maxrows * x.W);
-      }
-    }
     note_act(y);
+    // the op's scratch, alive for this op only: Q, K, V^T, the width bands' gathered queries and
+    // their output before the scatter, and the bf16 path's key-split partials or the fp32 path's
+    // scores, probabilities and row sums of its largest band (the plan walks one band)
+    const size_t qkv_b = (size_t)F * (size_t)Ntok * (size_t)C * oes;
+    const int s_q = new_slot(qkv_b), s_k = new_slot(qkv_b), s_vt = new_slot(qkv_b);
+    const int s_qg = new_slot(qkv_b), s_ob = new_slot(qkv_b);
+    int s_work = -1, s_s = -1, s_p = -1, s_l = -1;
+    if (h_->dtype == kBF16) {
+      s_work = new_slot(flash_work_bytes(F, Ntok, C));
+    } else {
+      int maxp = 0;
+      for (int r : band_rows(axis_ == 1 ? x.W : x.H, n_bands_)) maxp = std::max(maxp, r);
+      const size_t nrmax = (size_t)maxp * (size_t)(axis_ == 1 ? x.H : x.W);
+      s_s = new_slot(nrmax * (size_t)Ntok * sizeof(float));
+      s_p = new_slot(nrmax * (size_t)Ntok * oes);
+      s_l = new_slot(nrmax * sizeof(float));
+    }
+    void* const attn_q = slot_ptr(s_q);
+    void* const attn_k = slot_ptr(s_k);
+    void* const attn_vt = slot_ptr(s_vt);
+    void* const attn_qg = slot_ptr(s_qg);
+    void* const attn_ob = slot_ptr(s_ob);
+    void* const attn_work = slot_ptr(s_work);
+    float* const attn_s = static_cast<float*>(slot_ptr(s_s));
+    void* const attn_p = slot_ptr(s_p);
+    float* const attn_l = static_cast<float*>(slot_ptr(s_l));
     // projections 4 x (2 N C^2) plus scores and probabilities x values 2 x (2 N^2 C), per sequence
     const double attn_flops = (double)F * (8.0 * (double)Ntok * C * C + 4.0 * (double)Ntok * (double)Ntok * C);
     std::ostringstream fl;
@@ -784,11 +883,11 @@ class Walker {
         g.osy = g.osx = 1;
         g.out_f32 = odt_ == kF32;
         g.scale = 1.f;
-        launch(g, ptr(hn), wq, wq.w, wq.b, nullptr, nullptr, h_->attn_q, nullptr, "attention q");
-        launch(g, ptr(hn), wk, wk.w, wk.b, nullptr, nullptr, h_->attn_k, nullptr, "attention k");
+        launch(g, ptr(hn), wq, wq.w, wq.b, nullptr, nullptr, attn_q, nullptr, "attention q");
+        launch(g, ptr(hn), wk, wk.w, wk.b, nullptr, nullptr, attn_k, nullptr, "attention k");
         ConvGeom gv = g;
         gv.out_chfirst = 1;
-        launch(gv, ptr(hn), wv, wv.w, wv.b, nullptr, nullptr, h_->attn_vt, nullptr, "attention v");
+        launch(gv, ptr(hn), wv, wv.w, wv.b, nullptr, nullptr, attn_vt, nullptr, "attention v");
         // band-local queries against every key/value of the frame; width bands are gathered into a
         // dense query buffer and their output scattered back (each query's arithmetic is the same
         // whichever band holds it)
@@ -797,7 +896,7 @@ class Walker {
         if (h_->dtype == kBF16) {
           // fused tensor-core attention: one launch covers every band of every frame (query tiles
           // never cross a band), then the merge of its key splits
-          void* q_src = h_->attn_q;
+          void* q_src = attn_q;
           void* o_dst = ptr(hn);
           if (wband) {
             // frame f's width band b goes to rows f * Ntok + H * c0 of the gathered buffer
@@ -806,23 +905,23 @@ class Walker {
               for (int band = 0; band < n_bands_ && live(); ++band) {
                 count();
                 if (live())
-                  check(launch_band_cols(odt_, static_cast<char*>(h_->attn_q) + (size_t)f * Ntok * C * oes,
-                                         static_cast<char*>(h_->attn_qg) + ((size_t)f * Ntok + (size_t)x.H * c0) * C * oes,
+                  check(launch_band_cols(odt_, static_cast<char*>(attn_q) + (size_t)f * Ntok * C * oes,
+                                         static_cast<char*>(attn_qg) + ((size_t)f * Ntok + (size_t)x.H * c0) * C * oes,
                                          x.H, x.W, C, c0, rows[band], 1, st_),
                         "attention band gather");
                 c0 += rows[band];
               }
             }
-            q_src = h_->attn_qg;
-            o_dst = h_->attn_ob;
+            q_src = attn_qg;
+            o_dst = attn_ob;
           }
           FlashArgs fa;
           fa.q = q_src;
-          fa.k = h_->attn_k;
-          fa.vt = h_->attn_vt;
+          fa.k = attn_k;
+          fa.vt = attn_vt;
           fa.out = o_dst;
-          fa.part = static_cast<float*>(h_->attn_work);
-          fa.ml = static_cast<char*>(h_->attn_work) +
+          fa.part = static_cast<float*>(attn_work);
+          fa.ml = static_cast<char*>(attn_work) +
                   (size_t)flash_splits(Ntok) * (size_t)F * (size_t)Ntok * (size_t)C * sizeof(float);
           fa.F = F;
           fa.ntok = Ntok;
@@ -831,8 +930,6 @@ class Walker {
           fa.n_seg = n_bands_;
           fa.seg_q = (wband ? x.W : x.H) / n_bands_;
           fa.seg_rem = (wband ? x.W : x.H) % n_bands_;
-          if (flash_splits(Ntok) > 1 && h_->attn_work_bytes < flash_work_bytes(F, Ntok, C))
-            set_err(VAEDEC_ERR_INVALID_ARG, "attention workspace too small for this shape");
           if (live()) {
             count();
             const char* why = nullptr;
@@ -850,7 +947,7 @@ class Walker {
               for (int band = 0; band < n_bands_ && live(); ++band) {
                 count();
                 if (live())
-                  check(launch_band_cols(odt_, static_cast<char*>(h_->attn_ob) + ((size_t)f * Ntok + (size_t)x.H * c0) * C * oes,
+                  check(launch_band_cols(odt_, static_cast<char*>(attn_ob) + ((size_t)f * Ntok + (size_t)x.H * c0) * C * oes,
                                          static_cast<char*>(ptr(hn)) + (size_t)f * Ntok * C * oes, x.H, x.W, C, c0,
                                          rows[band], 0, st_),
                         "attention band scatter");
@@ -878,11 +975,11 @@ class Walker {
               // height band: its queries and its output are contiguous rows of the frame (O overwrites
               // the band's normalised rows); width band: gathered / scattered through dense buffers
               const size_t qoff = wband ? 0 : ((size_t)f * Ntok + (size_t)r0 * x.W) * C;
-              void* q_band = static_cast<char*>(wband ? h_->attn_qg : h_->attn_q) + qoff * oes;
-              void* o_band = wband ? h_->attn_ob : static_cast<void*>(static_cast<char*>(ptr(hn)) + qoff * oes);
+              void* q_band = static_cast<char*>(wband ? attn_qg : attn_q) + qoff * oes;
+              void* o_band = wband ? attn_ob : static_cast<void*>(static_cast<char*>(ptr(hn)) + qoff * oes);
               if (wband) {
                 count();
-                check(launch_band_cols(odt_, static_cast<char*>(h_->attn_q) + (size_t)f * Ntok * C * oes, h_->attn_qg,
+                check(launch_band_cols(odt_, static_cast<char*>(attn_q) + (size_t)f * Ntok * C * oes, attn_qg,
                                        x.H, x.W, C, r0, rows[band], 1, st_),
                       "attention band gather");
               }
@@ -904,18 +1001,18 @@ class Walker {
               gs.out_f32 = 1;
               gs.scale = scale;
               launch(gs, q_band, kview,
-                     static_cast<char*>(h_->attn_k) + (size_t)f * Ntok * C * oes, nullptr, nullptr, nullptr,
-                     h_->attn_s, nullptr, "attention scores");
+                     static_cast<char*>(attn_k) + (size_t)f * Ntok * C * oes, nullptr, nullptr, nullptr,
+                     attn_s, nullptr, "attention scores");
               count();
-              check(launch_softmax_rows(odt_, h_->attn_s, h_->attn_p, h_->attn_l, nr, (int)Ntok, st_), "softmax");
+              check(launch_softmax_rows(odt_, attn_s, attn_p, attn_l, nr, (int)Ntok, st_), "softmax");
               ConvGeom go = gs;
               go.Cin = (int)Ntok;
               go.Cout = C;
               go.oC = C;
               go.out_f32 = odt_ == kF32;
               go.scale = 1.f;
-              launch(go, h_->attn_p, vview, static_cast<char*>(h_->attn_vt) + (size_t)f * C * Ntok * oes, nullptr,
-                     nullptr, h_->attn_l, o_band, nullptr, "attention pv");
+              launch(go, attn_p, vview, static_cast<char*>(attn_vt) + (size_t)f * C * Ntok * oes, nullptr,
+                     nullptr, attn_l, o_band, nullptr, "attention pv");
               if (wband && live()) {
                 count();
                 check(launch_band_cols(odt_, o_band, static_cast<char*>(ptr(hn)) + (size_t)f * Ntok * C * oes, x.H,
@@ -932,7 +1029,12 @@ class Walker {
         gp.res_f32 = x.dt == kF32;
         launch(gp, ptr(hn), wo, wo.w, wo.b, ptr(x), nullptr, ptr(y), nullptr, "attention out");
       }
+      use(hn);
     }
+    use(x);
+    use(y);
+    for (int sl : {s_q, s_k, s_vt, s_qg, s_ob, s_work, s_s, s_p, s_l})
+      if (sl >= 0) use_slot(sl);
     --nest_;
     end(&x, nullptr, y);
     return y;
@@ -978,7 +1080,16 @@ class Walker {
     Act hh = conv(t, p + ".conv1", wan ? C3 : K3, nullptr, hb, sdt_, nullptr, nullptr, -1, !wan);
     Act t2 = wan ? rms_norm(hh, p + ".norm2", true, tb) : group_norm(hh, p + ".norm2", true, tb);
     if (sc && need_raw && fuse_shortcut(t2, p)) {
-      // the 1x1 shortcut runs inside conv2 (extra K over the raw operand copy of x)
+      // the 1x1 shortcut runs inside conv2 (extra K over the raw operand copy of x).  Whether it can
+      // depends on the geometry, so the workspace slot the separate shortcut output would take is
+      // still created (and left unused): the walk's slot sequence stays the same for every shape.
+      {
+        Act unused = t2;
+        unused.buf = 0;
+        unused.dt = sdt_;
+        unused.C = h_->conv.at(p + ".conv_shortcut").cout;
+        note_act(unused);
+      }
       if (copy && mixed())
         return conv(t2, p + ".conv2", K3, nullptr, hb, sdt_, nullptr, copy, pick({tb, hb, rb}), true, &xb,
                     p + ".conv_shortcut");
@@ -1249,6 +1360,49 @@ vaedec_status check_latent(const vaedec* h, const int64_t* shape, int ndim, int 
 
 }  // namespace
 
+namespace {
+
+// Dry walk at max_latent with one band (the fp32 path's largest score buffer): the workspace slots
+// with their lifetimes, the GroupNorm scratch sizes and the host-path staging sizes.
+vaedec_status plan_walk(vaedec* h, Plan* plan) {
+  const vaedec_config* config = &h->cfg;
+  int64_t shape[5];
+  int ndim;
+  const int64_t* m = config->max_latent;
+  if (config->family == VAEDEC_FAMILY_KL2D) {
+    ndim = 4;
+    shape[0] = m[0]; shape[1] = (int64_t)config->latent_channels * h->patch * h->patch; shape[2] = m[2]; shape[3] = m[3];
+  } else {
+    ndim = 5;
+    shape[0] = m[0]; shape[1] = config->latent_channels; shape[2] = m[1]; shape[3] = m[2]; shape[4] = m[3];
+  }
+  Walker w(h, nullptr, true, 1);
+  w.plan = plan;
+  vaedec_status s = w.run(nullptr, shape, ndim, kDryOut);
+  if (s != VAEDEC_OK) return s;
+  int64_t oshape[5];
+  if (vaedec_output_shape(h, shape, ndim, oshape) != VAEDEC_OK) return VAEDEC_ERR_INVALID_ARG;
+  h->io_latent_bytes = h->es;
+  h->io_out_bytes = h->es;
+  for (int i = 0; i < ndim; ++i) {
+    h->io_latent_bytes *= (size_t)shape[i];
+    h->io_out_bytes *= (size_t)oshape[i];
+  }
+  return VAEDEC_OK;
+}
+
+// Places the plan's slots in one arena; returns the whole workspace in bytes (arena, GroupNorm
+// chunk moments and scale/shift, host-path staging, status word).
+size_t layout_workspace(vaedec* h, const Plan& plan) {
+  h->arena_bytes = place_slots(plan.slots, &h->slot_off, &h->act_peak_bytes) + kArenaGuard;
+  h->slot_bytes.resize(plan.slots.size());
+  for (size_t i = 0; i < plan.slots.size(); ++i) h->slot_bytes[i] = plan.slots[i].bytes;
+  return h->arena_bytes + std::max<size_t>(plan.part, 1) * sizeof(GnPartial) +
+         2 * std::max<size_t>(plan.sc, 1) * sizeof(float) + h->io_latent_bytes + h->io_out_bytes + sizeof(int);
+}
+
+}  // namespace
+
 void vd::record_last_error(const std::string& message) { g_err = message; }
 
 // ====================================================================== C ABI
@@ -1419,50 +1573,12 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
     if (e != cudaSuccess) return bail(cuda_fail(e, "latent batchnorm upload"));
   }
 
-  // workspace plan: a dry walk at max_latent with one band (the largest score buffer)
   Plan plan;
-  {
-    int64_t shape[5];
-    int ndim;
-    const int64_t* m = config->max_latent;
-    if (config->family == VAEDEC_FAMILY_KL2D) {
-      ndim = 4;
-      shape[0] = m[0]; shape[1] = (int64_t)config->latent_channels * h->patch * h->patch; shape[2] = m[2]; shape[3] = m[3];
-    } else {
-      ndim = 5;
-      shape[0] = m[0]; shape[1] = config->latent_channels; shape[2] = m[1]; shape[3] = m[2]; shape[4] = m[3];
-    }
-    Walker w(h, nullptr, true, 1);
-    w.plan = &plan;
-    s = w.run(nullptr, shape, ndim, kDryOut);
-    if (s != VAEDEC_OK) return bail(s);
-    int64_t oshape[5];
-    if (vaedec_output_shape(h, shape, ndim, oshape) != VAEDEC_OK) return bail(VAEDEC_ERR_INVALID_ARG);
-    h->io_latent_bytes = 1;
-    for (int i = 0; i < ndim; ++i) h->io_latent_bytes *= (size_t)shape[i];
-    h->io_out_bytes = 1;
-    for (int i = 0; i < ndim; ++i) h->io_out_bytes *= (size_t)oshape[i];
-    h->io_latent_bytes *= h->es;
-    h->io_out_bytes *= h->es;
-  }
-  h->act_bytes = plan.act;
-  for (int i = 0; i < kNumAct && s == VAEDEC_OK; ++i) s = h->dalloc(&h->act[i], plan.act, "activations");
-  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_q, plan.qkv, "attention q");
-  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_k, plan.qkv, "attention k");
-  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_vt, plan.qkv, "attention v");
-  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_qg, plan.qkv, "attention width-band queries");
-  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_ob, plan.qkv, "attention width-band output");
-  h->qkv_bytes = plan.qkv;
+  s = plan_walk(h, &plan);
+  if (s != VAEDEC_OK) return bail(s);
+  h->ws_bytes = layout_workspace(h, plan);
+  s = h->dalloc(&h->arena, h->arena_bytes, "workspace arena");
   void* tmp = nullptr;
-  if (s == VAEDEC_OK) s = h->dalloc(&tmp, plan.s * sizeof(float), "attention scores");
-  h->attn_s = static_cast<float*>(tmp);
-  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_p, plan.s * h->es, "attention probabilities");
-  if (s == VAEDEC_OK) s = h->dalloc(&tmp, plan.l * sizeof(float), "attention row sums");
-  h->attn_l = static_cast<float*>(tmp);
-  h->s_elems = plan.s;
-  h->l_elems = plan.l;
-  if (s == VAEDEC_OK) s = h->dalloc(&h->attn_work, plan.attn_work, "attention key-split partials");
-  h->attn_work_bytes = plan.attn_work;
   if (s == VAEDEC_OK) s = h->dalloc(&tmp, std::max<size_t>(plan.part, 1) * sizeof(GnPartial), "groupnorm partials");
   h->gn_part = static_cast<GnPartial*>(tmp);
   if (s == VAEDEC_OK) s = h->dalloc(&tmp, std::max<size_t>(plan.sc, 1) * sizeof(float), "groupnorm scale");
@@ -1476,8 +1592,6 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
   if (s != VAEDEC_OK) return bail(s);
   cudaError_t e = cudaMemset(h->status, 0, sizeof(int));
   if (e != cudaSuccess) return bail(cuda_fail(e, "status init"));
-  h->ws_bytes = kNumAct * plan.act + 5 * plan.qkv + plan.s * (4 + h->es) + plan.l * 4 + plan.attn_work + plan.part * sizeof(GnPartial) +
-                2 * plan.sc * 4 + h->io_latent_bytes + h->io_out_bytes;
   *out = h;
   return VAEDEC_OK;
 }
@@ -1508,6 +1622,75 @@ vaedec_status vaedec_output_shape(const vaedec_t* h, const int64_t* shape, int n
     out_shape[2] = shape[2] * f;
     out_shape[3] = shape[3] * f;
   }
+  return VAEDEC_OK;
+}
+
+vaedec_status vaedec_plan_workspace(const vaedec_config* config, size_t* bytes, size_t* arena_bytes,
+                                    size_t* peak_live_bytes) {
+  g_err.clear();
+  if (config == nullptr || bytes == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  vaedec_status s = validate_config(config);
+  if (s != VAEDEC_OK) return s;
+  vaedec h;   // layer shapes only: no weights, no device memory
+  h.cfg = *config;
+  h.patch = config->latent_patch == 2 ? 2 : 1;
+  h.dtype = config->dtype == VAEDEC_DTYPE_BF16 ? kBF16 : kF32;
+  h.es = h.dtype == kBF16 ? 2 : 4;
+  std::vector<Need> needs;
+  if (config->family == VAEDEC_FAMILY_KL2D)
+    needs_kl(*config, needs);
+  else
+    needs_wan(*config, needs);
+  for (const Need& nd : needs) {
+    if (nd.kind == 0) {
+      DevConv dc;
+      dc.cin = nd.cin;
+      dc.cout = nd.cout;
+      dc.kt = nd.kt > 0 ? nd.kt : 1;
+      dc.kh = nd.kh;
+      dc.kw = nd.kw;
+      dc.ntaps = dc.kt * nd.kh * nd.kw;
+      dc.rows = h.dtype == kBF16 ? round_up(nd.cout, 16) : nd.cout;
+      h.conv[nd.name] = dc;
+    } else {
+      DevNorm dn;
+      dn.c = nd.cout;
+      h.norm[nd.name] = dn;
+    }
+  }
+  if (h.dtype == kBF16) {
+    // as at create: a block with a 1x1 shortcut gets a combined conv2 bias (never read by a dry walk)
+    static const std::string kShortcut = ".conv_shortcut";
+    for (auto& kv : h.conv) {
+      const std::string& nm = kv.first;
+      if (nm.size() <= kShortcut.size() || nm.compare(nm.size() - kShortcut.size(), kShortcut.size(), kShortcut) != 0)
+        continue;
+      auto c2 = h.conv.find(nm.substr(0, nm.size() - kShortcut.size()) + ".conv2");
+      if (c2 != h.conv.end() && c2->second.cout == kv.second.cout) c2->second.b_sc = reinterpret_cast<float*>(kDryOut);
+    }
+  }
+  Plan plan;
+  s = plan_walk(&h, &plan);
+  if (s != VAEDEC_OK) return s;
+  *bytes = layout_workspace(&h, plan);
+  {
+    // the layout covers a decode walk at max_latent (same slots, same sizes)
+    const int64_t* m = config->max_latent;
+    int64_t shape[5];
+    int ndim;
+    if (config->family == VAEDEC_FAMILY_KL2D) {
+      ndim = 4;
+      shape[0] = m[0]; shape[1] = (int64_t)config->latent_channels * h.patch * h.patch; shape[2] = m[2]; shape[3] = m[3];
+    } else {
+      ndim = 5;
+      shape[0] = m[0]; shape[1] = config->latent_channels; shape[2] = m[1]; shape[3] = m[2]; shape[4] = m[3];
+    }
+    Walker w(&h, nullptr, true, 1);
+    s = w.run(nullptr, shape, ndim, kDryOut);
+    if (s != VAEDEC_OK) return s;
+  }
+  if (arena_bytes) *arena_bytes = h.arena_bytes;
+  if (peak_live_bytes) *peak_live_bytes = h.act_peak_bytes;
   return VAEDEC_OK;
 }
 

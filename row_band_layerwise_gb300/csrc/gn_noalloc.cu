@@ -10,10 +10,14 @@
 //
 // The array below is a device symbol: in host code its name is only a host-side
 // stand-in, so the host asks the runtime for its device address once per device
-// (cudaGetSymbolAddress, with that device current) and passes that address to the
-// kernels.  Every GPU that loads this library holds the array until the process
-// exits.  All calls share it: two calls whose kernels overlap on the GPU (for
-// example on two streams) race on it and must be ordered by the caller.
+// context (cudaGetSymbolAddress, with that device current) and passes that address
+// to the kernels.  The address is cached under the context's unique id, so a new
+// context on the same device (after cudaDeviceReset, or a caller's own driver-API
+// context) gets its own look-up instead of a stale address.  Every GPU that loads
+// this library holds the array until the process exits.  All calls share it: two
+// calls whose kernels overlap on the GPU (for example on two streams) race on it
+// and must be ordered by the caller.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -35,7 +39,39 @@ static __device__ __align__(256) unsigned char g_gn_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-void* g_scratch_dev[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;   // unique id of the context the address belongs to (0: none yet)
+  void* ptr = nullptr;
+};
+ScratchAddr g_scratch_dev[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 when there is none or the driver
+// cannot say).  The driver entry points are resolved once through the runtime.
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_cur == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 vaedec_status noalloc_fail(vaedec_status s, const std::string& m) {
   record_last_error(m);
@@ -69,7 +105,7 @@ extern "C" vaedec_status vaedec_groupnorm_noalloc(int in_dtype, int out_dtype, c
                                                      " exceeds the fixed scratch limit of " +
                                                      std::to_string(kMaxScaleShift));
 
-  // One-time set-up per device: the device address of the scratch array.
+  // Set-up once per device context: the device address of the scratch array.
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return noalloc_fail(VAEDEC_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
@@ -77,14 +113,17 @@ extern "C" vaedec_status vaedec_groupnorm_noalloc(int in_dtype, int out_dtype, c
   void* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (g_scratch_dev[dev] == nullptr) {
+    ScratchAddr& a = g_scratch_dev[dev];
+    const unsigned long long id = current_ctx_id();
+    if (a.ptr == nullptr || id == 0 || id != a.ctx_id) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_gn_scratch);
       if (e != cudaSuccess || p == nullptr)
         return noalloc_fail(VAEDEC_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-      g_scratch_dev[dev] = p;
+      a.ptr = p;
+      a.ctx_id = current_ctx_id();   // the look-up made the device's context current if none was
     }
-    base = g_scratch_dev[dev];
+    base = a.ptr;
   }
   GnPartial* part = static_cast<GnPartial*>(base);
   float* scale = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kMaxPartials * sizeof(GnPartial));

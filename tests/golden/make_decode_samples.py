@@ -1,17 +1,25 @@
-"""Write sampled float64 oracle outputs of full-size decodes to text fixtures.
+"""Write float64 oracle outputs of full-size decodes to test fixtures.
 
     python tests/golden/make_decode_samples.py kl_zimage_512 [kl_zimage_1024 ...]
 
 For each named workload this runs the oracle's dense decode (whole image, no
 bands) on the workload's seeded latent and seeded weights, and writes
-``decode_samples_<workload>.txt``: a header with the output shape and the
-output's L2 norm, then one line per sampled output element, ``flat_index value``.
-The positions are drawn with a fixed seed: uniformly over the whole output, plus
-extra positions on the two output rows on each side of every band boundary of the
-workload's band schedule (where the halo rows of every layer meet).
+``decode_full_<workload>.npz`` (float64 results rounded once to float32):
+
+* image decoders (output [B, 3, H, W]): ``out``, the complete output;
+* video decoders (output [B, 3, T, H, W]): ``frames`` (frame indices: the
+  first, the middle and the last frame) with ``frame_out`` [B, 3, len(frames),
+  H, W], their complete outputs; and ``rows`` (every output row within three
+  rows of a band boundary of the workload's band schedule, where the halo rows
+  of every layer meet) with ``row_out`` [B, 3, T, len(rows), W], those rows in
+  every frame.
+
+Every file also holds ``shape`` (the whole output's shape) and ``l2norm`` (the
+float64 L2 norm of the whole output).  Float32 storage moves a value by at most
+2^-24 of itself, far below the bf16 bars the fixtures are checked against.
 
 Only ``synth`` (seeded inputs) and ``oracle`` are used; nothing here touches the
-CUDA library.  A full-size decode takes minutes of CPU time per workload.
+CUDA library.  A full-size decode takes minutes to an hour of CPU time.
 """
 from __future__ import annotations
 
@@ -29,34 +37,34 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 from oracle import decoder as odec  # noqa: E402
 
-N_UNIFORM = 3000
-N_PER_EDGE_ROW = 64
-SEED = 20261202
+EDGE_ROWS = 3           # rows kept on each side of a band boundary (video decoders)
 
 
-def sample_positions(shape, arch, latent_shape, n_bands):
-    """Flat indices: uniform samples plus samples on rows next to band boundaries."""
-    rng = np.random.default_rng(SEED)
-    total = int(np.prod(shape))
-    idx = set(int(i) for i in rng.integers(0, total, N_UNIFORM))
-    # output rows per latent row
-    f = 2 ** sum(1 for u in arch.stage_upsample if u)
-    rows = odec.band_rows(latent_shape[-2], n_bands)
-    h_out, w_out = shape[-2], shape[-1]
-    edges, r0 = [], 0
-    for r in rows[:-1]:
+def boundary_rows(arch, latent_shape, n_bands, h_out):
+    """Output rows within EDGE_ROWS of a band boundary of the band schedule."""
+    f = h_out // latent_shape[-2]               # output rows per latent row
+    rows, r0 = [], 0
+    for r in odec.band_rows(latent_shape[-2], n_bands)[:-1]:
         r0 += r
-        edges.append(r0 * f)
-    lead = shape[:-2]
-    for e in edges:
-        for y in (e - 2, e - 1, e, e + 1):
-            if not 0 <= y < h_out:
-                continue
-            for _ in range(N_PER_EDGE_ROW):
-                lead_idx = tuple(int(rng.integers(0, n)) for n in lead)
-                x = int(rng.integers(0, w_out))
-                idx.add(int(np.ravel_multi_index(lead_idx + (y, x), shape)))
-    return np.array(sorted(idx), dtype=np.int64)
+        e = r0 * f
+        rows.extend(y for y in range(e - EDGE_ROWS, e + EDGE_ROWS) if 0 <= y < h_out)
+    return np.array(sorted(set(rows)), np.int64)
+
+
+def fixture_arrays(y: np.ndarray, w) -> dict:
+    arrays = dict(shape=np.array(y.shape, np.int64),
+                  l2norm=np.array(float(np.linalg.norm(y.reshape(-1)))))
+    if y.ndim == 4:
+        arrays["out"] = y.astype(np.float32)
+        return arrays
+    t = y.shape[2]
+    frames = np.array(sorted({0, t // 2, t - 1}), np.int64)
+    rows = boundary_rows(w.arch, w.latent_shape, w.n_bands, y.shape[3])
+    arrays["frames"] = frames
+    arrays["frame_out"] = np.ascontiguousarray(y[:, :, frames]).astype(np.float32)
+    arrays["rows"] = rows
+    arrays["row_out"] = np.ascontiguousarray(y[:, :, :, rows]).astype(np.float32)
+    return arrays
 
 
 def main(names):
@@ -67,19 +75,14 @@ def main(names):
         t0 = time.time()
         y = odec.decode(w.arch, W, z, None)
         dt = time.time() - t0
-        pos = sample_positions(y.shape, w.arch, w.latent_shape, w.n_bands)
-        flat = y.reshape(-1)
-        path = os.path.join(HERE, f"decode_samples_{name}.txt")
-        with open(path, "w") as fh:
-            fh.write(f"# float64 oracle dense decode of workload {name}: {w.description}\n")
-            fh.write("# written by tests/golden/make_decode_samples.py (oracle only); "
-                     f"decode took {dt:.0f} s on {os.cpu_count()} cores\n")
-            fh.write("shape " + " ".join(str(s) for s in y.shape) + "\n")
-            fh.write(f"l2norm {float(np.linalg.norm(flat)):.12e}\n")
-            fh.write(f"samples {len(pos)}\n")
-            for i in pos:
-                fh.write(f"{int(i)} {float(flat[i]):.9e}\n")
-        print(f"{name}: {len(pos)} samples, decode {dt:.0f} s -> {path}", flush=True)
+        arrays = fixture_arrays(y, w)
+        arrays["note"] = np.array(
+            f"float64 oracle dense decode of workload {name}: {w.description}; written by "
+            f"tests/golden/make_decode_samples.py (oracle only); decode took {dt:.0f} s on "
+            f"{os.cpu_count()} cores")
+        path = os.path.join(HERE, f"decode_full_{name}.npz")
+        np.savez_compressed(path, **arrays)
+        print(f"{name}: decode {dt:.0f} s -> {path}", flush=True)
 
 
 if __name__ == "__main__":

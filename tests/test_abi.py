@@ -153,3 +153,40 @@ def test_band_attention_workspace_and_arguments_checked_without_cuda(lib):
                 None) == 1                                                                # misaligned
     assert call(fake, fake, fake, fake, 1, 64, 64, 512, 1, None, 0, st, None) == 1        # needs work
     assert b"work" in lib.vaedec_last_error()
+
+
+def test_workspace_plan_is_the_largest_layers_live_set(lib):
+    """The band scheduler's workspace (row a15): every activation and the attention's scratch share
+    one arena, placed by lifetime.  For the Z-Image decoder the largest live set is the first
+    GroupNorm of the last stage at full resolution: its fp32 input (256 channels), the bf16
+    normalised output and the bf16 operand copy for the fused 1x1 shortcut, i.e.
+    B * H_out * W_out * 256 * (4 + 2 + 2) bytes; the placement reaches that bound exactly (plus a
+    1 MiB guard), and everything else the handle owns is small."""
+    mib = 1 << 20
+    for name in ("kl_zimage_512", "kl_zimage_1024", "kl_zimage_b2_800x1088", "flux2_1024"):
+        w = synth.WORKLOADS[name]
+        b, _, h, wd = w.latent_shape
+        p = w.arch.latent_patch
+        h_out, w_out = h * p * 8, wd * p * 8
+        plan = rbl.plan_workspace(w.arch, w.dtype, (b, 1, h, wd))
+        assert plan["peak_live"] == b * h_out * w_out * 256 * 8, name
+        assert plan["arena"] == plan["peak_live"] + mib, name
+        assert plan["peak_live"] <= plan["bytes"] <= plan["arena"] + 40 * mib, (name, plan)
+    # the 1024x1024 decode: 2.07 GiB in all (five whole-image buffers used to take 5.6 GB)
+    w = synth.WORKLOADS["kl_zimage_1024"]
+    assert rbl.plan_workspace(w.arch, w.dtype, (1, 1, 128, 128))["bytes"] <= 2.2e9
+    # linear in the pixel count: twice the width, twice the arena
+    a1 = rbl.plan_workspace(w.arch, w.dtype, (1, 1, 64, 64))["peak_live"]
+    a2 = rbl.plan_workspace(w.arch, w.dtype, (1, 1, 64, 128))["peak_live"]
+    assert a2 == 2 * a1
+
+
+def test_workspace_plan_rejects_bad_configs(lib):
+    cfg = rbl.make_config(synth.KL_TINY, "fp32", (1, 1, 16, 16))
+    cfg.family = 7
+    n = ctypes.c_size_t()
+    assert lib.vaedec_plan_workspace(ctypes.byref(cfg), ctypes.byref(n), None, None) == 1
+    assert lib.vaedec_plan_workspace(None, ctypes.byref(n), None, None) == 1
+    cfg = rbl.make_config(synth.WAN, "bf16", (1, 5, 60, 104))
+    assert lib.vaedec_plan_workspace(ctypes.byref(cfg), ctypes.byref(n), None, None) == 0
+    assert n.value > 0

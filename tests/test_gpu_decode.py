@@ -125,3 +125,19 @@ def test_shape_above_max_rejected(kl_small):
     z = torch.zeros((1, 16, 13, 20), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(rbl.VaedecError):
         kl_small.dec.decode(z, 1)
+
+
+def test_bf16_grid_the_attention_cannot_take_is_unsupported(kl_small):
+    """The bf16 path's fused attention streams keys as 16-byte rows: a latent grid whose H*W is
+    not a multiple of 8 is refused with UNSUPPORTED before any launch, and the handle stays usable."""
+    import torch
+    import row_band_layerwise_gb300 as rbl
+    n0 = kl_small.dec.launch_count()
+    for shp in ((1, 16, 3, 5), (1, 16, 1, 7), (1, 16, 5, 9)):
+        z = torch.zeros(shp, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(rbl.VaedecError) as ei:
+            kl_small.dec.decode(z, 1)
+        assert ei.value.status == 2, str(ei.value)
+        assert "multiple of 8" in str(ei.value)
+    assert kl_small.dec.launch_count() == n0
+    assert kl_small.decode(2).shape == (1, 3, 96, 160)
