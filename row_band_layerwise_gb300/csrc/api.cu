@@ -64,6 +64,7 @@ bool fault_now(int kind) {
 
 struct DevConv {
   void* w = nullptr;     // [rows][ntaps][cin] model dtype
+  void* wup = nullptr;   // bf16 upsample convs: [rows][4 phases x 7][cin] two-by-two phase weights (hi, lo parts)
   void* wn = nullptr;    // bf16 3x3(x kt) convs with 3 outputs: [16][kt * 3][cin], row = kernel_row * 3 + co
   float* b_sc = nullptr; // a resnet conv2: its bias plus the block's shortcut bias (fused shortcut)
   float* b = nullptr;    // [cout]
@@ -91,6 +92,43 @@ struct Act {
 };
 
 enum ConvKind { K3, K1, C3, UP, TIME };
+
+// Nearest-2x upsample then a 3x3 conv, output phase (py, px) on the low-resolution grid: the kernel
+// rows i fall on low-resolution row offsets floor((py + i - 1) / 2), i.e. two offsets per phase,
+// one taking a single kernel row and one the sum of two (likewise for columns).  So each phase is
+// a two-by-two conv whose weights are sums of 1, 2, 2 and 4 of the 3x3 weights.  Those sums are
+// not bf16 values; each is split into hi = bf16(sum) and lo = bf16(sum - hi), which together hold
+// it to 2^-17 of its size, so the phase has 7 weight taps (the single weight needs no lo part)
+// instead of the 9 taps of the direct form, with the same arithmetic up to that rounding.
+struct UpTap {
+  int oy, ox;            // low-resolution offsets
+  int lo;                // 0: hi part of the summed weight, 1: lo part
+  int nrow, ncol;        // kernel rows / columns summed
+  int rows[2], cols[2];
+};
+
+constexpr int kUpTaps = 7;
+
+void up_phase_taps(int ph, UpTap (&t)[kUpTaps]) {
+  const int py = ph >> 1, px = ph & 1;
+  // (offset, kernel indices) of the single-index and the two-index group along one axis
+  struct Grp { int off, n, idx[2]; };
+  const Grp ry1 = py == 0 ? Grp{-1, 1, {0, 0}} : Grp{1, 1, {2, 2}};
+  const Grp ry2 = py == 0 ? Grp{0, 2, {1, 2}} : Grp{0, 2, {0, 1}};
+  const Grp cx1 = px == 0 ? Grp{-1, 1, {0, 0}} : Grp{1, 1, {2, 2}};
+  const Grp cx2 = px == 0 ? Grp{0, 2, {1, 2}} : Grp{0, 2, {0, 1}};
+  auto mk = [](const Grp& r, const Grp& c, int lo) {
+    return UpTap{r.off, c.off, lo, r.n, c.n, {r.idx[0], r.idx[1]}, {c.idx[0], c.idx[1]}};
+  };
+  // weight stages of 3, 3 and 1 taps
+  t[0] = mk(ry1, cx1, 0);
+  t[1] = mk(ry1, cx2, 0);
+  t[2] = mk(ry1, cx2, 1);
+  t[3] = mk(ry2, cx1, 0);
+  t[4] = mk(ry2, cx1, 1);
+  t[5] = mk(ry2, cx2, 0);
+  t[6] = mk(ry2, cx2, 1);
+}
 
 std::vector<int> band_rows(int h, int n) {
   std::vector<int> r(n, h / n);
@@ -535,6 +573,19 @@ class Walker {
     if (e != cudaSuccess) set_err(VAEDEC_ERR_CUDA, std::string(what) + ": " + (why ? why : cudaGetErrorString(e)));
   }
 
+  // The exact two-by-two phase form of an upsample conv (weights w.wup).
+  static void fill_taps_up7(ConvGeom& g) {
+    std::memset(g.taps, 0, sizeof(g.taps));
+    g.nphase = 4;
+    g.ntaps = kUpTaps;
+    for (int ph = 0; ph < 4; ++ph) {
+      UpTap t[kUpTaps];
+      up_phase_taps(ph, t);
+      for (int k = 0; k < kUpTaps; ++k)
+        g.taps[ph][k] = ConvTap{0, (int8_t)t[k].oy, (int8_t)t[k].ox, (int8_t)(ph * kUpTaps + k)};
+    }
+  }
+
   static void fill_taps(ConvGeom& g, ConvKind kind, const DevConv& w) {
     std::memset(g.taps, 0, sizeof(g.taps));
     g.nphase = 1;
@@ -636,16 +687,32 @@ class Walker {
       g.res_f32 = (res && res->dt == kF32) ? 1 : 0;
       g.scale = 1.f;
     }
+    // an upsample conv runs in its exact two-by-two phase form where the channel-major kernel takes
+    // it (7 weight taps per phase instead of 9)
+    DevConv wrun = *w;
+    bool up7 = false;
+    if (kind == UP && w->wup != nullptr) {
+      ConvGeom g7 = g;
+      fill_taps_up7(g7);
+      if (conv_halo_t_applicable(g7)) {
+        g = g7;
+        wrun.w = w->wup;
+        wrun.ntaps = 4 * kUpTaps;
+        up7 = true;
+      }
+    }
     // a fused 1x1 shortcut (sc_x, weights sc_name) adds its flops and uses the combined bias
     const DevConv* scw = sc_x ? W(sc_name) : nullptr;
     if (sc_x && (!scw || !w->b_sc)) return y;
     double flops = conv_flops(x, y, *w, kind);
     if (scw) flops += 2.0 * (double)y.pixels() * scw->cout * scw->cin;
+    // multiply-adds the tensor cores execute (the exact phase form: 7 of the 9 taps' worth)
+    const double exec_flops = up7 ? flops * kUpTaps / 9.0 : flops;
     std::ostringstream d;
     d << "kind=conv name=" << name << " conv="
       << (kind == K3 ? "k3" : kind == K1 ? "k1" : kind == C3 ? "causal3" : kind == UP ? "up2x_k3" : "time")
       << io(x, sc_x ? sc_x : res, y) << " res=" << (res ? 1 : 0) << " final=" << (final_out ? 1 : 0)
-      << " taps=" << w->ntaps << " flops=" << flops
+      << " taps=" << w->ntaps << " flops=" << flops << " exec_flops=" << exec_flops
       << " kernel=" << (scw ? "conv_halo_t" : conv_kernel(g, res != nullptr, copy != nullptr, w->wn != nullptr));
     if (scw) d << " shortcut=" << sc_name;
     if (begin(d.str())) {
@@ -681,8 +748,8 @@ class Walker {
           csc.cin = scw->cin;
           csc.w_rows = scw->rows;
         }
-        const int chunks = launch(g, in, *w, w->w, scw ? w->b_sc : w->b, res ? ptr(*res) : nullptr, nullptr, ptr(y),
-                                  out2, name.c_str(), scw ? &csc : nullptr);
+        const int chunks = launch(g, in, wrun, wrun.w, scw ? w->b_sc : w->b, res ? ptr(*res) : nullptr, nullptr,
+                                  ptr(y), out2, name.c_str(), scw ? &csc : nullptr);
         if (chunks > 0) {
           y.stats_chunks = chunks;
           y.stats_epoch = ++stats_epoch_;
@@ -1174,6 +1241,17 @@ uint16_t f32_to_bf16(float f) {
   return static_cast<uint16_t>(u >> 16);
 }
 
+float bf16_to_f32(uint16_t b) {
+  const uint32_t u = static_cast<uint32_t>(b) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+bool ends_with(const std::string& s, const std::string& suffix) {
+  return s.size() >= suffix.size() && s.compare(s.size() - suffix.size(), suffix.size(), suffix) == 0;
+}
+
 size_t numel(const vaedec_tensor& t) {
   size_t n = 1;
   for (int i = 0; i < t.ndim; ++i) n *= (size_t)t.shape[i];
@@ -1490,6 +1568,33 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
           s = h->dalloc(&dc.wn, nn * 2, nd.name.c_str());
           if (s != VAEDEC_OK) return bail(s);
           e = cudaMemcpy(dc.wn, wn.data(), nn * 2, cudaMemcpyHostToDevice);
+          if (e != cudaSuccess) return bail(cuda_fail(e, "weight upload"));
+        }
+        if (nd.kh == 3 && nd.kw == 3 && kt == 1 && !nd.linear &&
+            (ends_with(nd.name, ".upsamplers.0.conv") || ends_with(nd.name, ".upsamplers.0.resample.1"))) {
+          // the exact two-by-two phase form: per phase 7 taps, summed weights split into hi and lo
+          const size_t nu = (size_t)dc.rows * 4 * kUpTaps * nd.cin;
+          std::vector<uint16_t> wu(nu, 0);
+          for (int ph = 0; ph < 4; ++ph) {
+            UpTap tp[kUpTaps];
+            up_phase_taps(ph, tp);
+            for (int k = 0; k < kUpTaps; ++k)
+              for (int co = 0; co < nd.cout; ++co)
+                for (int ci = 0; ci < nd.cin; ++ci) {
+                  double sum = 0.0;
+                  for (int a = 0; a < tp[k].nrow; ++a)
+                    for (int c = 0; c < tp[k].ncol; ++c) {
+                      const int t = tp[k].rows[a] * 3 + tp[k].cols[c];
+                      sum += bf16_to_f32(buf[((size_t)co * ntaps + t) * nd.cin + ci]);
+                    }
+                  const uint16_t hi = f32_to_bf16(static_cast<float>(sum));
+                  const uint16_t v = tp[k].lo ? f32_to_bf16(static_cast<float>(sum - bf16_to_f32(hi))) : hi;
+                  wu[((size_t)co * 4 * kUpTaps + ph * kUpTaps + k) * nd.cin + ci] = v;
+                }
+          }
+          s = h->dalloc(&dc.wup, nu * 2, nd.name.c_str());
+          if (s != VAEDEC_OK) return bail(s);
+          e = cudaMemcpy(dc.wup, wu.data(), nu * 2, cudaMemcpyHostToDevice);
           if (e != cudaSuccess) return bail(cuda_fail(e, "weight upload"));
         }
       } else {

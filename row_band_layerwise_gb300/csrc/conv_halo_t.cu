@@ -206,7 +206,10 @@ __device__ __forceinline__ void gn_store(const HaloTParams& p, const TileT& d, i
 // waiter saw the abort flag raised.
 __device__ __forceinline__ bool stage_handoff(bool aborted) { return bar_sync_or(1, 64, aborted); }
 
-template <int BK, int kOut>
+// kNsp: spatial taps per causal frame, 9 (three kernel rows of 3), or 7 for an upsample conv in its exact
+// two-by-two phase form (weight stages of 3, 3 and 1 taps).  A compile-time count keeps the MMA issue
+// loop free of per-stage tap tests.
+template <int BK, int kOut, int kNsp>
 __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_constant__ HaloTParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t x_full[2], x_empty[2];
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smX = smem;
   uint8_t* smW = smem + 2 * p.x_stage_bytes;
-  const int nsp = g.ntaps / p.ndt;   // 9 spatial taps per causal frame, in three kernel rows of 3
+  const int nsp = g.ntaps / p.ndt;   // 9 spatial taps per causal frame (kernel rows of 3), or 7
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -263,7 +266,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
   pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
   const int nac = p.ndt * p.n_kchunks;   // staged activation chunks per tile
-  const int ngrp = nsp / 3;              // weight stages per chunk (kernel rows)
+  const int ngrp = (nsp + 2) / 3;        // weight stages per chunk (up to 3 taps each)
 
   if (warp == 0) {
     // ---- TMA producer: activation chunks (R + 2 rows) and weight stages (3 taps), tile after tile
@@ -293,10 +296,11 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
           }
           ++acg;
           for (int gi = 0; gi < ngrp; ++gi) {
+            const int ntp = kNsp == 9 ? 3 : min(3, nsp - 3 * gi);   // taps in this weight stage
             if (kbg >= p.nw && !mbar_wait(&w_empty[sw], wpar, p.status, kErrTimeoutEmpty, &abort_flag)) break;
-            mbar_arrive_expect_tx(&w_full[sw], w_tx);
+            mbar_arrive_expect_tx(&w_full[sw], kNsp == 9 ? w_tx : static_cast<uint32_t>(ntp) * p.w_tap_bytes);
             uint8_t* ws = smW + sw * p.w_stage_bytes;
-            for (int tp = 0; tp < 3; ++tp)
+            for (int tp = 0; tp < ntp; ++tp)
               tma_load_3d(ws + tp * p.w_tap_bytes, &p.tmW, &w_full[sw], kc * BK,
                           g.taps[d.phase][dti * nsp + gi * 3 + tp].wtap, d.m0);
             ++kbg;
@@ -416,6 +420,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
         const uint64_t dBs = dB0 + static_cast<uint64_t>(sx * x_stage16);
 #pragma unroll
         for (int gi = 0; gi < 3; ++gi) {
+          const int ntp = (kNsp == 9 || gi < 2) ? 3 : kNsp - 6;   // taps of this stage (compile time)
           const bool aborted = stage_handoff(false);
           tc_fence_after();
           if (lane == 0) {
@@ -423,6 +428,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
               const uint64_t dAs = dA0 + static_cast<uint64_t>(sw * w_stage16);
 #pragma unroll
               for (int tp = 0; tp < 3; ++tp) {
+                if (tp >= ntp) continue;   // resolved at compile time in the unrolled loop
                 const uint64_t dAt = dAs + tp * w_tap16;
                 const uint64_t dBt = dBs + xoff[gi * 3 + tp];
 #pragma unroll
@@ -760,15 +766,16 @@ int round_up_t(int a, int b) { return (a + b - 1) / b * b; }
 // rows wide enough for at least 96-pixel tiles.
 bool conv_halo_t_applicable(const ConvGeom& g) {
   if (g.out_chfirst || g.time_up_c > 0) return false;
-  if (g.ntaps != 9 && g.ntaps != 27) return false;
+  if (g.ntaps != 9 && g.ntaps != 27 && !(g.ntaps == 7 && g.nphase == 4)) return false;
   if (g.W < 96) return false;
   if (g.Cout % 16 != 0 || g.Cin % 16 != 0) return false;
-  const int ndt = g.ntaps / 9;
+  const int ndt = g.ntaps == 27 ? 3 : 1;
+  const int nsp = g.ntaps / ndt;
   for (int ph = 0; ph < g.nphase; ++ph)
     for (int d = 0; d < ndt; ++d)
-      for (int s = 0; s < 9; ++s) {
-        const ConvTap t = g.taps[ph][d * 9 + s];
-        if (t.dt != g.taps[ph][d * 9].dt) return false;
+      for (int s = 0; s < nsp; ++s) {
+        const ConvTap t = g.taps[ph][d * nsp + s];
+        if (t.dt != g.taps[ph][d * nsp].dt) return false;
         if (t.dy < -1 || t.dy > 1 || t.dx < -1 || t.dx > 1) return false;
       }
   return true;
@@ -828,7 +835,7 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
     return cudaErrorInvalidValue;
   }
   p.n_kchunks = g.Cin / bk;
-  p.ndt = g.ntaps / 9;
+  p.ndt = g.ntaps == 27 ? 3 : 1;
   p.row_bytes = static_cast<uint32_t>(2 * p.half * bk * 2);
   p.x_stage_bytes = static_cast<uint32_t>((p.R + 2) * p.row_bytes);
   p.w_tap_bytes = static_cast<uint32_t>(128 * bk * 2);
@@ -970,16 +977,29 @@ cudaError_t launch_conv_halo_t(const ConvGeom& g, const void* in, const void* wt
     if (r == cudaSuccess) launch_pdl(kern, (unsigned)nblocks, kThreadsT, smem, stream, p);
     return r;
   };
-  switch (bk * 4 + p.tma_out) {
-    case 64 * 4 + 0: e = go(conv_halo_t_kernel<64, 0>); break;
-    case 64 * 4 + 1: e = go(conv_halo_t_kernel<64, 1>); break;
-    case 64 * 4 + 2: e = go(conv_halo_t_kernel<64, 2>); break;
-    case 32 * 4 + 0: e = go(conv_halo_t_kernel<32, 0>); break;
-    case 32 * 4 + 1: e = go(conv_halo_t_kernel<32, 1>); break;
-    case 32 * 4 + 2: e = go(conv_halo_t_kernel<32, 2>); break;
-    case 16 * 4 + 0: e = go(conv_halo_t_kernel<16, 0>); break;
-    case 16 * 4 + 1: e = go(conv_halo_t_kernel<16, 1>); break;
-    default: e = go(conv_halo_t_kernel<16, 2>); break;
+  if (g.ntaps == 7) {
+    // upsample convs in the two-by-two phase form: the serial epilogue (no TMA stores)
+    if (p.tma_out != 0) {
+      *why = "the two-by-two upsample form has no TMA-store epilogue";
+      return cudaErrorInvalidValue;
+    }
+    switch (bk) {
+      case 64: e = go(conv_halo_t_kernel<64, 0, 7>); break;
+      case 32: e = go(conv_halo_t_kernel<32, 0, 7>); break;
+      default: e = go(conv_halo_t_kernel<16, 0, 7>); break;
+    }
+  } else {
+    switch (bk * 4 + p.tma_out) {
+      case 64 * 4 + 0: e = go(conv_halo_t_kernel<64, 0, 9>); break;
+      case 64 * 4 + 1: e = go(conv_halo_t_kernel<64, 1, 9>); break;
+      case 64 * 4 + 2: e = go(conv_halo_t_kernel<64, 2, 9>); break;
+      case 32 * 4 + 0: e = go(conv_halo_t_kernel<32, 0, 9>); break;
+      case 32 * 4 + 1: e = go(conv_halo_t_kernel<32, 1, 9>); break;
+      case 32 * 4 + 2: e = go(conv_halo_t_kernel<32, 2, 9>); break;
+      case 16 * 4 + 0: e = go(conv_halo_t_kernel<16, 0, 9>); break;
+      case 16 * 4 + 1: e = go(conv_halo_t_kernel<16, 1, 9>); break;
+      default: e = go(conv_halo_t_kernel<16, 2, 9>); break;
+    }
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
