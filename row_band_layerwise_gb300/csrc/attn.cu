@@ -58,7 +58,6 @@ template <typename SIn, typename P>
 __global__ void __launch_bounds__(kSmThreads) softmax_rows_kernel(const SIn* __restrict__ S, P* __restrict__ Pm,
                                                                   float* __restrict__ inv_l, int nk) {
   pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
   __shared__ float red[32];
   const long long row = blockIdx.x;
   const SIn* s = S + row * nk;
@@ -88,7 +87,6 @@ template <typename SIn, typename P, int NV>
 __global__ void __launch_bounds__(kSmThreads) softmax_rows_reg_kernel(const SIn* __restrict__ S, P* __restrict__ Pm,
                                                                       float* __restrict__ inv_l, int nk) {
   pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
   __shared__ float red[32];
   const long long row = blockIdx.x;
   const SIn* srow = S + row * nk;
@@ -126,7 +124,6 @@ template <typename T>
 __global__ void to_channels_last_kernel(const T* __restrict__ x, T* __restrict__ y, int C, long long spatial,
                                         long long total) {
   pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int c = static_cast<int>(i % C);
@@ -190,7 +187,6 @@ template <typename T>
 __global__ void band_cols_kernel(const T* __restrict__ src, T* __restrict__ dst, int H, int W, int C, int c0, int nc,
                                  int to_band) {
   pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
   const int vpp = C * static_cast<int>(sizeof(T)) / 16;   // vectors per pixel
   const long long n = static_cast<long long>(H) * nc * vpp;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
@@ -241,7 +237,6 @@ template <typename T>
 __global__ void latent_frontend_kernel(const T* __restrict__ zp, T* __restrict__ y, int B, int C, int Hp, int Wp,
                                        int p, const float* __restrict__ scale, const float* __restrict__ shift) {
   pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
   const int H = Hp * p, W = Wp * p;
   const long long n = static_cast<long long>(B) * H * W * C;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;

@@ -178,7 +178,6 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   pdl_wait();   // the previous kernel on the stream has finished and its writes are visible
-  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
 
   if (warp == 0) {
@@ -515,7 +514,6 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
 __global__ void attn_combine_kernel(const float* __restrict__ part, const float2* __restrict__ ml,
                                     __nv_bfloat16* __restrict__ out, long long rows, int C, int splits) {
   pdl_wait();
-  pdl_trigger();
   const int c4 = C >> 2;
   const long long n = rows * c4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {

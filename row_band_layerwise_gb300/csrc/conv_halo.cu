@@ -132,7 +132,6 @@ __global__ void __launch_bounds__(kHaloThreads, 1) conv_halo_kernel(const __grid
   tc_fence_after();
   // the previous kernel on the stream has finished and its writes are visible from here on
   pdl_wait();
-  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
   const int nac = p.ndt * p.n_kchunks;
 

@@ -263,7 +263,6 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
   tc_fence_after();
   // the previous kernel on the stream has finished and its writes are visible from here on
   pdl_wait();
-  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
   const int nac = p.ndt * p.n_kchunks;   // staged activation chunks per tile
   const int ngrp = (nsp + 2) / 3;        // weight stages per chunk (up to 3 taps each)

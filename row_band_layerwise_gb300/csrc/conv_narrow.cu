@@ -103,7 +103,6 @@ __global__ void __launch_bounds__(kThreadsN, 1) conv_narrow_kernel(const __grid_
   tc_fence_after();
   // the previous kernel on the stream has finished and its writes are visible from here on
   pdl_wait();
-  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
 
   // tile t -> (tx, ty, frame, sample)

@@ -17,7 +17,6 @@ __global__ void conv_simple_f32_kernel(const ConvGeom g, const float* __restrict
                                        const float* __restrict__ residual, const float* __restrict__ rowscale,
                                        float* __restrict__ out, long long total) {
   pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     long long r = idx;

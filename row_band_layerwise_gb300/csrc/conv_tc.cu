@@ -119,7 +119,6 @@ __global__ void __launch_bounds__(kThreads) conv_tc_kernel(const __grid_constant
   tc_fence_after();
   // the previous kernel on the stream has finished and its writes are visible from here on
   pdl_wait();
-  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
 
   const int ksteps = g.ntaps * p.n_kchunks;

@@ -137,7 +137,6 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_cm_kernel(const __grid_cons
   tc_fence_after();
   // the previous kernel on the stream has finished and its writes are visible from here on
   pdl_wait();
-  pdl_trigger();
   const uint32_t tmem = tmem_base_sh;
 
   if (warp == 0) {

@@ -101,7 +101,6 @@ __global__ void __launch_bounds__(kGnThreads) gn_partials_kernel(const T* __rest
                                                                  int G, int chunk_rows, int n_chunks,
                                                                  GnPartial* __restrict__ part) {
   pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
   extern __shared__ float sh[];   // [nthreads][8][3]
   const int chunk = blockIdx.x, b = blockIdx.y;
   const int vpp = C / 8;                        // vectors per pixel
@@ -184,7 +183,6 @@ __global__ void __launch_bounds__(kFinThreads) gn_finalize_kernel(const GnPartia
                                                                   float* __restrict__ scale,
                                                                   float* __restrict__ shift) {
   pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
   __shared__ float sn[kFinThreads], sm[kFinThreads], s2[kFinThreads];
   const int b = blockIdx.x / G, g = blockIdx.x % G;
   const int t = threadIdx.x;
@@ -247,7 +245,6 @@ __global__ void __launch_bounds__(1024) gn_apply_kernel(const Tin* __restrict__ 
                                                        const float* __restrict__ scale,
                                                        const float* __restrict__ shift, int silu) {
   pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
   // 32-bit vector indices (the launcher guarantees nvec < 2^31); the channel of a vector is a
   // mask when C / 8 is a power of two (every GroupNorm width here), else a 32-bit remainder
   const uint32_t vpp = static_cast<uint32_t>(C / 8);
@@ -314,7 +311,6 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(const Tin* __restrict__ x
                                                        Tout* __restrict__ y_raw, long long pixels, int C, int gs,
                                                        const float* __restrict__ gamma, int silu) {
   pdl_wait();   // the previous kernel on the stream has finished (programmatic launch)
-  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int j = lane & (gs - 1);          // position in the group
   const int ppw = 32 / gs;                // pixels per warp step

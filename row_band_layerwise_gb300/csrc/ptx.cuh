@@ -120,12 +120,14 @@ __device__ __forceinline__ bool bar_sync_or(int id, int count, bool v) {
   return r != 0;
 }
 
-// Programmatic dependent launch.  Every kernel of this library is launched so that it may start while
-// the previous kernel on its stream is still finishing; it calls pdl_wait() before its first access to
-// global memory (the wait returns once the previous grid has completed and its writes are visible),
-// and pdl_trigger() to let the next kernel start its own prologue early.
+// Programmatic dependent launch.  Every kernel of this library is launched with programmatic stream
+// serialization and calls pdl_wait() before its first access to global memory (the wait returns once
+// the previous grid has completed and its writes are visible).  No kernel signals its dependents
+// early (griddepcontrol.launch_dependents): the next kernel is released as the previous one's CTAs
+// finish, so its launch and prologue overlap only that tail.  An early signal let a dependent's CTAs
+// occupy SMs that a many-wave kernel (GroupNorm apply, the one-tile convs) still needed for its later
+// waves; the 1024x1024 decode took 10.39 ms with the early signal and 9.61 ms without it.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
