@@ -141,3 +141,24 @@ def test_bf16_grid_the_attention_cannot_take_is_unsupported(kl_small):
         assert "multiple of 8" in str(ei.value)
     assert kl_small.dec.launch_count() == n0
     assert kl_small.decode(2).shape == (1, 3, 96, 160)
+
+
+def test_one_workspace_layout_serves_every_smaller_shape():
+    """The workspace arena is laid out once, at create time, for max_latent; every smaller latent
+    reuses that layout.  A 16x16-bounded handle decodes an 8x8 latent (whose last stage is too
+    narrow for the fused 1x1 shortcut, so the walk takes the other branch) and a 16x12 one, bit for
+    bit as handles created for exactly those shapes, and within the bars of the oracle."""
+    from gpu_helpers import Case
+    import torch
+    big = Case(synth.KL_ZIMAGE, "bf16", (1, 16, 16, 16))
+    for shp in [(1, 16, 8, 8), (1, 16, 16, 12)]:
+        exact = Case(synth.KL_ZIMAGE, "bf16", shp)
+        z = exact.z_dev
+        a = big.dec.decode(z, 2)
+        torch.cuda.synchronize()
+        big.dec.sync()
+        b = exact.decode(2)
+        assert bool((a == b).all()), shp
+        assert_bf16_parity(a.float().cpu().numpy(), exact.oracle())
+        exact.dec.close()
+    big.dec.close()
