@@ -381,6 +381,11 @@ def run_ours(args, w: synth.Workload):
                          "executed_flops_per_step": dom_exec,
                          "executed_tflops": dom_exec / (dom_ms / 1e3) / 1e12 if dom_ms > 0 else None,
                          "executed_frac": dom_exec / (dom_ms / 1e3) / 1e12 / peak if dom_ms > 0 and peak else None,
+                         "conv_tensor_util_pct": 100.0 * achieved / peak if peak else None,
+                         "conv_tensor_util_note": "the metric's conv tensor-pipe utilisation: the dominant conv "
+                                                  "kernel's algorithmic flops per second over the measured bf16 "
+                                                  "peak; ncu's sm__pipe_tensor_cycles_active for sampled launches "
+                                                  "is in profiles/conv_halo_t_kernel_kl_zimage_512_full.md",
                          "per_launch": "algorithmic flops (nearest-2x then 3x3 counted as 3x3 on the high-resolution "
                                        "output) / CUDA-event duration, summed over its launches; executed_* count "
                                        "the multiply-adds the tensor cores run",
