@@ -402,6 +402,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
     const uint64_t dB0 = smem_desc_kmajor(smem_u32(smX), SwzT<BK>::kSbo, SwzT<BK>::kMode);
     const uint32_t w_stage16 = p.w_stage_bytes >> 4, w_tap16 = p.w_tap_bytes >> 4;
     const uint32_t x_stage16 = p.x_stage_bytes >> 4, row16 = p.row_bytes >> 4;
+    const bool one_row = p.R == 1;
     int it = 0, sw = 0, acg = 0;
     for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
       const int phase = decode_tile(p, t).phase;
@@ -425,18 +426,32 @@ __global__ void __launch_bounds__(kThreadsT, 1) conv_halo_t_kernel(const __grid_
           if (lane == 0) {
             if (!aborted) {
               const uint64_t dAs = dA0 + static_cast<uint64_t>(sw * w_stage16);
+              if (one_row) {
+                // one-row tiles: the stage's MMAs back to back with no test between them (the tensor
+                // pipe queues few MMAs, so work between two issues can leave it idle)
 #pragma unroll
-              for (int tp = 0; tp < 3; ++tp) {
-                if (tp >= ntp) continue;   // resolved at compile time in the unrolled loop
-                const uint64_t dAt = dAs + tp * w_tap16;
-                const uint64_t dBt = dBs + xoff[gi * 3 + tp];
+                for (int tp = 0; tp < 3; ++tp) {
+                  if (tp >= ntp) continue;   // resolved at compile time in the unrolled loop
+                  const uint64_t dAt = dAs + tp * w_tap16;
+                  const uint64_t dBt = dBs + xoff[gi * 3 + tp];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                  if (r < p.R) {
+                  for (int k = 0; k < BK / 16; ++k)
+                    tc_mma_bf16(dcol, dAt + 2 * k, dBt + 2 * k, idesc, (ac | gi | tp | k) != 0 ? 1u : 0u);
+                }
+              } else {
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                      tc_mma_bf16(dcol + static_cast<uint32_t>(r * p.npx), dAt + 2 * k, dBt + r * row16 + 2 * k, idesc,
-                                  (ac | gi | tp | k) != 0 ? 1u : 0u);
+                for (int tp = 0; tp < 3; ++tp) {
+                  if (tp >= ntp) continue;
+                  const uint64_t dAt = dAs + tp * w_tap16;
+                  const uint64_t dBt = dBs + xoff[gi * 3 + tp];
+#pragma unroll
+                  for (int r = 0; r < 4; ++r) {
+                    if (r < p.R) {
+#pragma unroll
+                      for (int k = 0; k < BK / 16; ++k)
+                        tc_mma_bf16(dcol + static_cast<uint32_t>(r * p.npx), dAt + 2 * k, dBt + r * row16 + 2 * k,
+                                    idesc, (ac | gi | tp | k) != 0 ? 1u : 0u);
+                    }
                   }
                 }
               }
