@@ -184,6 +184,8 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
     // ---- K producer: each item's query tile, then the key stages of every block in order
     if (lane == 0) {
       int g = 0, it = 0, qn = 0;   // key stages and query tiles issued
+      int s = 0;                   // slot of key stage g and the parity of the empty phase that frees it
+      uint32_t epar = 1u;
       for (int t = blockIdx.x; t < p.n_items && !abort_flag; t += gridDim.x, ++it) {
         const FItem d = flash_item(p, t);
         if (it >= 1 && !mbar_wait(&q_empty, static_cast<uint32_t>(it - 1) & 1u, p.status, kErrTimeoutEmpty,
@@ -197,10 +199,7 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
         bool stop = false;
         for (int kb = d.kb0; kb < d.kb1 && !stop; ++kb) {
           for (int kc = 0; kc < p.kst; ++kc) {
-            const int s = g % p.nk;
-            if ((g >= p.nk && !mbar_wait(&kempty[s], (static_cast<uint32_t>(g / p.nk) & 1u) ^ 1u, p.status,
-                                         kErrTimeoutEmpty, &abort_flag)) ||
-                abort_flag) {
+            if ((g >= p.nk && !mbar_wait(&kempty[s], epar, p.status, kErrTimeoutEmpty, &abort_flag)) || abort_flag) {
               stop = true;
               break;
             }
@@ -208,6 +207,10 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
             tma_load_3d(kring + s * kFKSlot, &p.tmK, &kfull[s], kc * 128, kb * 128, d.f);
             tma_load_3d(kring + s * kFKSlot + kFSlot, &p.tmK, &kfull[s], kc * 128 + 64, kb * 128, d.f);
             ++g;
+            if (++s == p.nk) {
+              s = 0;
+              epar ^= 1u;
+            }
           }
         }
         if (stop) break;
@@ -224,21 +227,24 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
     if (lane == 0) {
       const uint32_t v_tx = p.vslot;
       int g = 0;
+      int s = 0;              // slot of value stage g and the parity of the empty phase that frees it
+      uint32_t epar = 1u;
       bool stop = false;
       for (int t = blockIdx.x; t < p.n_items && !abort_flag && !stop; t += gridDim.x) {
         const FItem d = flash_item(p, t);
         for (int kb = d.kb0; kb < d.kb1 && !stop; ++kb) {
           for (int v = 0; v < 2; ++v) {
-            const int s = g % p.nv;
-            if ((g >= p.nv && !mbar_wait(&vempty[s], (static_cast<uint32_t>(g / p.nv) & 1u) ^ 1u, p.status,
-                                         kErrTimeoutEmpty, &abort_flag)) ||
-                abort_flag) {
+            if ((g >= p.nv && !mbar_wait(&vempty[s], epar, p.status, kErrTimeoutEmpty, &abort_flag)) || abort_flag) {
               stop = true;
               break;
             }
             mbar_arrive_expect_tx(&vfull[s], v_tx);
             tma_load_3d(vring + s * p.vslot, &p.tmV, &vfull[s], kb * 128 + v * 64, d.half * p.half_c, d.f);
             ++g;
+            if (++s == p.nv) {
+              s = 0;
+              epar ^= 1u;
+            }
           }
         }
       }
@@ -253,7 +259,9 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
       const uint32_t idesc_s = idesc_bf16_f32(128, 128);
       const uint64_t dQ0 = smem_desc_kmajor(smem_u32(smQ), 1024, 2);
       const uint64_t dK0 = smem_desc_kmajor(smem_u32(kring), 1024, 2);
-      int g = 0, it = 0;
+      int it = 0;
+      int s = 0;              // key slot of the next stage, and the parity of its full phase: running
+      uint32_t kpar = 0u;     // counts, so the issue loop has no division between two MMA groups
       long long sg = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x, ++it) {
@@ -264,9 +272,8 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
             ok = mbar_wait(&p_free[sg & 1], (static_cast<uint32_t>(sg >> 1) & 1u) ^ 1u, p.status, kErrTimeoutEmpty,
                            &abort_flag);
           const uint32_t dS = tmem + kFSCol + static_cast<uint32_t>(sg & 1) * 128u;
-          for (int kc = 0; kc < p.kst && ok; ++kc, ++g) {
-            const int s = g % p.nk;
-            ok = mbar_wait(&kfull[s], static_cast<uint32_t>(g / p.nk) & 1u, p.status, kErrTimeoutFull, &abort_flag);
+          for (int kc = 0; kc < p.kst && ok; ++kc) {
+            ok = mbar_wait(&kfull[s], kpar, p.status, kErrTimeoutFull, &abort_flag);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -278,6 +285,10 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
                 tc_mma_bf16(dS, da + 2 * k, db + 2 * k, idesc_s, (kc | h | k) != 0 ? 1u : 0u);
             }
             tc_commit(&kempty[s]);
+            if (++s == p.nk) {
+              s = 0;
+              kpar ^= 1u;
+            }
           }
           if (!ok) break;
           tc_commit(&s_full[sg & 1]);
@@ -295,7 +306,9 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
     if (lane == 0) {
       const uint32_t idesc_v = idesc_bf16_f32(128, p.half_c);
       const uint64_t dV0 = smem_desc_kmajor(smem_u32(vring), 1024, 2);
-      int g = 0, it = 0;
+      int it = 0;
+      int s = 0;              // value slot of the next stage and the parity of its full phase (running counts)
+      uint32_t vpar = 0u;
       long long pg = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x, ++it) {
@@ -307,9 +320,8 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
           ok = mbar_wait(&p_full, static_cast<uint32_t>(pg) & 1u, p.status, kErrTimeoutFull, &abort_flag);
           if (ok && first && it >= 1)
             ok = mbar_wait(&o_free, static_cast<uint32_t>(it - 1) & 1u, p.status, kErrTimeoutEmpty, &abort_flag);
-          for (int b = 0; b < 2 && ok; ++b, ++g) {
-            const int s = g % p.nv;
-            ok = mbar_wait(&vfull[s], static_cast<uint32_t>(g / p.nv) & 1u, p.status, kErrTimeoutFull, &abort_flag);
+          for (int b = 0; b < 2 && ok; ++b) {
+            ok = mbar_wait(&vfull[s], vpar, p.status, kErrTimeoutFull, &abort_flag);
             if (!ok) break;
             tc_fence_after();
             // P of the block: 64 columns of its score buffer, keys 2c and 2c + 1 in column c
@@ -319,6 +331,10 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
             for (int k = 0; k < 4; ++k)
               tc_mma_bf16_tmem_a(tmem, ta + 8 * k, db + 2 * k, idesc_v, (!first || b != 0 || k != 0) ? 1u : 0u);
             tc_commit(&vempty[s]);
+            if (++s == p.nv) {
+              s = 0;
+              vpar ^= 1u;
+            }
           }
           if (!ok) break;
           tc_commit(&p_free[pg & 1]);
