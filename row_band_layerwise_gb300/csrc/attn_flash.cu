@@ -129,7 +129,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& sum) {
 __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_constant__ FlashParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t kfull[kFMaxStages], kempty[kFMaxStages], vfull[kFMaxStages], vempty[kFMaxStages];
-  __shared__ __align__(8) uint64_t q_full, q_empty, s_full[2], p_free[2], p_full, o_full, o_free;
+  __shared__ __align__(8) uint64_t q_full, q_empty, s_full[2], p_free[2], p_full[2], o_full, o_free;
   __shared__ __align__(8) uint64_t s_done, v_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
@@ -155,8 +155,11 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_free[i], 1);
+      // probabilities ready, per block parity: the softmax can finish block g + 1 before the product
+      // has observed block g (block g + 2 needs block g's product), so one barrier could run two
+      // phases ahead of the product's parity wait
+      mbar_init(&p_full[i], 1);
     }
-    mbar_init(&p_full, 1);
     mbar_init(&o_full, 1);
     mbar_init(&o_free, 1);
     mbar_init(&s_done, 1);
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
           const bool first = kb == d.kb0;
           // the block's probabilities are in tensor memory (and the accumulator rescaled); before the
           // item's first block, the previous item's output has also been read out of the accumulator
-          ok = mbar_wait(&p_full, static_cast<uint32_t>(pg) & 1u, p.status, kErrTimeoutFull, &abort_flag);
+          ok = mbar_wait(&p_full[pg & 1], static_cast<uint32_t>(pg >> 1) & 1u, p.status, kErrTimeoutFull, &abort_flag);
           if (ok && first && it >= 1)
             ok = mbar_wait(&o_free, static_cast<uint32_t>(it - 1) & 1u, p.status, kErrTimeoutEmpty, &abort_flag);
           for (int b = 0; b < 2 && ok; ++b) {
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_flash_kernel(const __grid_c
           dead = true;
           break;
         }
-        if (r == 0) mbar_arrive(&p_full);
+        if (r == 0) mbar_arrive(&p_full[sg & 1]);
         if (jj >= 1 && !waited) {
           // keep step with the barrier: one wait per phase (nothing later can complete it again first);
           // a failure here is acted on at the next sync point
