@@ -249,6 +249,16 @@ __global__ void __launch_bounds__(1024) gn_apply_kernel(const Tin* __restrict__ 
   // mask when C / 8 is a power of two (every GroupNorm width here), else a 32-bit remainder
   const uint32_t vpp = static_cast<uint32_t>(C / 8);
   const uint32_t step = gridDim.x * blockDim.x;
+  // a thread's channels stay the same on every iteration when the grid stride is a multiple of C / 8
+  // (launchers use multiples of 256 threads, C / 8 <= 64); with one sample its scale and shift are
+  // then fixed and loaded once
+  const bool fixed = vec_per_sample == nvec && vpp_log2 >= 0 && (step & (vpp - 1)) == 0;
+  float fa[8], fsh[8];
+  if (fixed) {
+    const uint32_t c0 = ((blockIdx.x * blockDim.x + threadIdx.x) & (vpp - 1)) * 8;
+    load8f(scale + c0, fa);
+    load8f(shift + c0, fsh);
+  }
   // two 8-element vectors per thread and iteration: more loads in flight
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += 2 * step) {
     const uint32_t i2 = i + step;
@@ -262,11 +272,19 @@ __global__ void __launch_bounds__(1024) gn_apply_kernel(const Tin* __restrict__ 
       const uint32_t iv = h == 0 ? i : i2;
       float (&u)[8] = h == 0 ? v : w;
       if (y_raw != nullptr) Vec8<Tout>::store(y_raw + static_cast<size_t>(iv) * 8, u);
-      const uint32_t bs = vec_per_sample == nvec ? 0u : iv / vec_per_sample;
-      const uint32_t c0 = (vpp_log2 >= 0 ? (iv & (vpp - 1)) : iv % vpp) * 8;
       float a[8], sh[8], o[8];
-      load8f(scale + static_cast<size_t>(bs) * C + c0, a);
-      load8f(shift + static_cast<size_t>(bs) * C + c0, sh);
+      if (fixed) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          a[j] = fa[j];
+          sh[j] = fsh[j];
+        }
+      } else {
+        const uint32_t bs = vec_per_sample == nvec ? 0u : iv / vec_per_sample;
+        const uint32_t c0 = (vpp_log2 >= 0 ? (iv & (vpp - 1)) : iv % vpp) * 8;
+        load8f(scale + static_cast<size_t>(bs) * C + c0, a);
+        load8f(shift + static_cast<size_t>(bs) * C + c0, sh);
+      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float t = fmaf(u[j], a[j], sh[j]);
