@@ -103,7 +103,10 @@ typedef struct {
 } vaedec_config;
 
 /*
- * Create a decoder on the current CUDA device.  Copies and repacks every weight
+ * Create a decoder on the current CUDA device.  Every later call that launches work or reads the
+ * handle's device memory (decode, decode_bands, decode_host, sync, profile_read, the debug runs)
+ * must be made with that device current; otherwise it returns VAEDEC_ERR_INVALID_ARG and launches
+ * nothing.  vaedec_destroy switches to the handle's device to free it and restores the caller's.  Copies and repacks every weight
  * (host memory, any of the two dtypes) into device layouts owned by the handle and
  * allocates the workspace for config->max_latent.  Synchronous.
  * Errors: INVALID_ARG (missing/extra-shaped weight, bad config), UNSUPPORTED

@@ -240,10 +240,30 @@ def band_attention(q, k, vt, out, grid_h: int, grid_w: int, n_bands: int, work, 
     """
     lib = load_library()
     torch = _torch()
+    # the kernel reads and writes through raw pointers: every extent is checked here first
+    if q.dim() != 3:
+        raise ValueError("q must be [F, ntok, C]")
     F, ntok, C = (int(v) for v in q.shape)
+    if ntok != int(grid_h) * int(grid_w):
+        raise ValueError(f"q has {ntok} tokens per frame, the grid {grid_h} x {grid_w} has {int(grid_h) * int(grid_w)}")
+    dev = q.device
+    for name, t, shape in (("q", q, (F, ntok, C)), ("k", k, (F, ntok, C)), ("vt", vt, (F, C, ntok)),
+                           ("out", out, (F, ntok, C))):
+        if not t.is_cuda or t.device != dev or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor on {dev}")
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+    if not status.is_cuda or status.device != dev or status.dtype != torch.int32 or status.numel() < 1:
+        raise ValueError(f"status must be an int32 tensor on {dev}")
+    need = band_attention_work_bytes(F, grid_h, grid_w, C)
+    if work is not None:
+        if not work.is_cuda or work.device != dev or not work.is_contiguous():
+            raise ValueError(f"work must be a contiguous tensor on {dev}")
+    wb = work.numel() * work.element_size() if work is not None else 0
+    if wb < need:
+        raise ValueError(f"work holds {wb} bytes, the key splits need {need}")
     st = torch.cuda.current_stream() if stream is None else stream
     wp = work.data_ptr() if work is not None else None
-    wb = work.numel() * work.element_size() if work is not None else 0
     _check(lib, lib.vaedec_band_attention(q.data_ptr(), k.data_ptr(), vt.data_ptr(), out.data_ptr(), F, int(grid_h),
                                           int(grid_w), C, int(n_bands), wp, wb, status.data_ptr(),
                                           int(st.cuda_stream)))
@@ -278,6 +298,7 @@ class Decoder:
         handle = ctypes.c_void_p()
         _check(self.lib, self.lib.vaedec_create(ctypes.byref(cfg), arr, len(weights), ctypes.byref(handle)))
         self._h = handle
+        self.device = _torch().cuda.current_device()   # the device the handle's memory lives on
         del keep
 
     # ------------------------------------------------------------------ basics
@@ -328,11 +349,14 @@ class Decoder:
         torch = _torch()
         if not latent.is_cuda or latent.dtype != self.torch_dtype or not latent.is_contiguous():
             raise ValueError("latent must be a contiguous CUDA tensor in the model dtype")
+        if latent.device.index != self.device:
+            raise ValueError(f"latent is on {latent.device}, the decoder on cuda:{self.device}")
         oshape = self.output_shape(latent.shape)
         if out is None:
             out = torch.empty(oshape, dtype=self.torch_dtype, device=latent.device)
-        elif tuple(out.shape) != oshape or out.dtype != self.torch_dtype or not out.is_contiguous():
-            raise ValueError("out has the wrong shape, dtype or layout")
+        elif (not out.is_cuda or out.device != latent.device or tuple(out.shape) != oshape or
+              out.dtype != self.torch_dtype or not out.is_contiguous()):
+            raise ValueError(f"out must be a contiguous {self.torch_dtype} tensor of shape {oshape} on {latent.device}")
         if axis == "height":
             _check(self.lib, self.lib.vaedec_decode(self._h, latent.data_ptr(), _shape_arg(latent.shape),
                                                     latent.dim(), out.data_ptr(), int(n_bands),
@@ -345,6 +369,12 @@ class Decoder:
 
     def decode_host(self, latent_host, out_host, n_bands: int, stream=None):
         """Host buffers in, host buffers out (copies inside the call; synchronous)."""
+        for name, t in (("latent_host", latent_host), ("out_host", out_host)):
+            if t.is_cuda or t.dtype != self.torch_dtype or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous host tensor of dtype {self.torch_dtype}")
+        oshape = self.output_shape(latent_host.shape)
+        if tuple(out_host.shape) != oshape:
+            raise ValueError(f"out_host has shape {tuple(out_host.shape)}, expected {oshape}")
         _check(self.lib, self.lib.vaedec_decode_host(self._h, latent_host.data_ptr(),
                                                      _shape_arg(latent_host.shape), latent_host.dim(),
                                                      out_host.data_ptr(), int(n_bands),

@@ -147,6 +147,7 @@ void* const kDryOut = &kDryOutTag;
 
 struct vaedec {
   vaedec_config cfg{};
+  int device = 0;        // the CUDA device current at create: weights, workspace and launches live there
   int dtype = kBF16;
   size_t es = 2;
   std::map<std::string, DevConv> conv;
@@ -1484,6 +1485,19 @@ size_t layout_workspace(vaedec* h, const Plan& plan) {
 void vd::record_last_error(const std::string& message) { g_err = message; }
 
 // ====================================================================== C ABI
+// Calls that launch kernels or touch the handle's device memory need the handle's device to be the
+// current one: kernels launched on another device would dereference this device's pointers.
+vaedec_status check_device(const vaedec* h) {
+  int dev = -1;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "current device");
+  if (dev != h->device)
+    return fail(VAEDEC_ERR_INVALID_ARG, "the current CUDA device (" + std::to_string(dev) +
+                                            ") is not the one the handle was created on (" +
+                                            std::to_string(h->device) + ")");
+  return VAEDEC_OK;
+}
+
 extern "C" {
 
 const char* vaedec_last_error(void) { return g_err.c_str(); }
@@ -1505,6 +1519,10 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
     delete h;
     return st;
   };
+  {
+    const cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "current device"));
+  }
 
   std::vector<Need> needs;
   if (config->family == VAEDEC_FAMILY_KL2D)
@@ -1703,8 +1721,14 @@ vaedec_status vaedec_create(const vaedec_config* config, const vaedec_tensor* we
 
 void vaedec_destroy(vaedec_t* h) {
   if (h == nullptr) return;
+  // the handle's memory is freed on its own device; the caller's current device is restored
+  const int hd = h->device;
+  int cur = -1;
+  const bool other = cudaGetDevice(&cur) == cudaSuccess && cur != hd;
+  if (other) cudaSetDevice(hd);
   cudaDeviceSynchronize();
   delete h;
+  if (other) cudaSetDevice(cur);
 }
 
 vaedec_status vaedec_output_shape(const vaedec_t* h, const int64_t* shape, int ndim, int64_t* out_shape) {
@@ -1808,7 +1832,9 @@ vaedec_status vaedec_workspace_bytes(const vaedec_t* h, size_t* bytes) {
 vaedec_status vaedec_decode(vaedec_t* h, const void* latent, const int64_t* shape, int ndim, void* out, int n_bands,
                             void* stream) {
   if (h == nullptr || latent == nullptr || out == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
-  vaedec_status s = check_latent(h, shape, ndim, n_bands);
+  vaedec_status s = check_device(h);
+  if (s != VAEDEC_OK) return s;
+  s = check_latent(h, shape, ndim, n_bands);
   if (s != VAEDEC_OK) return s;
   Walker w(h, static_cast<cudaStream_t>(stream), false, n_bands);
   return w.run(latent, shape, ndim, out);
@@ -1826,7 +1852,9 @@ vaedec_status vaedec_decode_bands(vaedec_t* h, const void* latent, const int64_t
     return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
   if (ndim != 4 && ndim != 5) return fail(VAEDEC_ERR_INVALID_ARG, "latent ndim must be 4 or 5");
   int ax = 0;
-  vaedec_status s = resolve_band_axis(shape[ndim - 2] * h->patch, shape[ndim - 1] * h->patch, n_bands, axis, &ax);
+  vaedec_status s = check_device(h);
+  if (s != VAEDEC_OK) return s;
+  s = resolve_band_axis(shape[ndim - 2] * h->patch, shape[ndim - 1] * h->patch, n_bands, axis, &ax);
   if (s != VAEDEC_OK) return s;
   s = check_latent(h, shape, ndim, n_bands, ax);
   if (s != VAEDEC_OK) return s;
@@ -1836,6 +1864,8 @@ vaedec_status vaedec_decode_bands(vaedec_t* h, const void* latent, const int64_t
 
 vaedec_status vaedec_sync(vaedec_t* h, void* stream) {
   if (h == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL handle");
+  vaedec_status s = check_device(h);
+  if (s != VAEDEC_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
@@ -1852,7 +1882,9 @@ vaedec_status vaedec_sync(vaedec_t* h, void* stream) {
 vaedec_status vaedec_decode_host(vaedec_t* h, const void* latent_host, const int64_t* shape, int ndim, void* out_host,
                                  int n_bands, void* stream) {
   if (h == nullptr || latent_host == nullptr || out_host == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
-  vaedec_status s = check_latent(h, shape, ndim, n_bands);
+  vaedec_status s = check_device(h);
+  if (s != VAEDEC_OK) return s;
+  s = check_latent(h, shape, ndim, n_bands);
   if (s != VAEDEC_OK) return s;
   int64_t oshape[5];
   s = vaedec_output_shape(h, shape, ndim, oshape);
@@ -1944,6 +1976,8 @@ vaedec_status vaedec_debug_set_wait_limit(uint64_t ns) {
 
 vaedec_status vaedec_debug_wait_probe(vaedec_t* h, void* stream) {
   if (h == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL handle");
+  const vaedec_status s = check_device(h);
+  if (s != VAEDEC_OK) return s;
   cudaError_t e = launch_wait_probe(h->status, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(VAEDEC_ERR_CUDA, std::string("wait probe: ") + cudaGetErrorString(e));
   return VAEDEC_OK;
@@ -1964,6 +1998,8 @@ vaedec_status vaedec_profile_enable(vaedec_t* h, int enable) {
 
 vaedec_status vaedec_profile_read(vaedec_t* h, float* ms, int max_ops, int* n_ops) {
   if (h == nullptr || n_ops == nullptr || (ms == nullptr && max_ops > 0)) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
+  const vaedec_status s = check_device(h);
+  if (s != VAEDEC_OK) return s;
   *n_ops = h->prof_ops;
   for (int i = 0; i < h->prof_ops && i < max_ops; ++i) {
     cudaError_t e = cudaEventSynchronize(h->prof_ev[2 * i + 1]);
@@ -2005,7 +2041,9 @@ vaedec_status vaedec_debug_run_until(vaedec_t* h, const void* latent, const int6
                                      int op, void* dst_in, size_t in_bytes, void* dst_aux, size_t aux_bytes,
                                      void* dst_out, size_t out_bytes, void* stream) {
   if (h == nullptr || latent == nullptr) return fail(VAEDEC_ERR_INVALID_ARG, "NULL argument");
-  vaedec_status s = check_latent(h, shape, ndim, n_bands);
+  vaedec_status s = check_device(h);
+  if (s != VAEDEC_OK) return s;
+  s = check_latent(h, shape, ndim, n_bands);
   if (s != VAEDEC_OK) return s;
   if (op < 0) return fail(VAEDEC_ERR_INVALID_ARG, "op index out of range");
   // the final op writes the caller's output: route it to a scratch output buffer

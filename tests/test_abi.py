@@ -190,3 +190,19 @@ def test_workspace_plan_rejects_bad_configs(lib):
     cfg = rbl.make_config(synth.WAN, "bf16", (1, 5, 60, 104))
     assert lib.vaedec_plan_workspace(ctypes.byref(cfg), ctypes.byref(n), None, None) == 0
     assert n.value > 0
+
+
+def test_band_attention_binding_checks_operands_without_cuda():
+    """The binding rejects operands it cannot pass safely as raw pointers (host tensors, wrong shapes
+    or dtypes) before the library sees them."""
+    torch = pytest.importorskip("torch")
+    import row_band_layerwise_gb300 as rbl
+    q = torch.zeros((1, 64, 128), dtype=torch.bfloat16)
+    vt = torch.zeros((1, 128, 64), dtype=torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        rbl.band_attention(q, q, vt, q, 8, 8, 1, None, st)            # host tensors
+    with pytest.raises(ValueError):
+        rbl.band_attention(q[0], q, vt, q, 8, 8, 1, None, st)         # q not [F, ntok, C]
+    with pytest.raises(ValueError):
+        rbl.band_attention(q, q, vt, q, 8, 7, 1, None, st)            # tokens do not fill the grid

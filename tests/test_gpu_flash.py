@@ -101,16 +101,32 @@ def test_fused_attention_rising_maximum():
 def test_fused_attention_rejects_bad_arguments():
     torch, rbl = require_gpu()
     dev = torch.device("cuda")
-    t = torch.zeros((1, 64, 512), dtype=torch.bfloat16, device=dev)
+
+    def qkv(ntok, C):
+        t = torch.zeros((1, ntok, C), dtype=torch.bfloat16, device=dev)
+        return t, torch.zeros((1, C, ntok), dtype=torch.bfloat16, device=dev)
+
     st = torch.zeros(1, dtype=torch.int32, device=dev)
+    t, tv = qkv(64, 512)
     with pytest.raises(rbl.VaedecError):
-        rbl.band_attention(t, t, t, t, 8, 8, 9, None, st)        # more bands than grid rows
-    t2 = torch.zeros((1, 64, 96), dtype=torch.bfloat16, device=dev)
+        rbl.band_attention(t, t, tv, t, 8, 8, 9, None, st)        # more bands than grid rows
+    t2, tv2 = qkv(64, 96)
     with pytest.raises(rbl.VaedecError):
-        rbl.band_attention(t2, t2, t2, t2, 8, 8, 1, None, st)    # C not a multiple of 128
-    t3 = torch.zeros((1, 64, 1024), dtype=torch.bfloat16, device=dev)
+        rbl.band_attention(t2, t2, tv2, t2, 8, 8, 1, None, st)    # C not a multiple of 128
+    t3, tv3 = qkv(64, 1024)
     with pytest.raises(rbl.VaedecError):
-        rbl.band_attention(t3, t3, t3, t3, 8, 8, 1, None, st)    # C above 512
-    t4 = torch.zeros((1, 4400, 384), dtype=torch.bfloat16, device=dev)
-    with pytest.raises(rbl.VaedecError):
-        rbl.band_attention(t4, t4, t4, t4, 50, 88, 1, None, st)  # key splits need a work buffer
+        rbl.band_attention(t3, t3, tv3, t3, 8, 8, 1, None, st)    # C above 512
+    t4, tv4 = qkv(4400, 384)
+    with pytest.raises(ValueError):
+        rbl.band_attention(t4, t4, tv4, t4, 50, 88, 1, None, st)  # key splits need a work buffer
+    small = torch.empty(16, dtype=torch.uint8, device=dev)
+    with pytest.raises(ValueError):
+        rbl.band_attention(t4, t4, tv4, t4, 50, 88, 1, small, st)  # ... of at least the stated size
+    with pytest.raises(ValueError):
+        rbl.band_attention(t, t, t, t, 8, 8, 1, None, st)          # V^T must be [F, C, ntok]
+    with pytest.raises(ValueError):
+        rbl.band_attention(t, t, tv, t, 8, 9, 1, None, st)         # tokens must fill the grid
+    with pytest.raises(ValueError):
+        rbl.band_attention(t, t, tv, t.cpu(), 8, 8, 1, None, st)   # every operand on the device
+    with pytest.raises(ValueError):
+        rbl.band_attention(t, t, tv, t, 8, 8, 1, None, st.float())  # status is int32

@@ -41,3 +41,28 @@ def test_host_decode_matches_device_decode(arch_name, shapes, max_latent):
     _check(torch, dec, *shapes[0], seed=3)
     dec.profile(False)
     dec.sync()
+
+
+def test_decode_checks_its_buffers():
+    """Output buffers of the wrong place, shape or dtype are refused before any copy or launch (a host
+    buffer too small for the output would otherwise be overrun by the download)."""
+    torch, rbl = require_gpu()
+    shape = (1, 16, 8, 8)
+    W = synth.make_weights(synth.KL_ZIMAGE, "bf16")
+    dec = rbl.Decoder(synth.KL_ZIMAGE, W, "bf16", (1, 1, 8, 8))
+    z = torch.from_numpy(synth.make_latent(shape, "bf16")).to(torch.bfloat16)
+    oshape = dec.output_shape(shape)
+    zd = z.cuda()
+    with pytest.raises(ValueError):
+        dec.decode(zd, 1, out=torch.empty(oshape, dtype=torch.bfloat16))                  # host output
+    with pytest.raises(ValueError):
+        dec.decode(zd, 1, out=torch.empty((1, 3, 64, 32), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):
+        dec.decode(zd, 1, out=torch.empty(oshape, dtype=torch.float32, device="cuda"))
+    with pytest.raises(ValueError):
+        dec.decode_host(z, torch.empty((1, 3, 64, 32), dtype=torch.bfloat16), 1)          # too small
+    with pytest.raises(ValueError):
+        dec.decode_host(zd, torch.empty(oshape, dtype=torch.bfloat16), 1)                 # device latent
+    out = dec.decode_host(z, torch.empty(oshape, dtype=torch.bfloat16), 1)
+    assert tuple(out.shape) == tuple(oshape)
+    dec.close()
