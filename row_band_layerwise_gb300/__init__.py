@@ -421,8 +421,17 @@ class Decoder:
 
     def run_until(self, latent, n_bands: int, op: int, dst_in=None, dst_aux=None, dst_out=None, stream=None):
         """Run ops [0, op] and copy that op's input / aux / output activations into the given device tensors."""
+        if not latent.is_cuda or latent.dtype != self.torch_dtype or not latent.is_contiguous():
+            raise ValueError("latent must be a contiguous CUDA tensor in the model dtype")
+        if latent.device.index != self.device:
+            raise ValueError(f"latent is on {latent.device}, the decoder on cuda:{self.device}")
+
         def ptr_size(t):
-            return (0, 0) if t is None else (t.data_ptr(), t.numel() * t.element_size())
+            if t is None:
+                return (0, 0)
+            if not t.is_cuda or t.device != latent.device or not t.is_contiguous():
+                raise ValueError(f"debug buffers must be contiguous tensors on {latent.device}")
+            return (t.data_ptr(), t.numel() * t.element_size())
         pi, si = ptr_size(dst_in)
         pa, sa = ptr_size(dst_aux)
         po, so = ptr_size(dst_out)
