@@ -44,7 +44,7 @@ constexpr int kPipeBytesT = 212 * 1024;
 constexpr int kStageOutBytes = 16 * 32 * 4;   // one epilogue warp's [16 px][32 ch] fp32 staging
 constexpr int kResBufs = 3;                    // staging buffers per warp when the residual comes by TMA
 constexpr int kStageOut2Bytes = 16 * 32 * 2;   // one epilogue warp's [16 px][32 ch] bf16 copy staging
-constexpr int kMaxDynSmemT = 227 * 1024;
+constexpr int kMaxDynSmemT = 227 * 1024 - 512;   // per-CTA limit, less room for the static barriers (336 B)
 
 struct HaloTParams {
   CUtensorMap tmX;               // activations 5D (Cin, W, H, T, B), box (BK, half, 1, 1, 1)
